@@ -1,0 +1,147 @@
+/*
+ * fp4moe.h -- C ABI of libfp4moe.so: the quantized MoE expert projection on GB300 (sm_103a).
+ *
+ * The operation (memra-engine 0.98.0, src/bin/dsv4_native_gemm_gate.rs):
+ *   1. fn quant_rows: every activation row is cut into groups of 128; per group
+ *      amax = max(max|x|, 1e-4), s = pow2_ceil(amax * f32(1/448)) and
+ *      code = e4m3(clamp(x / s, -448, 448)) (round to nearest even, sign kept).
+ *   2. fn f64_ref / fn mirror_gemm: out[r][c] = sum over weight groups j of
+ *      (sum_{i<gs} e4m3(code) * E2M1(nibble)) * (ws_j * s_{r, j*gs/128}), f32 accumulation,
+ *      where NVFP4 (gs = 16) has ws = f32(e4m3(scale byte) * scale2) and MXFP4 (gs = 32)
+ *      has ws = 2^(e8m0 byte - 127). Weight rows hold k/2 bytes of nibble pairs, the low
+ *      nibble being the even k (struct ExpertRaw; the nibble split in mirror_gemm).
+ *
+ * Conventions for every call:
+ *   - All array arguments are device pointers on the current CUDA device, row-major and
+ *     contiguous, owned by the caller; the library allocates nothing and never frees.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are stream-ordered
+ *     and asynchronous: they enqueue kernels and return without synchronising.
+ *   - Sizes are elements unless named *_bytes. k must be a positive multiple of 128.
+ *   - Every pointer must be 16-byte aligned (the kernels use 128-bit accesses).
+ *   - The return value is an fp4_status; a non-zero status means nothing was enqueued.
+ *   - Inputs must be finite: non-finite activations give unspecified codes (no crash).
+ *   - Device-side checks (CSR offsets, row ids) cannot return a status without a sync;
+ *     they set bits in a per-device error word read by fp4_get_device_error().
+ */
+#ifndef FP4MOE_H
+#define FP4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP4_OK = 0,
+    FP4_ERR_ARG = -1,       /* null required pointer, unknown recipe, negative size */
+    FP4_ERR_SHAPE = -2,     /* k % 128 != 0, k or n < 1, sizes past the supported range */
+    FP4_ERR_ALIGN = -3,     /* a pointer that is not 16-byte aligned */
+    FP4_ERR_LAUNCH = -4,    /* the CUDA runtime refused a launch (see fp4_last_error) */
+    FP4_ERR_DEVICE = -5,    /* returned by fp4_get_device_error when device checks failed */
+    FP4_ERR_WORKSPACE = -6  /* workspace missing or below fp4_grouped_workspace_size() */
+} fp4_status;
+
+typedef enum { FP4_NVFP4 = 0, FP4_MXFP4 = 1 } fp4_recipe; /* matches the pages' kind 0/1 */
+
+/* Bits of the device error word (fp4_get_device_error). */
+enum {
+    FP4_DEVERR_OFFSETS = 1, /* offsets not non-decreasing from 0 to total_rows */
+    FP4_DEVERR_ROW_ID = 2,  /* a row id outside [0, num_tokens) */
+    FP4_DEVERR_TIMEOUT = 4  /* a pipeline wait gave up after its iteration limit */
+};
+
+/* Kernel paths (fp4_gemm_path / fp4_force_path). */
+enum {
+    FP4_PATH_AUTO = 0,   /* library choice by shape (fp4_gemm_path) */
+    FP4_PATH_STREAM = 1, /* CUDA-core weight-streaming kernel with fused act-quant prologue */
+    FP4_PATH_TC = 2      /* tcgen05 tensor-core kernel over a quantized-activation workspace */
+};
+
+/*
+ * act_quant_fp8 -- stage 1 alone (fn quant_rows of dsv4_native_gemm_gate.rs).
+ *   x      [rows, k] f32 in
+ *   codes  [rows, k] e4m3 bytes out
+ *   scales [rows, k/128] f32 out (powers of two)
+ * Bit-exact with the oracle's act_quant. rows == 0 is a no-op returning FP4_OK.
+ */
+int act_quant_fp8(const float *x, uint8_t *codes, float *scales, int64_t rows, int64_t k,
+                  void *stream);
+
+/*
+ * fp4_expert_gemm -- one expert, act_quant fused into the GEMM:
+ * out[g, n] = quant(x)[g, k] . W[n, k]^T (fn f64_ref / fn mirror_gemm of
+ * dsv4_native_gemm_gate.rs, with the activation quantized on device first).
+ *   x          [g, k] f32 activations
+ *   w          [n, k/2] nibble pairs (low nibble = even k)
+ *   wscale     [n, k/16] e4m3 bytes (NVFP4) or [n, k/32] e8m0 bytes (MXFP4)
+ *   scale2     per-tensor f32 factor (NVFP4; ignored for MXFP4)
+ *   out        [g, n] f32
+ *   codes_out  nullable [g, k] e4m3 bytes: the quantized activations (as act_quant_fp8)
+ *   scales_out nullable [g, k/128] f32
+ *   workspace  nullable; with at least fp4_grouped_workspace_size(g, g, n, k, recipe)
+ *              bytes the tensor-core path may be used, otherwise the streaming path.
+ */
+int fp4_expert_gemm(const float *x, const uint8_t *w, const uint8_t *wscale, float scale2,
+                    int recipe, float *out, int64_t g, int64_t n, int64_t k, uint8_t *codes_out,
+                    float *scales_out, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes fp4_grouped_expert_gemm (and fp4_expert_gemm) needs for this shape. */
+size_t fp4_grouped_workspace_size(int64_t num_tokens, int64_t total_rows, int64_t n, int64_t k,
+                                  int recipe);
+
+/*
+ * fp4_grouped_expert_gemm -- all experts of one projection in one call. Routed row p
+ * (0 <= p < total_rows) reads activation row x[row_ids[p]] (x[p] when row_ids is NULL)
+ * and belongs to the expert e with offsets[e] <= p < offsets[e+1] (CSR offsets, as the
+ * grouped MoE GEMM section of memra-engine 0.71.0 src/bin/kernel_check.rs builds them).
+ *   x         [num_tokens, k] f32
+ *   row_ids   nullable [total_rows] int32 (device)
+ *   offsets   [num_experts + 1] int32 (device): offsets[0] = 0, non-decreasing,
+ *             offsets[num_experts] = total_rows
+ *   w         [num_experts, n, k/2] nibble pairs; expert e's block starts at e*n*k/2
+ *   wscale    [num_experts, n, k/gs] scale bytes
+ *   scale2    [num_experts] f32 (device; NVFP4; may be NULL for MXFP4)
+ *   out       [total_rows, n] f32
+ *   workspace at least fp4_grouped_workspace_size(...) bytes (may be NULL if that is 0)
+ * Experts with no rows cost nothing but a CTA exit. Offsets or row ids that fail the
+ * device checks set fp4_get_device_error bits; their rows are skipped (out untouched).
+ */
+int fp4_grouped_expert_gemm(const float *x, int64_t num_tokens, const int32_t *row_ids,
+                            const int32_t *offsets, int num_experts, int64_t total_rows,
+                            const uint8_t *w, const uint8_t *wscale, const float *scale2,
+                            int recipe, float *out, int64_t n, int64_t k, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/* Which path a grouped call of this shape takes (never FP4_PATH_AUTO). */
+int fp4_gemm_path(int64_t total_rows, int num_experts, int64_t n, int64_t k, int recipe,
+                  int have_workspace);
+
+/*
+ * The n_ops of the per-output error model |out - f64 reference| <= n_ops * 2^-24 *
+ * sum|scaled products| (dsv4_native_gemm_gate.rs, header comment and the f64 check)
+ * for `path` at this recipe and k. Derived from the kernel's summation structure.
+ */
+double fp4_error_ops(int path, int recipe, int64_t k);
+
+/* Test hook: force a path for later calls (FP4_PATH_AUTO restores the choice by shape). */
+void fp4_force_path(int path);
+
+/*
+ * Synchronises `stream`, then returns FP4_OK or FP4_ERR_DEVICE and stores the device
+ * error word (FP4_DEVERR_* bits) of the current device in *bits (nullable), clearing it.
+ */
+int fp4_get_device_error(void *stream, unsigned *bits);
+
+/* Text of the last CUDA error a call met on this thread ("" if none). */
+const char *fp4_last_error(void);
+
+/* Name of a status code. */
+const char *fp4_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP4MOE_H */

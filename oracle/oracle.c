@@ -1,0 +1,271 @@
+/*
+ * oracle.c -- plain, slow CPU oracle for the quantized MoE expert projection.
+ *
+ * TEST INFRASTRUCTURE. This file is the reference the CUDA path is checked against.
+ * Only the tests, the smoke check and the benchmark's CPU-baseline leg load it; the
+ * library's product path never includes, links or calls anything here, and this file
+ * includes nothing from the library.
+ *
+ * What it follows (docs.rs source pages of the memra-engine crate):
+ *   [Q]  memra-engine 0.98.0, src/bin/dsv4_native_gemm_gate.rs, fn quant_rows
+ *        (per-row, per-128 FP8-E4M3 activation quantisation, all in f32).
+ *   [R]  same page, fn f64_ref (f64-ordered reference of the quantised GEMM plus the
+ *        per-output sum of |scaled products| used by the error model).
+ *   [D]  memra-engine 0.71.0, src/bin/kernel_check.rs, the F8-E4M3 MMVQ section's CPU
+ *        e4m3 decode closure (sign / 4-bit exponent, bias 7 / 3-bit mantissa,
+ *        exponent 0 -> subnormal, exponent 15 with mantissa 7 -> NaN).
+ *   [S]  same page as [Q]: struct ExpertRaw (nibble pairs [n,k/2], low nibble = even k;
+ *        e4m3 scale per 16 (NVFP4) or e8m0 scale per 32 (MXFP4); f32 scale2 for NVFP4).
+ *
+ * Readings where the pages import a helper without printing it (each is a plain
+ * definition written out here):
+ *   pow2_ceil(x)       smallest power of two >= x (x > 0, finite).
+ *   f32_to_fp8_e4m3(v) nearest finite e4m3fn value, ties to the even code, sign kept
+ *                      (so -0.0 and negative values that round to zero give 0x80);
+ *                      callers clamp to [-448, 448] first, as [Q] does.
+ *   E2M1[c]            the OCP E2M1 element: 1 sign, 2 exponent bits (bias 1),
+ *                      1 mantissa bit, exponent 0 subnormal; no inf/NaN.
+ *   e8m0_to_f32(e)     2^(e-127); e = 255 is NaN.
+ * All four minifloat decoders go through one generic sign/exponent/mantissa decoder.
+ *
+ * Precision: [Q] fixes f32 arithmetic (amax, amax*inv, v/s, clamp) and it is kept in
+ * f32 here; [R] is f64 with the per-group weight scale first rounded in f32, kept too.
+ * Build with -O2 -ffp-contract=off (no fused multiply-add contraction).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "oracle.h"
+
+/* ------------------------------------------------------------------ minifloats */
+
+/* Decode `bits` as a sign / ebits exponent / mbits mantissa minifloat with the given
+ * bias; exponent field 0 is subnormal. No special values here (callers add them). */
+static double minifloat_decode(unsigned bits, int ebits, int mbits, int bias)
+{
+    const unsigned sign = (bits >> (ebits + mbits)) & 1u;
+    const unsigned e = (bits >> mbits) & ((1u << ebits) - 1u);
+    const unsigned m = bits & ((1u << mbits) - 1u);
+    double mag;
+    if (e == 0)
+        mag = ldexp((double)m, 1 - bias - mbits);
+    else
+        mag = ldexp((double)((1u << mbits) | m), (int)e - bias - mbits);
+    return sign ? -mag : mag;
+}
+
+double orc_e4m3_decode(uint8_t b)
+{
+    /* [D]: exponent 15 with mantissa 7 is NaN; no infinities (e4m3fn). */
+    if ((b & 0x7Fu) == 0x7Fu)
+        return NAN;
+    return minifloat_decode(b, 4, 3, 7);
+}
+
+double orc_e2m1_decode(uint8_t nib)
+{
+    return minifloat_decode(nib & 0x0Fu, 2, 1, 1);
+}
+
+double orc_e8m0_decode(uint8_t e)
+{
+    if (e == 0xFFu)
+        return NAN;
+    return ldexp(1.0, (int)e - 127);
+}
+
+/* Decode tables, filled once from the decoders above (speed only). */
+static double g_e4m3[256];
+static double g_e2m1[16];
+static double g_grid[127]; /* non-negative finite e4m3 values, codes 0x00..0x7E */
+static int g_init = 0;
+
+static void init_tables(void)
+{
+    if (g_init)
+        return;
+    for (int c = 0; c < 256; ++c)
+        g_e4m3[c] = orc_e4m3_decode((uint8_t)c);
+    for (int c = 0; c < 16; ++c)
+        g_e2m1[c] = orc_e2m1_decode((uint8_t)c);
+    for (int c = 0; c < 127; ++c)
+        g_grid[c] = g_e4m3[c];
+    g_init = 1;
+}
+
+uint8_t orc_e4m3_encode(float v)
+{
+    /* Nearest value of the finite e4m3 grid, ties to the even code. Codes 0x00..0x7E
+     * are strictly increasing in value, so a bisection finds the bracketing pair. */
+    init_tables();
+    const int neg = signbit(v) ? 1 : 0;
+    const double a = fabs((double)v);
+    int c;
+    if (a >= g_grid[126]) {
+        c = 126; /* only reached at |v| = 448 inside the contract (inputs are clamped) */
+    } else {
+        int lo = 0, hi = 126; /* invariant: g_grid[lo] <= a < g_grid[hi] */
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) / 2;
+            if (g_grid[mid] <= a)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const double dlo = a - g_grid[lo];
+        const double dhi = g_grid[hi] - a;
+        if (dhi < dlo || (dhi == dlo && (hi & 1) == 0))
+            c = hi;
+        else
+            c = lo;
+    }
+    return (uint8_t)(c | (neg ? 0x80 : 0x00));
+}
+
+float orc_pow2_ceil(float x)
+{
+    /* Smallest power of two >= x, for finite x > 0: x = f * 2^e with f in [0.5, 1). */
+    int e;
+    const double f = frexp((double)x, &e);
+    if (f == 0.5)
+        return x;
+    return (float)ldexp(1.0, e);
+}
+
+/* ------------------------------------------------------------------ act_quant [Q] */
+
+void orc_act_quant(const float *x, int64_t rows, int64_t k, uint8_t *codes, float *scales)
+{
+    init_tables();
+    const int64_t kq = k / 128;
+    const float inv = (float)(1.0 / 448.0);
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t g = 0; g < kq; ++g) {
+            const float *grp = x + r * k + g * 128;
+            float amax = 0.0f;
+            for (int i = 0; i < 128; ++i) {
+                const float a = fabsf(grp[i]);
+                if (a > amax)
+                    amax = a;
+            }
+            if (amax < 1e-4f)
+                amax = 1e-4f;
+            const float t = amax * inv;
+            const float s = orc_pow2_ceil(t);
+            scales[r * kq + g] = s;
+            for (int i = 0; i < 128; ++i) {
+                float q = grp[i] / s;
+                if (q < -448.0f)
+                    q = -448.0f;
+                if (q > 448.0f)
+                    q = 448.0f;
+                codes[r * k + g * 128 + i] = orc_e4m3_encode(q);
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ GEMM reference [R] */
+
+static int group_size(int recipe)
+{
+    return recipe == ORC_NVFP4 ? 16 : 32;
+}
+
+/* Per-group weight scale `ws` exactly as [R] forms it: NVFP4 rounds e4m3 * scale2 in f32. */
+static float weight_scale(int recipe, uint8_t scbyte, float scale2)
+{
+    if (recipe == ORC_NVFP4)
+        return (float)g_e4m3[scbyte] * scale2;
+    return (float)orc_e8m0_decode(scbyte);
+}
+
+/* One output of [R]: activation row `arow` (codes) with its per-128 scales `asrow`
+ * against weight column `col` of one expert. */
+static void ref_one(const uint8_t *arow, const float *asrow, const uint8_t *w, const uint8_t *sc,
+                    float scale2, int recipe, int64_t k, int64_t col, double *out, double *absp)
+{
+    const int gs = group_size(recipe);
+    const int64_t ngroups = k / gs;
+    const uint8_t *wrow = w + col * (k / 2);
+    const uint8_t *srow = sc + col * ngroups;
+    double acc = 0.0, aabs = 0.0;
+    for (int64_t j = 0; j < ngroups; ++j) {
+        const double ws = (double)weight_scale(recipe, srow[j], scale2);
+        const double scl = ws * (double)asrow[(j * gs) / 128];
+        for (int i = 0; i < gs; ++i) {
+            const int64_t kk = j * gs + i;
+            const uint8_t byte = wrow[kk >> 1];
+            const uint8_t nib = (kk & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0x0F);
+            const double p = g_e4m3[arow[kk]] * g_e2m1[nib] * scl;
+            acc += p;
+            aabs += fabs(p);
+        }
+    }
+    *out = acc;
+    *absp = aabs;
+}
+
+void orc_gemm_ref(const uint8_t *codes, const float *scales, const uint8_t *w, const uint8_t *sc,
+                  float scale2, int recipe, int64_t g, int64_t n, int64_t k, double *out,
+                  double *absp)
+{
+    init_tables();
+    const int64_t kq = k / 128;
+    for (int64_t row = 0; row < g; ++row)
+        for (int64_t col = 0; col < n; ++col)
+            ref_one(codes + row * k, scales + row * kq, w, sc, scale2, recipe, k, col,
+                    out + row * n + col, absp + row * n + col);
+}
+
+/* ------------------------------------------------------------------ grouped, sampled */
+
+/* Expert owning routed row p under CSR offsets (offsets[e] <= p < offsets[e+1]). */
+static int expert_of(const int32_t *offsets, int num_experts, int64_t p)
+{
+    for (int e = 0; e < num_experts; ++e)
+        if (p >= offsets[e] && p < offsets[e + 1])
+            return e;
+    return -1;
+}
+
+int orc_grouped_ref_sampled(const float *x, int64_t T, int64_t k, const int32_t *row_ids,
+                            const int32_t *offsets, int num_experts, int64_t P, const uint8_t *w,
+                            const uint8_t *sc, const float *scale2, int recipe, int64_t n,
+                            const int64_t *sample_p, const int64_t *sample_col, int64_t ns,
+                            double *out, double *absp, uint8_t *tmp_codes, float *tmp_scales)
+{
+    /* Routed row p is x[row_ids[p]] (or x[p] without row_ids), quantised by [Q] and
+     * multiplied by [R] against the weights of the expert whose offset range holds p.
+     * tmp_codes [k] and tmp_scales [k/128] are caller scratch. Returns 0, or -1 on a
+     * row id / offset outside its range. */
+    init_tables();
+    const int gs = group_size(recipe);
+    const int64_t wbytes = n * (k / 2);
+    const int64_t sbytes = n * (k / gs);
+    int64_t cur_p = -1;
+    int cur_e = -1;
+    for (int64_t s = 0; s < ns; ++s) {
+        const int64_t p = sample_p[s];
+        if (p < 0 || p >= P)
+            return -1;
+        if (p != cur_p) {
+            const int64_t t = row_ids ? (int64_t)row_ids[p] : p;
+            if (t < 0 || t >= T)
+                return -1;
+            cur_e = expert_of(offsets, num_experts, p);
+            if (cur_e < 0)
+                return -1;
+            orc_act_quant(x + t * k, 1, k, tmp_codes, tmp_scales);
+            cur_p = p;
+        }
+        const int64_t col = sample_col[s];
+        if (col < 0 || col >= n)
+            return -1;
+        const float s2 = (recipe == ORC_NVFP4) ? scale2[cur_e] : 0.0f;
+        ref_one(tmp_codes, tmp_scales, w + (int64_t)cur_e * wbytes, sc + (int64_t)cur_e * sbytes,
+                s2, recipe, k, col, out + s, absp + s);
+    }
+    return 0;
+}

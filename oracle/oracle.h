@@ -1,0 +1,41 @@
+/*
+ * oracle.h -- declarations of the CPU oracle (test infrastructure only; see oracle.c).
+ * Nothing in the CUDA library includes this header.
+ */
+#ifndef FP4MOE_ORACLE_H
+#define FP4MOE_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORC_NVFP4 = 0, ORC_MXFP4 = 1 };
+
+double orc_e4m3_decode(uint8_t b);
+double orc_e2m1_decode(uint8_t nib);
+double orc_e8m0_decode(uint8_t e);
+uint8_t orc_e4m3_encode(float v);
+float orc_pow2_ceil(float x);
+
+/* x [rows,k] f32 -> codes [rows,k] e4m3 bytes, scales [rows,k/128] f32; k % 128 == 0. */
+void orc_act_quant(const float *x, int64_t rows, int64_t k, uint8_t *codes, float *scales);
+
+/* f64 reference: out/absp [g,n]; w [n,k/2] nibble pairs; sc [n,k/gs]. */
+void orc_gemm_ref(const uint8_t *codes, const float *scales, const uint8_t *w, const uint8_t *sc,
+                  float scale2, int recipe, int64_t g, int64_t n, int64_t k, double *out,
+                  double *absp);
+
+/* Grouped reference at sampled (routed row, column) pairs; samples sorted by row. */
+int orc_grouped_ref_sampled(const float *x, int64_t T, int64_t k, const int32_t *row_ids,
+                            const int32_t *offsets, int num_experts, int64_t P, const uint8_t *w,
+                            const uint8_t *sc, const float *scale2, int recipe, int64_t n,
+                            const int64_t *sample_p, const int64_t *sample_col, int64_t ns,
+                            double *out, double *absp, uint8_t *tmp_codes, float *tmp_scales);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

@@ -1,0 +1,411 @@
+"""Pins of the CPU oracle to things other than itself (no GPU).
+
+Each test ties an oracle function to a library routine, a hand-derived worked example
+from the pages' definitions, a closed form, an invariant, or brute force on tiny inputs,
+so that a dropped term, a wrong sign or index, or a transposed operand fails one of them.
+Pages: memra-engine 0.98.0 src/bin/dsv4_native_gemm_gate.rs (fn quant_rows, fn f64_ref,
+struct ExpertRaw) and 0.71.0 src/bin/kernel_check.rs (e4m3 decoder, FP4 grid facts).
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+# ----------------------------------------------------------------- independent decoders
+
+def torch_e4m3(codes):
+    """Library decode (torch float8_e4m3fn) -> float64."""
+    c = torch.as_tensor(np.asarray(codes, dtype=np.uint8))
+    return c.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def torch_encode(values):
+    v = torch.as_tensor(np.asarray(values, dtype=np.float32))
+    return v.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def golden_e2m1(golden_dir):
+    vals = {}
+    with open(os.path.join(golden_dir, "e2m1_grid.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            c, v = line.split()
+            vals[int(c)] = float(v)
+    table = np.zeros(16)
+    for c in range(8):
+        table[c] = vals[c]
+        table[c + 8] = -vals[c]
+    return table
+
+
+# ----------------------------------------------------------------- e4m3
+
+def test_e4m3_decode_matches_library_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.e4m3_decode(codes)
+    want = torch_e4m3(codes)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert set(np.flatnonzero(nan)) == {0x7F, 0xFF}  # exponent 15 with mantissa 7
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+def test_e4m3_decode_page_facts():
+    d = oracle.e4m3_decode(np.array([0x7E, 0x01, 0x07, 0x08, 0x38, 0x80, 0xFE], dtype=np.uint8))
+    assert d[0] == 448.0                 # largest finite
+    assert d[1] == 2.0 ** -9             # exponent 0: mantissa * 2^-9
+    assert d[2] == 7 * 2.0 ** -9
+    assert d[3] == 2.0 ** -6             # smallest normal, bias 7
+    assert d[4] == 1.0
+    assert d[5] == 0.0 and np.signbit(d[5])
+    assert d[6] == -448.0
+
+
+def test_e4m3_roundtrip_all_finite_codes():
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.uint8)
+    vals = oracle.e4m3_decode(codes).astype(np.float32)
+    assert np.array_equal(oracle.e4m3_encode(vals), codes)
+
+
+def _sweep_values():
+    grid = np.sort(np.unique(np.abs(torch_e4m3(np.arange(0, 0x7F, dtype=np.uint8)))))
+    mids = (grid[:-1] + grid[1:]) / 2.0          # exact in f32 (<= 5 significant bits)
+    mids32 = mids.astype(np.float32)
+    assert np.array_equal(mids32.astype(np.float64), mids)
+    up = np.nextafter(mids32, np.float32(np.inf))
+    dn = np.nextafter(mids32, np.float32(0))
+    rng = np.random.default_rng(7)
+    rnd = (2.0 ** rng.uniform(-24, math.log2(448), 20000)).astype(np.float32)
+    rnd = np.minimum(rnd, np.float32(448))
+    tiny = np.array([0.0, 1e-30, 1e-9, 2.0 ** -10, 2.0 ** -11, 2.0 ** -10 * 1.0000001],
+                    dtype=np.float32)
+    pos = np.concatenate([grid.astype(np.float32), mids32, up, dn, rnd, tiny])
+    return np.concatenate([pos, -pos, np.array([-0.0], dtype=np.float32)])
+
+
+def test_e4m3_encode_matches_library_rne():
+    v = _sweep_values()
+    assert np.all(np.abs(v) <= 448)
+    assert np.array_equal(oracle.e4m3_encode(v), torch_encode(v))
+
+
+def test_e4m3_encode_is_nearest_by_brute_force():
+    """Nearest of all 254 finite codes, ties to the even code, sign kept."""
+    codes = np.array([c for c in range(0x7F)], dtype=np.uint8)
+    grid = torch_e4m3(codes)
+    rng = np.random.default_rng(11)
+    v = np.concatenate([rng.uniform(-448, 448, 3000), rng.normal(0, 1e-2, 3000)]).astype(np.float32)
+    got = oracle.e4m3_encode(v)
+    a = np.abs(v.astype(np.float64))
+    d = np.abs(a[:, None] - grid[None, :])
+    best = d.min(axis=1)
+    for i in range(v.size):
+        cands = np.flatnonzero(d[i] == best[i])
+        c = cands[0] if cands.size == 1 else [c for c in cands if c % 2 == 0][0]
+        want = c | (0x80 if np.signbit(v[i]) else 0)
+        assert got[i] == want, (v[i], got[i], want)
+
+
+def test_e4m3_thresholds_match_library():
+    for code in range(0, 0x7F):
+        t = oracle.e4m3_threshold(code)
+        assert torch_encode([t])[0] == code
+        if code > 0:
+            below = np.nextafter(np.float32(t), np.float32(0))
+            assert torch_encode([below])[0] == code - 1
+
+
+# ----------------------------------------------------------------- e2m1 / e8m0
+
+def test_e2m1_grid_matches_golden(golden_dir):
+    got = oracle.e2m1_decode(np.arange(16))
+    want = golden_e2m1(golden_dir)
+    assert np.array_equal(np.abs(got), np.abs(want))
+    assert np.array_equal(got[1:8], want[1:8]) and np.array_equal(got[9:], want[9:])
+    assert np.all(np.signbit(got[8:])) and not np.any(np.signbit(got[:8]))
+    # page facts: 8 grid points per sign, top point 6
+    assert len(set(np.abs(got).tolist())) == 8 and np.max(np.abs(got)) == 6.0
+    assert np.all(np.diff(got[:8]) > 0)
+
+
+def test_e8m0_closed_form():
+    e = np.arange(255, dtype=np.uint8)
+    got = oracle.e8m0_decode(e)
+    assert np.array_equal(got, np.ldexp(1.0, e.astype(np.int64) - 127))
+    assert np.isnan(oracle.e8m0_decode(np.array([255], dtype=np.uint8))[0])
+    assert got[127] == 1.0 and got[0] == 2.0 ** -127
+
+
+# ----------------------------------------------------------------- pow2_ceil
+
+def test_pow2_ceil_invariants():
+    rng = np.random.default_rng(3)
+    x = (2.0 ** rng.uniform(-40, 100, 5000)).astype(np.float32)
+    x = np.concatenate([x, np.ldexp(np.float32(1), np.arange(-30, 30)).astype(np.float32),
+                        np.array([2.2321428e-07, 1.0, 0.75, 1.5, 3.0], dtype=np.float32)])
+    s = oracle.pow2_ceil(x)
+    m, _ = np.frexp(s.astype(np.float64))
+    assert np.all(m == 0.5)                         # a power of two
+    xs = x.astype(np.float64)
+    ss = s.astype(np.float64)
+    assert np.all(ss >= xs) and np.all(ss / 2 < xs)  # the smallest one >= x
+
+
+# ----------------------------------------------------------------- act_quant
+
+def _parse_examples(golden_dir):
+    out = []
+    with open(os.path.join(golden_dir, "act_quant_examples.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            ident, fill, over, slog, codes = [p.strip() for p in line.split("|")]
+            x = np.full(128, float(fill), dtype=np.float32)
+            if over != "-":
+                for item in over.split(","):
+                    i, v = item.split(":")
+                    x[int(i)] = np.float32(float(v))
+            exp = {int(i): int(c, 16) for i, c in (it.split(":") for it in codes.split(","))}
+            out.append((ident, x, float(2.0 ** int(slog)), exp))
+    return out
+
+
+def test_act_quant_worked_examples(golden_dir):
+    ex = _parse_examples(golden_dir)
+    assert len(ex) >= 7
+    for ident, x, scale, codes in ex:
+        c, s = oracle.act_quant(x[None, :])
+        assert s[0, 0] == scale, ident
+        for i, want in codes.items():
+            assert c[0, i] == want, (ident, i, hex(c[0, i]), hex(want))
+
+
+def _random_rows(rng, rows, k):
+    x = rng.standard_normal((rows, k)).astype(np.float32)
+    x[1] *= 1e-6                                   # floor territory
+    x[2, :128] = 0.0                               # all-zero group
+    x[3] = (rng.standard_t(3, k) * 100).astype(np.float32)
+    mask = rng.random((rows, k)) < 0.01
+    x[mask] *= 50.0
+    x[4, :64] = np.float32(1e-40) * rng.standard_normal(64).astype(np.float32)  # subnormals
+    x[5] = torch.tensor(x[5]).to(torch.bfloat16).float().numpy()  # bf16-range ties
+    return x
+
+
+def test_act_quant_invariants_and_brute_force_codes():
+    rng = np.random.default_rng(5)
+    rows, k = 8, 512
+    x = _random_rows(rng, rows, k)
+    codes, scales = oracle.act_quant(x)
+    grid_codes = np.array([c for c in range(0x7F)], dtype=np.uint8)
+    grid = torch_e4m3(grid_codes)
+    for r in range(rows):
+        for g in range(k // 128):
+            grp = x[r, g * 128:(g + 1) * 128].astype(np.float64)
+            s = float(scales[r, g])
+            m, _ = np.frexp(s)
+            assert m == 0.5                                   # power of two
+            amax = max(np.max(np.abs(grp)), float(np.float32(1e-4)))
+            assert s * 448 >= amax * (1 - 2.0 ** -23)         # x/s never needs the clamp
+            dec = torch_e4m3(codes[r, g * 128:(g + 1) * 128])
+            if np.max(np.abs(grp)) >= 1e-4:
+                top = np.max(np.abs(dec))
+                assert 224 <= top <= 448, (r, g, top)
+            if np.all(grp == 0):
+                assert s == 2.0 ** -22 and np.all(codes[r, g * 128:(g + 1) * 128] == 0)
+            q = grp / s                                       # exact (power of two)
+            d = np.abs(np.abs(q)[:, None] - grid[None, :])
+            best = d.min(axis=1)
+            for i in range(128):
+                cands = np.flatnonzero(d[i] == best[i])
+                c = cands[0] if cands.size == 1 else [c for c in cands if c % 2 == 0][0]
+                want = c | (0x80 if np.signbit(q[i]) else 0)
+                assert codes[r, g * 128 + i] == want
+
+
+def test_act_quant_matches_library_pipeline():
+    """Same steps with numpy f32 arithmetic and torch's e4m3 conversion."""
+    rng = np.random.default_rng(9)
+    x = _random_rows(rng, 8, 1024)
+    codes, scales = oracle.act_quant(x)
+    g = x.reshape(8, 8, 128)
+    amax = np.maximum(np.max(np.abs(g), axis=2), np.float32(1e-4)).astype(np.float32)
+    t = (amax * np.float32(1.0 / 448.0)).astype(np.float32)
+    s = np.exp2(np.ceil(np.log2(t.astype(np.float64)))).astype(np.float32)
+    assert np.array_equal(s, scales)
+    q = np.clip((g / s[:, :, None]).astype(np.float32), -448, 448)
+    assert np.array_equal(torch_encode(q.reshape(8, 1024)), codes)
+
+
+# ----------------------------------------------------------------- GEMM reference
+
+def _exact_inputs(rng, g, n, k, recipe):
+    """Lossless special case: per-group amax exactly 448*2^m with integer codes, unit weight
+    scales. Returns x, w, sc, and the decoded dense matrices."""
+    kq = k // 128
+    m = rng.integers(-1, 2, (g, kq))
+    c = rng.integers(-16, 17, (g, k)).astype(np.float64)
+    c.reshape(g, kq, 128)[:, :, 0] = 448.0 * rng.choice([-1, 1], (g, kq))
+    x = (c.reshape(g, kq, 128) * np.exp2(m)[:, :, None]).reshape(g, k).astype(np.float32)
+    w = rng.integers(0, 256, (n, k // 2), dtype=np.uint8)
+    gs = 16 if recipe == oracle.NVFP4 else 32
+    sc = np.full((n, k // gs), 0x38 if recipe == oracle.NVFP4 else 127, dtype=np.uint8)
+    return x, w, sc
+
+
+def _dense_weights(w, table):
+    n, kh = w.shape
+    lo = table[w & 0x0F]
+    hi = table[w >> 4]
+    dense = np.empty((n, kh * 2))
+    dense[:, 0::2] = lo       # low nibble = even k (struct ExpertRaw / mirror_gemm)
+    dense[:, 1::2] = hi
+    return dense
+
+
+@pytest.mark.parametrize("recipe", [oracle.NVFP4, oracle.MXFP4])
+def test_gemm_exact_special_case_is_plain_matmul(recipe, golden_dir):
+    rng = np.random.default_rng(21 + recipe)
+    table = golden_e2m1(golden_dir)
+    for g, n, k in [(3, 5, 256), (8, 64, 1024)]:
+        x, w, sc = _exact_inputs(rng, g, n, k, recipe)
+        codes, scales = oracle.act_quant(x)
+        # quantisation is lossless here
+        deq = torch_e4m3(codes) * np.repeat(scales.astype(np.float64), 128, axis=1)
+        assert np.array_equal(deq, x.astype(np.float64))
+        out, absp = oracle.gemm_ref(codes, scales, w, sc, 1.0, recipe)
+        want = x.astype(np.float64) @ _dense_weights(w, table).T
+        assert np.array_equal(out, want)
+        assert np.array_equal(absp, np.abs(x.astype(np.float64)) @ np.abs(_dense_weights(w, table)).T)
+
+
+def _rational_ref(codes, scales, w, sc, scale2, recipe, table):
+    g, k = codes.shape
+    n = w.shape[0]
+    gs = 16 if recipe == oracle.NVFP4 else 32
+    adec = torch_e4m3(codes)
+    wd = _dense_weights(w, table)
+    out = np.empty((g, n), dtype=object)
+    absp = np.empty((g, n), dtype=object)
+    for r in range(g):
+        for col in range(n):
+            acc = Fraction(0)
+            ab = Fraction(0)
+            for j in range(k // gs):
+                if recipe == oracle.NVFP4:
+                    ws = np.float32(torch_e4m3([sc[col, j]])[0]) * np.float32(scale2)
+                else:
+                    ws = np.float32(math.ldexp(1.0, int(sc[col, j]) - 127))
+                f = Fraction(float(ws)) * Fraction(float(scales[r, (j * gs) // 128]))
+                for i in range(gs):
+                    kk = j * gs + i
+                    p = Fraction(float(adec[r, kk])) * Fraction(float(wd[col, kk])) * f
+                    acc += p
+                    ab += abs(p)
+            out[r, col] = acc
+            absp[r, col] = ab
+    return out, absp
+
+
+@pytest.mark.parametrize("recipe,scale2", [(oracle.NVFP4, 1 / 64), (oracle.NVFP4, 5.9945243e-5),
+                                           (oracle.MXFP4, 0.0)])
+def test_gemm_matches_exact_rational_sum(recipe, scale2, golden_dir):
+    rng = np.random.default_rng(31 + recipe)
+    table = golden_e2m1(golden_dir)
+    for g, n, k in [(2, 3, 128), (1, 4, 256)]:
+        codes = rng.integers(0, 256, (g, k), dtype=np.uint8)
+        codes[(codes & 0x7F) == 0x7F] = 0x3C
+        scales = np.exp2(rng.integers(-12, 4, (g, k // 128))).astype(np.float32)
+        w = rng.integers(0, 256, (n, k // 2), dtype=np.uint8)
+        gs = 16 if recipe == oracle.NVFP4 else 32
+        if recipe == oracle.NVFP4:
+            sc = rng.integers(0x20, 0x41, (n, k // gs), dtype=np.uint8)
+        else:
+            sc = rng.integers(118, 135, (n, k // gs), dtype=np.uint8)
+        out, absp = oracle.gemm_ref(codes, scales, w, sc, scale2, recipe)
+        ex, exabs = _rational_ref(codes, scales, w, sc, scale2, recipe, table)
+        for r in range(g):
+            for c in range(n):
+                e = float(ex[r, c])
+                assert abs(out[r, c] - e) <= k * 2.0 ** -53 * float(exabs[r, c])
+                assert abs(absp[r, c] - float(exabs[r, c])) <= k * 2.0 ** -53 * float(exabs[r, c])
+
+
+def test_gemm_nibble_order_and_scale_indexing_worked_example():
+    """Hand-computed outputs for one-hot activations (values from the definitions):
+    row 0 is one-hot at k=1, row 1 one-hot at k=16, row 2 one-hot at k=128."""
+    k, n = 256, 2
+    x = np.zeros((3, k), dtype=np.float32)
+    x[0, 1] = 1.0      # group 0: amax 1 -> s = 2^-8, code 256
+    x[1, 16] = -2.0    # group 0: s = 2^-7, code -256
+    x[2, 128] = 3.0    # group 1: s = 2^-7, code 384
+    codes, scales = oracle.act_quant(x)
+    w = np.zeros((n, k // 2), dtype=np.uint8)
+    w[0, 0] = 0x21     # col 0: k=0 -> code 1 (0.5), k=1 -> code 2 (1.0)
+    w[0, 8] = 0x0D     # col 0: k=16 -> code 13 (-3.0), k=17 -> 0
+    w[1, 64] = 0x07    # col 1: k=128 -> code 7 (6.0)
+    w[1, 0] = 0xF0     # col 1: k=1 -> code 15 (-6.0)
+    sc = np.full((n, k // 16), 0x38, dtype=np.uint8)   # 1.0
+    sc[0, 1] = 0x40    # col 0, k in [16, 32): 2.0
+    sc[1, 8] = 0x30    # col 1, k in [128, 144): 0.5
+    out, _ = oracle.gemm_ref(codes, scales, w, sc, 0.25, oracle.NVFP4)
+    # out[r, c] = code * E2M1 * (e4m3 scale * scale2) * activation scale
+    assert out[0, 0] == 256 * 1.0 * (1.0 * 0.25) * 2.0 ** -8      # = 0.25
+    assert out[0, 1] == 256 * -6.0 * (1.0 * 0.25) * 2.0 ** -8     # = -1.5
+    assert out[1, 0] == -256 * -3.0 * (2.0 * 0.25) * 2.0 ** -7    # = 3.0
+    assert out[1, 1] == 0.0
+    assert out[2, 0] == 0.0
+    assert out[2, 1] == 384 * 6.0 * (0.5 * 0.25) * 2.0 ** -7      # = 2.25
+    # MXFP4: per-32 scale, e8m0 128 = 2.0 on k in [0, 32) of col 0
+    sc2 = np.full((n, k // 32), 127, dtype=np.uint8)
+    sc2[0, 0] = 128
+    out2, _ = oracle.gemm_ref(codes, scales, w, sc2, 0.0, oracle.MXFP4)
+    assert out2[0, 0] == 256 * 1.0 * 2.0 * 2.0 ** -8               # = 2.0
+    assert out2[1, 0] == -256 * -3.0 * 2.0 * 2.0 ** -7             # = 12.0
+    assert out2[2, 1] == 384 * 6.0 * 1.0 * 2.0 ** -7               # = 18.0
+
+
+def test_grouped_reference_routing_worked_example():
+    """Expert 1 empty; routed rows gather tokens out of order; each sampled output must
+    equal the single-expert reference on the hand-picked token and expert."""
+    rng = np.random.default_rng(41)
+    T, k, n, E = 5, 256, 6, 3
+    x = rng.standard_normal((T, k)).astype(np.float32)
+    offsets = np.array([0, 2, 2, 5], dtype=np.int32)
+    row_ids = np.array([4, 0, 1, 1, 3], dtype=np.int32)
+    expert_of_row = [0, 0, 2, 2, 2]
+    w = rng.integers(0, 256, (E, n, k // 2), dtype=np.uint8)
+    sc = rng.integers(0x20, 0x41, (E, n, k // 16), dtype=np.uint8)
+    s2 = np.array([1 / 64, 1 / 32, 1 / 16], dtype=np.float32)
+    sp = np.repeat(np.arange(5), n)
+    scol = np.tile(np.arange(n), 5)
+    out, absp = oracle.grouped_ref_sampled(x, row_ids, offsets, w, sc, s2, oracle.NVFP4, sp, scol)
+    for p in range(5):
+        e = expert_of_row[p]
+        codes, scales = oracle.act_quant(x[row_ids[p]][None, :])
+        ref, rabs = oracle.gemm_ref(codes, scales, w[e], sc[e], s2[e], oracle.NVFP4)
+        assert np.array_equal(out[p * n:(p + 1) * n], ref[0])
+        assert np.array_equal(absp[p * n:(p + 1) * n], rabs[0])
+    with pytest.raises(ValueError):
+        oracle.grouped_ref_sampled(x, np.array([4, 0, 1, 1, 9], dtype=np.int32), offsets, w, sc,
+                                   s2, oracle.NVFP4, np.array([4]), np.array([0]))
+
+
+def test_bound_checker_catches_planted_error():
+    ref = np.array([1.0, -2.0, 3.0])
+    absp = np.array([4.0, 4.0, 4.0])
+    ok, ratio, _ = oracle.within_bound(ref + 4.0 * 2.0 ** -24 * 4.0 * np.array([1, -1, 0.5]),
+                                       ref, absp, 4.0)
+    assert ok and ratio <= 1.0
+    ok, ratio, i = oracle.within_bound(ref + np.array([0, 0, 1e-3]), ref, absp, 4.0)
+    assert not ok and i == 2
+    assert oracle.max_rel(ref + 3e-3, ref) == pytest.approx(1e-3)
