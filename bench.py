@@ -1,0 +1,519 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized MoE expert projection on GB300.
+
+One step = the whole hot path over one batch: the gate/up and the down grouped
+projections of the prefill workload (256 NVFP4 experts, 4096 tokens top-8 Zipf(1.1);
+act_quant fused), each one call of fp4_grouped_expert_gemm. Headline value = expert GEMM
+TFLOP/s (algorithmic 2*rows*n*k). The same line carries the decode workload (64 NVFP4
+experts, 8 tokens top-8) as weight GB/s, the roofline of the dominant kernel, the CPU
+oracle baseline, the end-to-end number with host buffers, and the SM clocks seen.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload c4|c3|c5] [--no-decode]
+
+With N > 1 (torchrun, one rank per GPU) every rank runs an independent replica of the
+workload (weak scaling; the path has no cross-GPU exchange).
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "expert GEMM TFLOP/s (prefill) and weight GB/s (decode) vs GB300 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+WORKLOAD_NAMES = {"c3": "decode: 64 NVFP4 experts gate/up [3072,4096] + down [4096,1536], "
+                        "8 tokens top-8 uniform",
+                  "c4": "prefill grouped: 256 NVFP4 experts gate/up [2048,7168] + down "
+                        "[7168,2048], 4096 tokens top-8 Zipf(1.1)",
+                  "c5": "mixed: 128 NVFP4 + 128 MXFP4 experts [2048,4096], 16384 tokens "
+                        "top-8 uniform per recipe"}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (0 = about 2 s of work)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["c3", "c4", "c5"], default="c4")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--path", choices=["auto", "stream", "tc"], default="auto",
+                    help="force a kernel path (default: the library's choice by shape)")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ infrastructure
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = None
+        self.device_index = device_index
+
+    def _target(self):
+        import torch
+        try:
+            p = torch.cuda.get_device_properties(self.device_index)
+            return "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        except Exception:
+            return None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        tgt = self._target()
+        if tgt:
+            cmd[1:1] = ["-i", tgt]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    smax.append(float(parts[1]))
+                    power.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[4:8]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_scaled_fp4_act_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on the
+    current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(kernel_key)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ workload accounting
+
+def proj_flops(proj):
+    return 2.0 * proj.routing.P * proj.bank.n * proj.bank.k
+
+
+def proj_bytes(proj):
+    """Algorithmic bytes: touched experts' nibbles + scales + scale2, activations read
+    once, outputs written once."""
+    import torch
+    b = proj.bank
+    gs = 16 if b.recipe == 0 else 32
+    touched = int(torch.count_nonzero(torch.diff(proj.routing.offsets)).item())
+    weights = touched * (b.n * (b.k // 2) + b.n * (b.k // gs) + 4)
+    rows_x = proj.x.shape[0]
+    act = rows_x * b.k * 4
+    out = proj.routing.P * b.n * 4
+    return weights + act + out, weights
+
+
+def launches_per_call(fp4, proj, have_ws):
+    path = fp4.fp4_gemm_path(proj.routing.P, proj.bank.E, proj.bank.n, proj.bank.k,
+                             proj.bank.recipe, have_ws)
+    return path, (2 if path == fp4.PATH_TC else 1)
+
+
+# ------------------------------------------------------------------ our arm
+
+def make_calls(fp4, wl, device):
+    import torch
+    calls = []
+    for proj in wl.projections:
+        T, k = proj.x.shape
+        ws = fp4.workspace_for(T, proj.routing.P, proj.bank.n, k, proj.bank.recipe, device=device)
+        out = torch.empty(proj.routing.P, proj.bank.n, device=device)
+        rid = proj.routing.row_ids if proj.row_ids_used else None
+        path, nl = launches_per_call(fp4, proj, ws is not None)
+
+        def call(proj=proj, ws=ws, out=out, rid=rid, x=None):
+            fp4.fp4_grouped_expert_gemm(proj.x if x is None else x, rid, proj.routing.offsets,
+                                        proj.bank.w, proj.bank.sc, proj.bank.scale2,
+                                        proj.bank.recipe, out=out, workspace=ws)
+        calls.append({"proj": proj, "call": call, "out": out, "ws": ws, "path": path,
+                      "launches": nl})
+    return calls
+
+
+def time_steps(calls, steps, flush=None):
+    """Run `steps` steps; per call, CUDA events on the launching (current) stream.
+    Returns (elapsed ms of the whole region, per-call list of durations in ms)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in calls] for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for s in range(steps):
+        if flush is not None:
+            flush.zero_()
+        for i, c in enumerate(calls):
+            evs[s][i][0].record(stream)
+            c["call"]()
+            evs[s][i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    per_call = [[evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(steps)]
+                for i in range(len(calls))]
+    return t0.elapsed_time(t1), per_call
+
+
+def run_e2e(fp4, calls, steps):
+    """Same step through the public API with host buffers: pinned host inputs copied in,
+    outputs copied back, inside the timed region."""
+    import torch
+    host_in, host_out, dev_in = [], [], []
+    h2d = d2h = 0
+    for c in calls:
+        p = c["proj"]
+        hx = p.x.cpu().pin_memory()
+        hr = p.routing.row_ids.cpu().pin_memory()
+        ho = p.routing.offsets.cpu().pin_memory()
+        host_in.append((hx, hr, ho))
+        dev_in.append((torch.empty_like(p.x), torch.empty_like(p.routing.row_ids),
+                       torch.empty_like(p.routing.offsets)))
+        host_out.append(torch.empty(c["out"].shape, dtype=torch.float32).pin_memory())
+        h2d += hx.numel() * 4 + (hr.numel() * 4 if p.row_ids_used else 0) + ho.numel() * 4
+        d2h += c["out"].numel() * 4
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for c, (hx, hr, ho), (dx, dr, do), hout in zip(calls, host_in, dev_in, host_out):
+            p = c["proj"]
+            dx.copy_(hx, non_blocking=True)
+            do.copy_(ho, non_blocking=True)
+            rid = None
+            if p.row_ids_used:
+                dr.copy_(hr, non_blocking=True)
+                rid = dr
+            fp4.fp4_grouped_expert_gemm(dx, rid, do, p.bank.w, p.bank.sc, p.bank.scale2,
+                                        p.bank.recipe, out=c["out"], workspace=c["ws"])
+            hout.copy_(c["out"], non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps, h2d, d2h
+
+
+def cpu_oracle_sample(wl, budget_s, rows_cap=None, seed=0):
+    """Time the CPU oracle (as it stands, single-threaded C) on a bounded sample of the
+    workload's routed rows, all n columns each. Returns (flops, seconds, description)."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(seed)
+    flops = 0.0
+    secs = 0.0
+    rows_done = 0
+    per_proj = budget_s / len(wl.projections)
+    for proj in wl.projections:
+        b = proj.bank
+        off = proj.routing.offsets.cpu().numpy().astype(np.int64)
+        rid = proj.routing.row_ids.cpu().numpy()
+        P = proj.routing.P
+        t_start = time.perf_counter()
+        done_here = 0
+        while True:
+            p = int(rng.integers(0, P))
+            e = int(np.searchsorted(off, p, side="right") - 1)
+            t = int(rid[p]) if proj.row_ids_used else p
+            x = proj.x[t:t + 1].cpu().numpy()
+            w = b.w[e].cpu().numpy()
+            sc = b.sc[e].cpu().numpy()
+            s2 = float(b.scale2[e].item())
+            t1 = time.perf_counter()
+            codes, scales = oracle.act_quant(x)
+            oracle.gemm_ref(codes, scales, w, sc, s2, b.recipe)
+            secs += time.perf_counter() - t1
+            flops += 2.0 * b.n * b.k
+            done_here += 1
+            rows_done += 1
+            if rows_cap is not None and done_here >= rows_cap:
+                break
+            if time.perf_counter() - t_start >= per_proj and done_here >= 2:
+                break
+    desc = "%d random routed rows x all n columns (act_quant + f64 reference), %s" % (
+        rows_done, "+".join(p.name for p in wl.projections))
+    return flops, secs, desc
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import block_scaled_fp4_act_gb300 as fp4
+    from block_scaled_fp4_act_gb300 import build as libbuild
+    from block_scaled_fp4_act_gb300 import synth
+
+    libbuild.build()
+    fp4.lib()
+    fp4.fp4_force_path({"auto": fp4.PATH_AUTO, "stream": fp4.PATH_STREAM,
+                        "tc": fp4.PATH_TC}[args.path])
+    device = torch.device("cuda", torch.cuda.current_device())
+    peaks, peak_src = load_peaks()
+
+    wl = synth.workload(args.workload, device=device)
+    calls = make_calls(fp4, wl, device)
+    flops_step = sum(proj_flops(c["proj"]) for c in calls)
+    bytes_step = sum(proj_bytes(c["proj"])[0] for c in calls)
+    for _ in range(max(3, args.warmup)):
+        for c in calls:
+            c["call"]()
+    torch.cuda.synchronize()
+    steps = args.steps
+    if steps <= 0:
+        el, _ = time_steps(calls, 3)
+        steps = max(10, min(2000, int(2000.0 / max(el / 3, 1e-3))))
+    steps = int(max_over_ranks(steps, world))
+
+    barrier(world)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    elapsed, per_call = time_steps(calls, steps)
+    clk = clocks.stop()
+    barrier(world)
+    elapsed = max_over_ranks(elapsed, world)
+    ms_step = elapsed / steps
+    value = world * flops_step / (ms_step * 1e-3) / 1e12
+
+    # roofline of the dominant kernel: the grouped GEMM call (all launches of it)
+    paths = sorted({c["path"] for c in calls})
+    call_ms = [sum(d) / len(d) for d in per_call]
+    kflops = sum(proj_flops(c["proj"]) for c in calls)
+    kms = sum(call_ms)
+    tc = all(c["path"] == fp4.PATH_TC for c in calls)
+    recipes = {c["proj"].bank.recipe for c in calls}
+    if tc:
+        bf16 = peaks["bf16_tflops"]
+        peak = bf16 if recipes == {0} else 2 * bf16
+        bound = "tensor"
+        kernel = "tc_grouped_gemm"
+    else:
+        # CUDA-core f32 FMA peak: 152 SMs x 128 lanes x 2 flops x 2.07 GHz
+        peak = 152 * 128 * 2 * 2.07e9 / 1e12
+        bound = "alu"
+        kernel = "stream_gemm"
+    achieved = kflops / (kms * 1e-3) / 1e12
+    traffic = ncu_traffic("%s/%s" % (kernel, args.workload))
+    roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                "kernel": kernel, "peak_source": peak_src if tc else "derived: 152 SMs x 128 "
+                "FP32 lanes x 2 x 2.07 GHz", "launches": steps * sum(c["launches"] for c in calls),
+                "per_call_ms": [round(m, 4) for m in call_ms]}
+
+    result = {"metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+              "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+              "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+              "dtype": "e4m3 x e2m1 -> f32 (tensor path: bf16 operands, f32 accumulate)"
+              if tc else "e4m3 x e2m1 -> f32 (f16 operands, f32 accumulate)",
+              "data": "synthetic (seeded; weights, routing and activations as the workload "
+                      "recipe states)",
+              "config": {"workload": WORKLOAD_NAMES[args.workload], "paths": paths,
+                         "flops_per_step": flops_step, "bytes_per_step": bytes_step,
+                         "l2": "inputs larger than L2 (weights %.2f GB per step)" %
+                               (sum(proj_bytes(c["proj"])[1] for c in calls) / 1e9),
+                         "parallelism": "replicas x%d" % world},
+              "roofline": roofline, "clocks": clk,
+              "gpu_launches": steps * sum(c["launches"] for c in calls)}
+
+    # decode workload alongside: weight GB/s against HBM, L2 flushed between steps
+    if args.workload == "c4" and not args.no_decode:
+        wd = synth.decode_c3(device=device)
+        dcalls = make_calls(fp4, wd, device)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+        for _ in range(3):
+            for c in dcalls:
+                c["call"]()
+        dsteps = 200
+        _, dper = time_steps(dcalls, dsteps, flush=flush)
+        dms = [sum(d) / len(d) for d in dper]
+        dbytes = sum(proj_bytes(c["proj"])[0] for c in dcalls)
+        dweights = sum(proj_bytes(c["proj"])[1] for c in dcalls)
+        gbs = dbytes / (sum(dms) * 1e-3) / 1e9
+        result["decode"] = {
+            "workload": WORKLOAD_NAMES["c3"], "value": round(world * dweights /
+                                                              (sum(dms) * 1e-3) / 1e9, 1),
+            "unit": "weight GB/s", "us_per_step": round(sum(dms) * 1e3, 2),
+            "steps": dsteps, "l2": "flushed (256 MB write) between steps",
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4),
+                         "traffic": ncu_traffic("stream_gemm/c3"), "kernel": "stream_gemm",
+                         "bytes_per_step": dbytes, "peak_source": peak_src},
+            "gpu_launches": dsteps * sum(c["launches"] for c in dcalls)}
+        del dcalls, wd, flush
+
+    # end to end through the public API with host buffers
+    if not args.no_e2e:
+        e2e_steps = min(steps, 10)
+        e2e_ms, h2d, d2h = run_e2e(fp4, calls, e2e_steps)
+        e2e_ms = max_over_ranks(e2e_ms, world)
+        result["e2e"] = {"value": round(world * flops_step / (e2e_ms * 1e-3) / 1e12, 3),
+                         "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                         "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
+                         "steps": e2e_steps}
+
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        fl, secs, desc = cpu_oracle_sample(wl, 12.0)
+        result["cpu_baseline"] = {"value": fl / secs / 1e12, "unit": "TFLOP/s", "cores": 1,
+                                  "kind": "oracle", "sample": desc,
+                                  "seconds": round(secs, 2)}
+    return result
+
+
+def run_reference(args, world, rank):
+    """The oracle (as it stands) on the host cores: each step is a bounded sample of the
+    same workload (16 random routed rows per projection, all n columns)."""
+    import torch
+    from block_scaled_fp4_act_gb300 import synth
+    import oracle
+    oracle.lib_path()
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    wl = synth.workload(args.workload, device=device)
+    rows = 16
+    for i in range(args.warmup):
+        cpu_oracle_sample(wl, 1e9, rows_cap=rows, seed=1000 + i)
+    fl_tot, s_tot = 0.0, 0.0
+    steps = args.steps if args.steps > 0 else 10
+    for i in range(steps):
+        fl, secs, desc = cpu_oracle_sample(wl, 1e9, rows_cap=rows, seed=i)
+        fl_tot += fl
+        s_tot += secs
+    value = fl_tot / s_tot / 1e12
+    ms = s_tot / steps * 1e3
+    return {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "impl": "reference",
+            "config": {"workload": WORKLOAD_NAMES[args.workload],
+                       "sample": "%d random routed rows per projection per step" % rows},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        # the oracle arm runs on rank 0 only; other ranks exit without work
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        if rank == 0:
+            print(json.dumps(run_reference(args, world, rank)), flush=True)
+        return
+    world, rank, local = dist_setup()
+    result = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,167 @@
+// common.cuh -- device helpers shared by the library's kernels (sm_103a).
+//
+// Formats (memra-engine 0.98.0, src/bin/dsv4_native_gemm_gate.rs):
+//   activation code : e4m3fn byte, per-128 power-of-two f32 scale (fn quant_rows)
+//   weight          : E2M1 nibble pairs, low nibble = even k (struct ExpertRaw, mirror_gemm)
+//   NVFP4 scale     : e4m3 byte per 16 weights, times the f32 scale2 of the tensor
+//   MXFP4 scale     : e8m0 byte per 32 weights, 2^(e-127)
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace fp4moe {
+
+// Sets FP4_DEVERR_* bits in the per-device error word whose address the host passes in.
+__device__ __forceinline__ void raise_device_error(unsigned *err, unsigned bits)
+{
+    atomicOr(err, bits);
+}
+
+// ---------------------------------------------------------------- activation quantisation
+
+// f32(1/448) as fn quant_rows forms it: (1.0f64 / 448.0) rounded to f32.
+constexpr float kInv448 = (float)(1.0 / 448.0);
+
+// Smallest power of two >= t for a finite normal t > 0 (t = amax * f32(1/448) with
+// amax >= 1e-4 is always normal): keep t if its mantissa is zero, else round the
+// exponent up.
+__device__ __forceinline__ float pow2_ceil_normal(float t)
+{
+    const uint32_t b = __float_as_uint(t);
+    if ((b & 0x007FFFFFu) == 0u)
+        return t;
+    return __uint_as_float((b & 0x7F800000u) + 0x00800000u);
+}
+
+// 1/s for a power of two s in [2^-126, 2^126]: exact, by exponent arithmetic.
+__device__ __forceinline__ float pow2_reciprocal(float s)
+{
+    return __uint_as_float((254u << 23) - __float_as_uint(s));
+}
+
+// Group scale from the group's max |x| (fn quant_rows: floor 1e-4, times f32(1/448),
+// pow2_ceil).
+__device__ __forceinline__ float group_scale(float amax)
+{
+    amax = fmaxf(amax, 1e-4f);
+    return pow2_ceil_normal(amax * kInv448);
+}
+
+// x/s clamped to +-448, as fn quant_rows does before encoding. x * (1/s) equals x / s
+// bit for bit: both are the correctly rounded value of the same exact quotient.
+__device__ __forceinline__ float scaled_clamped(float x, float inv_s)
+{
+    return fminf(fmaxf(x * inv_s, -448.0f), 448.0f);
+}
+
+// Two f32 -> two e4m3 bytes, round to nearest even, saturating to finite (inputs are
+// already within +-448, so saturation never triggers). Low byte = `lo`.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return (uint32_t)r;
+}
+
+// Four f32 -> four e4m3 bytes packed little-endian.
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
+{
+    return e4m3x2(a, b) | (e4m3x2(c, d) << 16);
+}
+
+// Two e4m3 bytes (low 16 bits) -> f16x2, exact (low byte -> low half).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes)
+{
+    uint32_t r;
+    uint16_t v = (uint16_t)two_bytes;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
+}
+
+// ---------------------------------------------------------------- weight decoding
+
+// One byte of two E2M1 nibbles -> f16x2 (low nibble = even k -> low half), exact.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte_in_low_bits)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t}"
+        : "=r"(r)
+        : "r"(byte_in_low_bits));
+    return r;
+}
+
+// Four bytes (eight nibbles) -> four f16x2 words, k order preserved.
+__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t (&h)[4])
+{
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+}
+
+// e4m3 byte -> f32 (exact): through f16.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t byte)
+{
+    const uint32_t h2 = e4m3x2_to_f16x2(byte & 0xFFu);
+    return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+}
+
+// e8m0 byte -> f32: 2^(e-127); e = 0 is the subnormal 2^-127 (exact).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t e)
+{
+    return e == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);
+}
+
+// acc + w.lo*a.lo, then + w.hi*a.hi: f16 operands, exact products, f32 adds (one
+// rounding each). Keeps the k order of the pair.
+__device__ __forceinline__ float fma2_f16_f32(uint32_t w2, uint32_t a2, float acc)
+{
+    float r;
+    asm("{\n\t.reg .b16 wl, wh, al, ah;\n\t"
+        "mov.b32 {wl, wh}, %1;\n\t"
+        "mov.b32 {al, ah}, %2;\n\t"
+        "fma.rn.f32.f16 %0, wl, al, %3;\n\t"
+        "fma.rn.f32.f16 %0, wh, ah, %0;\n\t}"
+        : "=f"(r)
+        : "r"(w2), "r"(a2), "f"(acc));
+    return r;
+}
+
+// ---------------------------------------------------------------- memory
+
+// 128-bit streaming load of read-once data (weights): no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+} // namespace fp4moe

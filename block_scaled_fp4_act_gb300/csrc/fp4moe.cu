@@ -1,0 +1,277 @@
+// fp4moe.cu -- the exported C ABI (include/fp4moe.h): argument checks, path choice,
+// kernel launches and the per-device error word. No allocation, no synchronisation in
+// the compute calls.
+#include <atomic>
+#include <stdio.h>
+#include <string.h>
+
+#include "common.cuh"
+
+namespace fp4moe {
+
+__device__ unsigned int g_device_error = 0u;
+
+unsigned *device_error_word()
+{
+    static unsigned *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return nullptr;
+    if (!addr[dev]) {
+        void *a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_device_error) != cudaSuccess)
+            return nullptr;
+        addr[dev] = static_cast<unsigned *>(a);
+    }
+    return addr[dev];
+}
+
+int stream_max_rows_per_pass(int k);
+size_t tc_workspace_bytes(int64_t total_rows, int64_t k, int recipe);
+bool tc_supported(int64_t n, int64_t k, int recipe, int E);
+cudaError_t launch_tc_gemm(const GroupedProblem &p, void *workspace, cudaStream_t s);
+double tc_error_ops(int recipe, int64_t k);
+
+static std::atomic<int> g_forced_path{FP4_PATH_AUTO};
+static thread_local char g_last_error[256] = "";
+
+static int record(cudaError_t e)
+{
+    if (e == cudaSuccess)
+        return FP4_OK;
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e),
+             cudaGetErrorString(e));
+    return FP4_ERR_LAUNCH;
+}
+
+static bool aligned16(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0u;
+}
+
+static bool recipe_ok(int r)
+{
+    return r == FP4_NVFP4 || r == FP4_MXFP4;
+}
+
+// Rows per expert at or above which the tensor-core path pays for its workspace pass.
+constexpr int64_t kTcMinRowsPerExpert = 32;
+
+static int choose_path(int64_t P, int E, int64_t n, int64_t k, int recipe, bool have_ws)
+{
+    const int forced = g_forced_path.load();
+    if (forced != FP4_PATH_AUTO)
+        return forced;
+    if (have_ws && tc_supported(n, k, recipe, E) && P >= kTcMinRowsPerExpert * (int64_t)E)
+        return FP4_PATH_TC;
+    return FP4_PATH_STREAM;
+}
+
+static int stream_rows_per_pass(int64_t P, int E)
+{
+    const int64_t avg = E > 0 ? (P + E - 1) / E : P;
+    return avg >= 3 ? 4 : (avg >= 2 ? 2 : 2);
+}
+
+// Shared shape checks; returns FP4_OK or the status to report.
+static int check_shape(int64_t rows, int64_t n, int64_t k)
+{
+    if (rows < 0 || n < 0 || k < 0)
+        return FP4_ERR_ARG;
+    if (k == 0 || (k % 128) != 0 || n == 0)
+        return FP4_ERR_SHAPE;
+    if (k > (1 << 20) || n > (1 << 24) || rows > ((int64_t)1 << 31))
+        return FP4_ERR_SHAPE;
+    if (stream_max_rows_per_pass((int)k) == 0)
+        return FP4_ERR_SHAPE;
+    return FP4_OK;
+}
+
+static int run_grouped(GroupedProblem p, void *workspace, size_t ws_bytes, cudaStream_t s)
+{
+    p.err = device_error_word();
+    if (!p.err)
+        return record(cudaGetLastError() != cudaSuccess ? cudaGetLastError()
+                                                          : cudaErrorInvalidDevice);
+    const bool have_ws =
+        workspace != nullptr && ws_bytes >= tc_workspace_bytes(p.P, p.k, p.recipe);
+    const int path = choose_path(p.P, p.E, p.n, p.k, p.recipe, have_ws);
+    if (path == FP4_PATH_TC) {
+        if (!tc_supported(p.n, p.k, p.recipe, p.E))
+            return FP4_ERR_SHAPE;
+        if (!have_ws)
+            return FP4_ERR_WORKSPACE;
+        return record(launch_tc_gemm(p, workspace, s));
+    }
+    return record(launch_stream_gemm(p, stream_rows_per_pass(p.P, p.E), s));
+}
+
+} // namespace fp4moe
+
+using namespace fp4moe;
+
+extern "C" {
+
+int act_quant_fp8(const float *x, uint8_t *codes, float *scales, int64_t rows, int64_t k,
+                  void *stream)
+{
+    if (rows < 0 || k < 0)
+        return FP4_ERR_ARG;
+    if (k == 0 || k % 128 != 0)
+        return FP4_ERR_SHAPE;
+    if (rows == 0)
+        return FP4_OK;
+    if (!x || !codes || !scales)
+        return FP4_ERR_ARG;
+    if (!aligned16(x) || !aligned16(codes) || !aligned16(scales))
+        return FP4_ERR_ALIGN;
+    return record(launch_act_quant(x, codes, scales, rows, k, (cudaStream_t)stream));
+}
+
+int fp4_expert_gemm(const float *x, const uint8_t *w, const uint8_t *wscale, float scale2,
+                    int recipe, float *out, int64_t g, int64_t n, int64_t k, uint8_t *codes_out,
+                    float *scales_out, void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!recipe_ok(recipe))
+        return FP4_ERR_ARG;
+    int st = check_shape(g, n, k);
+    if (st != FP4_OK)
+        return st;
+    if (g == 0)
+        return FP4_OK;
+    if (!x || !w || !wscale || !out || ((codes_out == nullptr) != (scales_out == nullptr)))
+        return FP4_ERR_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(wscale) || !aligned16(out) ||
+        (codes_out && (!aligned16(codes_out) || !aligned16(scales_out))))
+        return FP4_ERR_ALIGN;
+    GroupedProblem p{};
+    p.x = x;
+    p.T = g;
+    p.row_ids = nullptr;
+    p.offsets = nullptr;
+    p.E = 1;
+    p.P = g;
+    p.w = w;
+    p.sc = wscale;
+    p.scale2 = nullptr;
+    p.scale2_host = scale2;
+    p.recipe = recipe;
+    p.out = out;
+    p.n = (int)n;
+    p.k = (int)k;
+    p.codes_out = codes_out;
+    p.scales_out = scales_out;
+    if (codes_out) {
+        // The quantised activations are a by-product of the streaming path's prologue.
+        p.err = device_error_word();
+        if (!p.err)
+            return record(cudaErrorInvalidDevice);
+        return record(launch_stream_gemm(p, stream_rows_per_pass(g, 1), (cudaStream_t)stream));
+    }
+    return run_grouped(p, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+size_t fp4_grouped_workspace_size(int64_t num_tokens, int64_t total_rows, int64_t n, int64_t k,
+                                  int recipe)
+{
+    (void)num_tokens;
+    if (!recipe_ok(recipe) || check_shape(total_rows, n, k) != FP4_OK)
+        return 0;
+    if (!tc_supported(n, k, recipe, 1))
+        return 0;  // the shape always takes the streaming path, which needs no workspace
+    return tc_workspace_bytes(total_rows, k, recipe);
+}
+
+int fp4_grouped_expert_gemm(const float *x, int64_t num_tokens, const int32_t *row_ids,
+                            const int32_t *offsets, int num_experts, int64_t total_rows,
+                            const uint8_t *w, const uint8_t *wscale, const float *scale2,
+                            int recipe, float *out, int64_t n, int64_t k, void *workspace,
+                            size_t workspace_bytes, void *stream)
+{
+    if (!recipe_ok(recipe) || num_experts < 1 || num_experts > 65535 || num_tokens < 0)
+        return FP4_ERR_ARG;
+    int st = check_shape(total_rows, n, k);
+    if (st != FP4_OK)
+        return st;
+    if (total_rows == 0)
+        return FP4_OK;
+    if (!x || !offsets || !w || !wscale || !out || (recipe == FP4_NVFP4 && !scale2))
+        return FP4_ERR_ARG;
+    if (!row_ids && num_tokens < total_rows)
+        return FP4_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(wscale) || !aligned16(out))
+        return FP4_ERR_ALIGN;
+    GroupedProblem p{};
+    p.x = x;
+    p.T = num_tokens;
+    p.row_ids = row_ids;
+    p.offsets = offsets;
+    p.E = num_experts;
+    p.P = total_rows;
+    p.w = w;
+    p.sc = wscale;
+    p.scale2 = recipe == FP4_NVFP4 ? scale2 : nullptr;
+    p.scale2_host = 1.0f;
+    p.recipe = recipe;
+    p.out = out;
+    p.n = (int)n;
+    p.k = (int)k;
+    p.codes_out = nullptr;
+    p.scales_out = nullptr;
+    return run_grouped(p, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+int fp4_gemm_path(int64_t total_rows, int num_experts, int64_t n, int64_t k, int recipe,
+                  int have_workspace)
+{
+    return choose_path(total_rows, num_experts, n, k, recipe, have_workspace != 0);
+}
+
+double fp4_error_ops(int path, int recipe, int64_t k)
+{
+    if (path == FP4_PATH_TC)
+        return tc_error_ops(recipe, k);
+    return stream_error_ops(recipe, k);
+}
+
+void fp4_force_path(int path)
+{
+    g_forced_path.store(path == FP4_PATH_STREAM || path == FP4_PATH_TC ? path : FP4_PATH_AUTO);
+}
+
+int fp4_get_device_error(void *stream, unsigned *bits)
+{
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return record(e);
+    unsigned v = 0u, zero = 0u;
+    e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v));
+    if (e == cudaSuccess)
+        e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
+    if (e != cudaSuccess)
+        return record(e);
+    if (bits)
+        *bits = v;
+    return v ? FP4_ERR_DEVICE : FP4_OK;
+}
+
+const char *fp4_last_error(void)
+{
+    return g_last_error;
+}
+
+const char *fp4_status_string(int status)
+{
+    switch (status) {
+    case FP4_OK: return "FP4_OK";
+    case FP4_ERR_ARG: return "FP4_ERR_ARG";
+    case FP4_ERR_SHAPE: return "FP4_ERR_SHAPE";
+    case FP4_ERR_ALIGN: return "FP4_ERR_ALIGN";
+    case FP4_ERR_LAUNCH: return "FP4_ERR_LAUNCH";
+    case FP4_ERR_DEVICE: return "FP4_ERR_DEVICE";
+    case FP4_ERR_WORKSPACE: return "FP4_ERR_WORKSPACE";
+    default: return "FP4_ERR_UNKNOWN";
+    }
+}
+
+} // extern "C"

@@ -1,0 +1,681 @@
+// gemm_tc.cu -- tensor-core grouped expert GEMM for prefill-sized row counts (sm_103a:
+// TMA, mbarrier pipeline, tcgen05.mma with the accumulator in tensor memory).
+//
+// Arithmetic (memra-engine 0.98.0, src/bin/dsv4_native_gemm_gate.rs, fn f64_ref): every
+// product e4m3(a) * s_a * E2M1(w) * ws is formed exactly and summed in f32. The MMA
+// kind that accepts FP8 A operands has only ue8m0 scales per 32, and the kind with e4m3
+// scales per 16 wants FP4 on both sides, so the exact route on this hardware is the bf16
+// MMA (kind::f16): both operands carry their scales and stay exact in bf16.
+//   A (M side) = weights:     bf16(E2M1 * e4m3 scale)  NVFP4 (<= 6 significant bits)
+//                             bf16(E2M1 * 2^(e-127))   MXFP4
+//   B (N side) = activations: bf16(e4m3 code * pow2 scale), written by the quantise pass
+//   D (TMEM)   = f32 [128 weight rows x N routed rows]; epilogue multiplies by scale2.
+//
+// Kernel structure: persistent, one CTA (10 warps) per SM, static round-robin over
+// tiles (expert, 256-row block of its routed rows, 128-row block of its weights),
+// weight-row block fastest so consecutive tiles share the activation block in L2.
+//   warp 0     TMA producer: activation tile (bf16, 128B swizzle), nibble tile, scales
+//   warp 1     TMEM owner and MMA issuer (one thread), 4 MMAs of K=16 per stage
+//   warps 2-5  converters: nibbles x scales -> bf16 A tile in the UMMA 128B-swizzle layout
+//   warps 6-9  epilogue: tcgen05.ld of the accumulator, x scale2, coalesced f32 stores
+// Two accumulators (2 x 256 TMEM columns) let the epilogue of one tile overlap the
+// main loop of the next. The MMA N of a tile is its routed-row count rounded up to 16,
+// so an expert's ragged last block costs at most 15 padded rows.
+//
+// Every mbarrier wait is bounded (about a second of clock64 cycles); on expiry the CTA
+// sets the TIMEOUT bit of the device error word, stops all roles, waits (bounded) for
+// its own copies and MMAs in flight, frees its tensor memory and returns.
+#include "common.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+namespace fp4moe {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int kMaxExperts = 1024;
+constexpr int kThreads = 320;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int NIB_BYTES = BM * BK / 2;
+constexpr int SC_BYTES = BM * 16;
+constexpr int STAGE_BYTES = B_BYTES + A_BYTES + NIB_BYTES + SC_BYTES;
+constexpr int TX_BYTES = B_BYTES + NIB_BYTES + SC_BYTES;
+constexpr int OFF_A = B_BYTES;
+constexpr int OFF_NIB = B_BYTES + A_BYTES;
+constexpr int OFF_SC = B_BYTES + A_BYTES + NIB_BYTES;
+constexpr int NUM_BARS = 3 * STAGES + 2 + 2 + 1;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + (kMaxExperts + 1) * 4;
+constexpr long long kTimeoutCycles = 2000000000LL;
+static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+
+struct Params {
+    const int32_t *offsets;  // nullable: one expert owning rows [0, P)
+    int E;
+    int64_t P;
+    int n;
+    int k;
+    int recipe;
+    int mt;  // weight-row blocks per expert
+    const float *scale2;  // nullable: scale2_host is used
+    float scale2_host;
+    float *out;
+    unsigned *err;
+};
+
+// CSR offset e, or the single-expert offsets {0, P} when the call has none.
+__device__ __forceinline__ int64_t offset_at(const Params &p, int e)
+{
+    return p.offsets ? (int64_t)__ldg(p.offsets + e) : (e == 0 ? 0 : p.P);
+}
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Bounded wait. Returns false if this CTA is aborting (flag set here or elsewhere).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          unsigned *err)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const long long t0 = clock64();
+    for (uint32_t spin = 1;; ++spin) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((spin & 255u) == 0u) {
+            if (*abort_flag)
+                return false;
+            if (clock64() - t0 > kTimeoutCycles) {
+                *abort_flag = 1;
+                raise_device_error(err, FP4_DEVERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag (used to drain in-flight work on abort).
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity)
+{
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > kTimeoutCycles / 4)
+            return;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before()
+{
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after()
+{
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     dst_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 operands, f32 accumulator.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, "
+                 "%9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, "
+                 "%25, %26, %27, %28, %29, %30, %31}, [%32];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                   "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),
+                   "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]),
+                   "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+                   "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
+                   "=r"(v[30]), "=r"(v[31])
+                 : "r"(taddr)
+                 : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle layout
+// (8-row groups of 128-byte rows, 16-byte chunks XOR-ed with the row index mod 8),
+// stride between 8-row groups 1024 bytes, tcgen05 descriptor version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr)
+{
+    uint64_t d = (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(16u >> 4) << 16;    // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024u >> 4) << 32;  // stride byte offset
+    d |= (uint64_t)1 << 46;             // descriptor version
+    d |= (uint64_t)2 << 61;             // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor of kind::f16: f32 accumulator, bf16 A and B, both K-major.
+__device__ __forceinline__ uint32_t idesc_bf16(int m, int n)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h)
+{
+    const __half2 v = *reinterpret_cast<const __half2 *>(&h);
+    return __half22float2(v);
+}
+
+// ------------------------------------------------------------------ tile schedule
+
+struct Tile {
+    int e;
+    int m;
+    int64_t row0;
+    int rows;
+};
+
+__device__ __forceinline__ Tile tile_at(int t, const int *prefix, const Params &p)
+{
+    const int E = p.E, mt = p.mt;
+    int lo = 0, hi = E;  // prefix[lo] <= t < prefix[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= t)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    Tile tl;
+    tl.e = lo;
+    const int local = t - prefix[lo];
+    const int j = local / mt;
+    tl.m = local - j * mt;
+    const int64_t r0 = offset_at(p, lo), r1 = offset_at(p, lo + 1);
+    tl.row0 = r0 + (int64_t)j * BN;
+    const int64_t left = r1 - tl.row0;
+    tl.rows = (int)(left < BN ? left : BN);
+    return tl;
+}
+
+// ------------------------------------------------------------------ the kernel
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmW,
+                   const __grid_constant__ CUtensorMap tmS, const Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NUM_BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *prefix = reinterpret_cast<int *>(tmem_slot + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto conv_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (3 * STAGES + 4);
+
+    // --- per-expert tile counts (validated offsets) and their prefix sums
+    const int E = p.E;
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        const int64_t r0 = offset_at(p, e), r1 = offset_at(p, e + 1);
+        const bool bad = r0 < 0 || r1 < r0 || r1 > p.P || (e == 0 && r0 != 0) ||
+                         (e == E - 1 && r1 != p.P);
+        int cnt = 0;
+        if (bad) {
+            if (blockIdx.x == 0)
+                raise_device_error(p.err, FP4_DEVERR_OFFSETS);
+        } else if (r1 > r0) {
+            cnt = (int)((r1 - r0 + BN - 1) / BN) * p.mt;
+        }
+        prefix[e + 1] = cnt;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(conv_bar(s), 4);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 4);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        prefix[0] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1)
+        tmem_alloc(smem_u32(tmem_slot), 512);
+    __syncthreads();
+    if (warp == 0) {  // prefix scan: each lane sums a contiguous chunk, then a warp scan
+        const int per = (E + 31) / 32;
+        const int lo = 1 + lane * per, hi = min(E + 1, lo + per);
+        int run = 0;
+        for (int i = lo; i < hi; ++i)
+            run += prefix[i];
+        int incl = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o)
+                incl += v;
+        }
+        int acc = incl - run;
+        for (int i = lo; i < hi; ++i) {
+            acc += prefix[i];
+            prefix[i] = acc;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = prefix[E];
+    const int nkb = p.k / BK;
+    const int gs = p.recipe == FP4_NVFP4 ? 16 : 32;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, issued_parity = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const Tile tl = tile_at(t, prefix, p);
+                const int yw = tl.e * p.n + tl.m * BM;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *st = smem + stage * STAGE_BYTES;
+                    mbar_arrive_expect_tx(full_bar(stage), TX_BYTES);
+                    tma_load_2d(smem_u32(st), &tmB, kb * BK, (int)tl.row0, full_bar(stage));
+                    tma_load_2d(smem_u32(st + OFF_NIB), &tmW, kb * (BK / 2), yw, full_bar(stage));
+                    tma_load_2d(smem_u32(st + OFF_SC), &tmS, ((kb * BK) / gs) & ~15, yw,
+                                full_bar(stage));
+                    issued_mask |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (*abort_flag) {  // let this CTA's own copies land before it exits
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued_mask & (1u << s))
+                        mbar_drain(full_bar(s), (issued_parity >> s) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int it = 0;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+                const Tile tl = tile_at(t, prefix, p);
+                const int nt = max(16, (tl.rows + 15) & ~15);
+                const uint32_t idesc = idesc_bf16(BM, nt);
+                const int buf = it & 1;
+                if (!mbar_wait(acce_bar(buf), ((it >> 1) & 1) ^ 1u, abort_flag, p.err))
+                    break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err) ||
+                        !mbar_wait(conv_bar(stage), phase, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint8_t *st = smem + stage * STAGE_BYTES;
+                    const uint64_t adesc = sw128_desc(smem_u32(st + OFF_A));
+                    const uint64_t bdesc = sw128_desc(smem_u32(st));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_bf16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+                                 (kb | kk) != 0 ? 1u : 0u);
+                    mma_commit(empty_bar(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok)
+                    mma_commit(accf_bar(buf));
+            }
+            mma_commit(drain_bar);  // completes once every MMA issued above has finished
+            mbar_drain(drain_bar, 0);
+        }
+    } else if (warp < 6) {
+        // ---------------------------------------------------------- converters
+        const int cw = warp - 2, c = lane & 7, rs = lane >> 3;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (int kb = 0; kb < nkb; ++kb) {
+                if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *st = smem + stage * STAGE_BYTES;
+                const uint8_t *nib = st + OFF_NIB;
+                const uint8_t *sc = st + OFF_SC;
+                uint8_t *a = const_cast<uint8_t *>(st) + OFF_A;
+                const int sidx = (gs == 16) ? (((kb * BK) >> 4) & 15) + (c >> 1)
+                                            : (((kb * BK) >> 5) & 15) + (c >> 2);
+#pragma unroll 4
+                for (int i = 0; i < 8; ++i) {
+                    const int r = cw * 32 + i * 4 + rs;
+                    const uint32_t wv = *reinterpret_cast<const uint32_t *>(nib + r * 32 + c * 4);
+                    const uint32_t sb = sc[r * 16 + sidx];
+                    const float s = (gs == 16) ? e4m3_to_f32(sb) : e8m0_to_f32(sb);
+                    uint32_t h[4];
+                    e2m1x8_to_f16x8(wv, h);
+                    uint4 o;
+                    float2 f;
+                    f = f16x2_to_f32x2(h[0]);
+                    o.x = pack_bf16x2(f.x * s, f.y * s);
+                    f = f16x2_to_f32x2(h[1]);
+                    o.y = pack_bf16x2(f.x * s, f.y * s);
+                    f = f16x2_to_f32x2(h[2]);
+                    o.z = pack_bf16x2(f.x * s, f.y * s);
+                    f = f16x2_to_f32x2(h[3]);
+                    o.w = pack_bf16x2(f.x * s, f.y * s);
+                    *reinterpret_cast<uint4 *>(a + r * 128 + ((c ^ (r & 7)) << 4)) = o;
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(conv_bar(stage));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        int it = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+            const Tile tl = tile_at(t, prefix, p);
+            const int buf = it & 1;
+            if (!mbar_wait(accf_bar(buf), (it >> 1) & 1, abort_flag, p.err))
+                break;
+            tc_fence_after();
+            const int col = tl.m * BM + q * 32 + lane;
+            const bool colok = col < p.n;
+            const float s2 =
+                (gs == 16) ? (p.scale2 ? __ldg(p.scale2 + tl.e) : p.scale2_host) : 1.0f;
+            float *orow = p.out + tl.row0 * (int64_t)p.n + col;
+            for (int c0 = 0; c0 < tl.rows; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c0), v);
+                if (colok) {
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj)
+                        if (c0 + jj < tl.rows)
+                            orow[(int64_t)(c0 + jj) * p.n] = __uint_as_float(v[jj]) * s2;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(acce_bar(buf));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+// ------------------------------------------------------------------ quantise pass
+
+// Routed row p of the workspace = bf16(e4m3 code * scale) of activation row x[row_ids[p]]
+// (fn quant_rows of dsv4_native_gemm_gate.rs; bf16 holds code * 2^m exactly).
+__global__ void __launch_bounds__(256) quant_ws_kernel(const float *__restrict__ x, int64_t T,
+                                                       const int32_t *__restrict__ row_ids,
+                                                       int64_t P, int k,
+                                                       uint2 *__restrict__ ws, unsigned *err)
+{
+    const int lane = threadIdx.x & 31;
+    const int kq = k >> 7;
+    const int64_t groups = P * kq;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t gi = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); gi < groups;
+         gi += warps) {
+        const int64_t pr = gi / kq;
+        const int g = (int)(gi - pr * kq);
+        const int64_t t = row_ids ? (int64_t)__ldg(row_ids + pr) : pr;
+        uint2 o = make_uint2(0u, 0u);
+        if (t >= 0 && t < T) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(x + t * k + g * 128) + lane);
+            float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+            amax = warp_max(amax);
+            const float s = group_scale(amax);
+            const float inv = pow2_reciprocal(s);
+            const uint32_t q = e4m3x4(scaled_clamped(v.x, inv), scaled_clamped(v.y, inv),
+                                      scaled_clamped(v.z, inv), scaled_clamped(v.w, inv));
+            const float2 lo = f16x2_to_f32x2(e4m3x2_to_f16x2(q & 0xFFFFu));
+            const float2 hi = f16x2_to_f32x2(e4m3x2_to_f16x2(q >> 16));
+            o.x = pack_bf16x2(lo.x * s, lo.y * s);
+            o.y = pack_bf16x2(hi.x * s, hi.y * s);
+        } else if (lane == 0 && g == 0) {
+            raise_device_error(err, FP4_DEVERR_ROW_ID);
+        }
+        ws[(pr * k + g * 128) / 4 + lane] = o;
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+static bool make_map(CUtensorMap *m, CUtensorMapDataType dt, int elem_bytes, const void *base,
+                     uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+                     CUtensorMapSwizzle swz)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * (uint64_t)elem_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+} // namespace tc
+
+size_t tc_workspace_bytes(int64_t total_rows, int64_t k, int recipe)
+{
+    (void)recipe;
+    return (size_t)total_rows * (size_t)k * 2 + 1024;
+}
+
+bool tc_supported(int64_t n, int64_t k, int recipe, int E)
+{
+    const int gs = recipe == FP4_NVFP4 ? 16 : 32;
+    if (k % (16 * gs) != 0 || k % tc::BK != 0)
+        return false;  // the scale tensor's rows must be whole 16-byte TMA units
+    if (E < 1 || E > tc::kMaxExperts || (int64_t)E * n >= ((int64_t)1 << 31))
+        return false;
+    return n >= 1;
+}
+
+cudaError_t launch_tc_gemm(const GroupedProblem &p, void *workspace, cudaStream_t s)
+{
+    using namespace tc;
+    if (!tc_supported(p.n, p.k, p.recipe, p.E))
+        return cudaErrorInvalidValue;
+    uint8_t *ws = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(workspace) + 1023) & ~(uintptr_t)1023);
+    int dev = 0, sms = 152;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+
+    // 1. quantise the routed rows into the bf16 workspace [P, k]
+    {
+        const int64_t groups = p.P * (p.k / 128);
+        const int64_t want = (groups + 7) / 8;
+        const int blocks = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
+        quant_ws_kernel<<<blocks, 256, 0, s>>>(p.x, p.T, p.row_ids, p.P, p.k,
+                                              reinterpret_cast<uint2 *>(ws), p.err);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+    }
+    // 2. tensor maps and the persistent GEMM
+    const int gs = p.recipe == FP4_NVFP4 ? 16 : 32;
+    alignas(64) CUtensorMap tmB, tmW, tmS;
+    if (!make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws, (uint64_t)p.k, (uint64_t)p.P, BK,
+                  BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w, (uint64_t)p.k / 2,
+                  (uint64_t)p.E * p.n, BK / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sc, (uint64_t)p.k / gs,
+                  (uint64_t)p.E * p.n, 16, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    Params kp;
+    kp.offsets = p.offsets;
+    kp.E = p.E;
+    kp.P = p.P;
+    kp.n = p.n;
+    kp.k = p.k;
+    kp.recipe = p.recipe;
+    kp.mt = (p.n + BM - 1) / BM;
+    kp.scale2 = p.scale2;
+    kp.scale2_host = p.scale2_host;
+    kp.out = p.out;
+    kp.err = p.err;
+    cudaError_t e =
+        cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess)
+        return e;
+    const int64_t max_tiles = ((p.P + BN - 1) / BN + p.E) * (int64_t)kp.mt;
+    const int grid = (int)(max_tiles < sms ? max_tiles : sms);
+    tc_gemm_kernel<<<grid, kThreads, SMEM_BYTES, s>>>(tmB, tmW, tmS, kp);
+    return cudaGetLastError();
+}
+
+// Summation depth for the tensor-core path: one f32 rounding per K=16 MMA step into the
+// TMEM accumulator (k/16 steps, products exact), one for the scale2 multiply in the
+// epilogue and one for the f32 rounding of ws = e4m3 * scale2 that the f64 reference
+// applies per group but this path does not.
+double tc_error_ops(int recipe, int64_t k)
+{
+    return (double)(k / 16) + (recipe == FP4_NVFP4 ? 2.0 : 0.0) + 1.0;
+}
+
+} // namespace fp4moe

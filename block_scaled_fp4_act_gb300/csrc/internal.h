@@ -1,0 +1,45 @@
+// internal.h -- declarations shared by the library's translation units (not exported).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/fp4moe.h"
+
+namespace fp4moe {
+
+// One grouped projection as the kernels see it. Single-expert calls use E = 1 and
+// offsets == nullptr (rows [0, P)).
+struct GroupedProblem {
+    const float *x;          // [T, k] f32
+    int64_t T;               // rows of x
+    const int32_t *row_ids;  // nullable [P]
+    const int32_t *offsets;  // nullable [E+1] (device)
+    int E;
+    int64_t P;               // routed rows
+    const uint8_t *w;        // [E, n, k/2]
+    const uint8_t *sc;       // [E, n, k/gs]
+    const float *scale2;     // nullable [E] (device)
+    float scale2_host;       // used when scale2 == nullptr (NVFP4)
+    int recipe;              // FP4_NVFP4 / FP4_MXFP4
+    float *out;              // [P, n]
+    int n;
+    int k;
+    uint8_t *codes_out;      // nullable [P, k]  (single-expert calls)
+    float *scales_out;       // nullable [P, k/128]
+    unsigned *err;           // device error word of the current device
+};
+
+// Address of the current device's error word (looked up once per device).
+unsigned *device_error_word();
+
+// Kernel launchers; each returns cudaSuccess or the launch error.
+cudaError_t launch_act_quant(const float *x, uint8_t *codes, float *scales, int64_t rows,
+                             int64_t k, cudaStream_t s);
+cudaError_t launch_stream_gemm(const GroupedProblem &p, int rows_per_pass, cudaStream_t s);
+
+// Error-model constants of each path (n_ops of |err| <= n_ops 2^-24 sum|p|).
+double stream_error_ops(int recipe, int64_t k);
+
+} // namespace fp4moe

@@ -1,0 +1,99 @@
+"""The C ABI without a GPU: the library loads, exports every function the header
+declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import block_scaled_fp4_act_gb300 as fp4
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp4moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fp4.build.build()
+    return fp4.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ["act_quant_fp8", "fp4_expert_gemm", "fp4_grouped_expert_gemm",
+                 "fp4_grouped_workspace_size", "fp4_get_device_error"]:
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", fp4.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_host_side_argument_checks(lib):
+    V = ctypes.c_void_p
+    a16 = V(0x10000)           # never dereferenced: every call below fails its checks first
+    odd = V(0x10004)
+    # act_quant_fp8
+    assert lib.act_quant_fp8(a16, a16, a16, 4, 100, None) == fp4.FP4_ERR_SHAPE
+    assert lib.act_quant_fp8(a16, a16, a16, -1, 128, None) == fp4.FP4_ERR_ARG
+    assert lib.act_quant_fp8(None, a16, a16, 4, 128, None) == fp4.FP4_ERR_ARG
+    assert lib.act_quant_fp8(odd, a16, a16, 4, 128, None) == fp4.FP4_ERR_ALIGN
+    assert lib.act_quant_fp8(None, None, None, 0, 128, None) == fp4.FP4_OK  # empty: no-op
+    # fp4_expert_gemm
+    g = lib.fp4_expert_gemm
+    assert g(a16, a16, a16, 1.0, 7, a16, 1, 1, 128, None, None, None, 0, None) == fp4.FP4_ERR_ARG
+    assert g(a16, a16, a16, 1.0, 0, a16, 1, 1, 96, None, None, None, 0, None) == fp4.FP4_ERR_SHAPE
+    assert g(a16, a16, a16, 1.0, 0, a16, 1, 0, 128, None, None, None, 0, None) == fp4.FP4_ERR_SHAPE
+    assert g(a16, None, a16, 1.0, 0, a16, 1, 4, 128, None, None, None, 0, None) == fp4.FP4_ERR_ARG
+    assert g(a16, a16, a16, 1.0, 0, odd, 1, 4, 128, None, None, None, 0, None) == fp4.FP4_ERR_ALIGN
+    assert g(a16, a16, a16, 1.0, 0, a16, 1, 4, 128, a16, None, None, 0, None) == fp4.FP4_ERR_ARG
+    assert g(None, None, None, 1.0, 0, None, 0, 4, 128, None, None, None, 0, None) == fp4.FP4_OK
+    # fp4_grouped_expert_gemm
+    G = lib.fp4_grouped_expert_gemm
+    assert G(a16, 8, None, a16, 0, 8, a16, a16, a16, 0, a16, 4, 128, None, 0, None) == \
+        fp4.FP4_ERR_ARG                                  # zero experts
+    assert G(a16, 8, None, a16, 2, 8, a16, a16, None, 0, a16, 4, 128, None, 0, None) == \
+        fp4.FP4_ERR_ARG                                  # NVFP4 without scale2
+    assert G(a16, 4, None, a16, 2, 8, a16, a16, a16, 0, a16, 4, 128, None, 0, None) == \
+        fp4.FP4_ERR_SHAPE                                # no row ids but fewer tokens than rows
+    assert G(a16, 8, None, a16, 2, 8, a16, a16, a16, 1, a16, 4, 130, None, 0, None) == \
+        fp4.FP4_ERR_SHAPE
+    assert G(a16, 8, None, a16, 2, 8, odd, a16, a16, 1, a16, 4, 128, None, 0, None) == \
+        fp4.FP4_ERR_ALIGN
+    assert G(a16, 8, None, a16, 2, 0, a16, a16, a16, 1, a16, 4, 128, None, 0, None) == fp4.FP4_OK
+
+
+def test_status_strings_and_error_model(lib):
+    assert lib.fp4_status_string(fp4.FP4_ERR_WORKSPACE) == b"FP4_ERR_WORKSPACE"
+    assert lib.fp4_status_string(123) == b"FP4_ERR_UNKNOWN"
+    for recipe, gs in ((fp4.NVFP4, 16), (fp4.MXFP4, 32)):
+        for k in (128, 1536, 4096, 7168):
+            n_ops = fp4.fp4_error_ops(fp4.PATH_STREAM, recipe, k)
+            # the pages' own kernel: (gs-1) + ceil(groups/128) + 7; ours is the same order
+            assert gs - 1 < n_ops <= (gs - 1) + k / 256 + 8
+
+
+def test_path_choice_by_shape(lib):
+    # decode-sized (about one row per expert) always streams
+    assert fp4.fp4_gemm_path(64, 64, 3072, 4096, fp4.NVFP4, True) == fp4.PATH_STREAM
+    # without a workspace there is only the streaming path
+    assert fp4.fp4_gemm_path(32768, 256, 2048, 7168, fp4.NVFP4, False) == fp4.PATH_STREAM
+    fp4.fp4_force_path(fp4.PATH_TC)
+    try:
+        assert fp4.fp4_gemm_path(64, 64, 3072, 4096, fp4.NVFP4, True) == fp4.PATH_TC
+    finally:
+        fp4.fp4_force_path(fp4.PATH_AUTO)
+    assert fp4.fp4_gemm_path(64, 64, 3072, 4096, fp4.NVFP4, True) == fp4.PATH_STREAM

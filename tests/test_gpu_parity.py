@@ -1,0 +1,280 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, on one GPU.
+
+act_quant codes and scales must be bit-exact; GEMM outputs must satisfy
+|gpu - f64 reference| <= n_ops 2^-24 sum|p| per output with the n_ops the library states
+for the path that ran, and max_rel <= 1e-3 (the error model and `rel` convention of the
+pages: dsv4_native_gemm_gate.rs, kernel_check.rs).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import block_scaled_fp4_act_gb300 as fp4
+from block_scaled_fp4_act_gb300 import synth
+from parity_util import (check_gemm, expert_reference, gemm_bound, grouped_sampled_check,
+                         run_projection, sample_rows, to_np)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    fp4.build.build()
+    fp4.lib()
+    torch.cuda.init()
+    fp4.fp4_force_path(fp4.PATH_AUTO)
+    yield
+    fp4.fp4_force_path(fp4.PATH_AUTO)
+
+
+def _gpu(a, dtype=None):
+    t = torch.as_tensor(np.ascontiguousarray(a))
+    return t.to(DEV) if dtype is None else t.to(device=DEV, dtype=dtype)
+
+
+# ------------------------------------------------------------------ act_quant
+
+@pytest.mark.parametrize("case", ["normal", "student_t", "outliers", "bf16", "tiny", "zeros"])
+def test_act_quant_bit_exact(case):
+    g = torch.Generator().manual_seed(hash(case) % 1000)
+    rows, k = 37, 1536
+    x = torch.randn(rows, k, generator=g)
+    if case == "student_t":
+        x = synth.student_t((rows, k), 3, g, "cpu")
+    elif case == "outliers":
+        x = synth.with_outliers(x, g, p=0.01)
+    elif case == "bf16":
+        x = synth.bf16_rounded(x)
+    elif case == "tiny":
+        x = x * 1e-6
+        x[0, :5] = torch.tensor([1e-40, -1e-42, 0.0, -0.0, 3e-39])
+    elif case == "zeros":
+        x[:5] = 0.0
+        x[5, :128] = -0.0
+    codes, scales = fp4.act_quant_fp8(x.to(DEV))
+    c_ref, s_ref = oracle.act_quant(x.numpy())
+    assert np.array_equal(to_np(scales).view(np.uint32), s_ref.view(np.uint32))
+    diff = np.flatnonzero(to_np(codes) != c_ref)
+    assert diff.size == 0, "first code mismatch at %d: x=%r gpu=%#x cpu=%#x" % (
+        diff[0], x.numpy().reshape(-1)[diff[0]], to_np(codes).reshape(-1)[diff[0]],
+        c_ref.reshape(-1)[diff[0]])
+
+
+def test_act_quant_golden_examples(golden_dir):
+    from test_oracle_pins import _parse_examples
+    ex = _parse_examples(golden_dir)
+    x = np.stack([e[1] for e in ex])
+    codes, scales = fp4.act_quant_fp8(_gpu(x))
+    for r, (ident, _, scale, want) in enumerate(ex):
+        assert to_np(scales)[r, 0] == scale, ident
+        for i, c in want.items():
+            assert to_np(codes)[r, i] == c, (ident, i)
+
+
+def test_act_quant_edge_shapes():
+    for rows, k in [(1, 128), (3, 256), (1, 7168), (4096 + 3, 128)]:
+        x = torch.randn(rows, k) * 3
+        codes, scales = fp4.act_quant_fp8(x.to(DEV))
+        c_ref, s_ref = oracle.act_quant(x.numpy())
+        assert np.array_equal(to_np(codes), c_ref)
+        assert np.array_equal(to_np(scales), s_ref)
+    # rows == 0 is a no-op
+    empty = torch.empty(0, 256, device=DEV)
+    c, s = fp4.act_quant_fp8(empty)
+    assert c.shape == (0, 256)
+
+
+def _sweep_chunk(start_bits, count):
+    """Codes of `count` consecutive f32 bit patterns starting at start_bits, computed by
+    act_quant with one 448 per group so that the group scale is exactly 1."""
+    groups = (count + 126) // 127
+    bits = torch.arange(start_bits, start_bits + groups * 127, dtype=torch.int64, device=DEV)
+    vals = bits.to(torch.int32).view(torch.float32)
+    last = start_bits + count - 1
+    vals = torch.where(bits <= last, vals, vals[count - 1])
+    x = torch.empty(groups, 128, device=DEV)
+    x[:, 0] = 448.0
+    x[:, 1:] = vals.view(groups, 127)
+    codes, scales = fp4.act_quant_fp8(x)
+    assert bool(torch.all(scales == 1.0))
+    return to_np(codes[:, 1:].reshape(-1)[:count])
+
+
+def test_act_quant_encoder_exhaustive_sweep():
+    """Every f32 in [-448, 448] (P-SWEEP): the GPU codes form the step function whose steps
+    are the oracle's thresholds, so every code equals the oracle's."""
+    thresholds = np.array([oracle.e4m3_threshold(c) for c in range(1, 0x7F)],
+                          dtype=np.float32).view(np.uint32).astype(np.int64)
+    top = int(np.array([448.0], dtype=np.float32).view(np.uint32)[0])
+    chunk = 127 << 19
+    for sign in (0, 0x80000000):
+        start = 0
+        while start <= top:
+            count = min(chunk, top + 1 - start)
+            codes = _sweep_chunk(start + sign if sign == 0 else
+                                 (start | sign) - (1 << 32), count)
+            mag = codes & 0x7F
+            assert np.all((codes & 0x80) == (0x80 if sign else 0))
+            first = oracle.e4m3_encode(np.array([start], dtype=np.uint32).view(np.float32))[0]
+            assert mag[0] == first
+            steps = np.flatnonzero(np.diff(mag.astype(np.int16)) != 0) + 1
+            assert np.all(np.diff(mag.astype(np.int16)) >= 0)
+            assert np.all(np.diff(mag.astype(np.int16)) <= 1)
+            want = thresholds[(thresholds > start) & (thresholds < start + count)] - start
+            assert np.array_equal(steps, want)
+            start += count
+
+
+# ------------------------------------------------------------------ single expert
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_expert_gemm_configs(cfg):
+    x, bank = synth.single_expert(cfg, device="cpu")
+    w, sc, s2 = bank.w[0], bank.sc[0], float(bank.scale2[0])
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=DEV)
+    scales = torch.empty(x.shape[0], x.shape[1] // 128, device=DEV)
+    out = fp4.fp4_expert_gemm(x.to(DEV), w.to(DEV), sc.to(DEV), s2, bank.recipe,
+                              codes_out=codes, scales_out=scales)
+    c_ref, s_ref, ref, absp = expert_reference(x.numpy(), w.numpy(), sc.numpy(), s2, bank.recipe)
+    assert np.array_equal(to_np(codes), c_ref) and np.array_equal(to_np(scales), s_ref)
+    n_ops = gemm_bound(fp4.PATH_STREAM, bank.recipe, x.shape[1])
+    check_gemm(to_np(out), ref, absp, n_ops, "c%d" % cfg)
+    out2 = fp4.fp4_expert_gemm(x.to(DEV), w.to(DEV), sc.to(DEV), s2, bank.recipe)
+    assert torch.equal(out, out2)
+
+
+@pytest.mark.parametrize("recipe", [fp4.NVFP4, fp4.MXFP4])
+@pytest.mark.parametrize("g,n,k", [(1, 1, 128), (3, 200, 256), (5, 64, 1536), (9, 129, 512),
+                                   (2, 70, 7168), (17, 100, 384)])
+def test_expert_gemm_shapes(recipe, g, n, k):
+    """Ragged n (not a multiple of the 64-column tile), short k (idle lanes), k that is
+    not a multiple of 1024, rows not a multiple of the rows per pass."""
+    rng = np.random.default_rng(g * 1000 + n + k + recipe)
+    x = (rng.standard_normal((g, k)) * rng.choice([1e-3, 1, 100], (g, 1))).astype(np.float32)
+    w = rng.integers(0, 256, (n, k // 2), dtype=np.uint8)
+    gs = fp4.group_size(recipe)
+    if recipe == fp4.NVFP4:
+        sc = rng.integers(0x08, 0x7E, (n, k // gs), dtype=np.uint8)
+        s2 = 5.9945243e-5
+    else:
+        sc = rng.integers(100, 150, (n, k // gs), dtype=np.uint8)
+        s2 = 0.0
+    out = fp4.fp4_expert_gemm(_gpu(x), _gpu(w), _gpu(sc), s2, recipe)
+    _, _, ref, absp = expert_reference(x, w, sc, s2, recipe)
+    check_gemm(to_np(out), ref, absp, gemm_bound(fp4.PATH_STREAM, recipe, k), "shape")
+
+
+@pytest.mark.parametrize("recipe", [fp4.NVFP4, fp4.MXFP4])
+def test_expert_gemm_exact_special_case(recipe, golden_dir):
+    """P-EXACT: lossless quantisation, unit weight scales -> bit-equal to a float64 matmul."""
+    from test_oracle_pins import _dense_weights, _exact_inputs, golden_e2m1
+    rng = np.random.default_rng(77 + recipe)
+    table = golden_e2m1(golden_dir)
+    for g, n, k in [(3, 5, 256), (8, 64, 1024), (4, 96, 2048)]:
+        x, w, sc = _exact_inputs(rng, g, n, k, recipe)
+        out = fp4.fp4_expert_gemm(_gpu(x), _gpu(w), _gpu(sc), 1.0, recipe)
+        want = x.astype(np.float64) @ _dense_weights(w, table).T
+        assert np.array_equal(to_np(out).astype(np.float64), want)
+
+
+# ------------------------------------------------------------------ grouped
+
+def _small_grouped(recipe, device=DEV, E=6, T=40, topk=3, n=136, k=512, empty=(1, 4)):
+    gen = torch.Generator(device="cpu").manual_seed(100 + recipe)
+    scores = torch.rand(T, E, generator=gen)
+    for e in empty:
+        scores[:, e] = -1.0
+    choices = torch.argsort(scores, dim=1, descending=True)[:, :topk]
+    r = synth.routing_from_choices(choices, E)
+    bank = synth.make_bank(recipe, E, n, k, 555, "cpu", scale2_value=5.9945243e-5)
+    x = torch.randn(T, k, generator=gen) * 4
+    proj = synth.Projection("small", x.to(device), synth.Routing(r.offsets.to(device),
+                                                                  r.row_ids.to(device)),
+                            synth.Bank(recipe, bank.w.to(device), bank.sc.to(device),
+                                       bank.scale2.to(device)))
+    return proj
+
+
+@pytest.mark.parametrize("recipe", [fp4.NVFP4, fp4.MXFP4])
+@pytest.mark.parametrize("path", [fp4.PATH_STREAM])
+def test_grouped_small_all_outputs(recipe, path):
+    proj = _small_grouped(recipe)
+    fp4.fp4_force_path(path)
+    try:
+        out, used = run_projection(proj)
+    finally:
+        fp4.fp4_force_path(fp4.PATH_AUTO)
+    assert used == path
+    P = proj.routing.P
+    grouped_sampled_check(proj, out, path, np.arange(P), "small grouped")
+    assert fp4.fp4_get_device_error() == 0
+
+
+def test_grouped_row_equals_single_row_launch():
+    """P-ROW: a routed row's output equals the single-expert call on that row alone."""
+    proj = _small_grouped(fp4.NVFP4)
+    fp4.fp4_force_path(fp4.PATH_STREAM)
+    try:
+        out, _ = run_projection(proj)
+    finally:
+        fp4.fp4_force_path(fp4.PATH_AUTO)
+    off = to_np(proj.routing.offsets)
+    rid = to_np(proj.routing.row_ids)
+    for p in [0, 5, int(off[-1]) - 1]:
+        e = int(np.searchsorted(off, p, side="right") - 1)
+        t = int(rid[p])
+        one = fp4.fp4_expert_gemm(proj.x[t:t + 1].contiguous(), proj.bank.w[e], proj.bank.sc[e],
+                                  float(proj.bank.scale2[e]), proj.bank.recipe)
+        assert torch.equal(one[0], out[p])
+
+
+def test_grouped_device_checks_flag_bad_routing():
+    proj = _small_grouped(fp4.NVFP4)
+    assert fp4.fp4_get_device_error() == 0
+    bad = proj.routing.row_ids.clone()
+    bad[3] = proj.x.shape[0] + 5
+    fp4.fp4_force_path(fp4.PATH_STREAM)
+    try:
+        fp4.fp4_grouped_expert_gemm(proj.x, bad, proj.routing.offsets, proj.bank.w, proj.bank.sc,
+                                    proj.bank.scale2, proj.bank.recipe)
+        assert fp4.fp4_get_device_error() & fp4.FP4_DEVERR_ROW_ID
+        off = proj.routing.offsets.clone()
+        off[2], off[3] = off[3].clone(), off[2].clone()
+        if int(off[2]) == int(off[3]):
+            off[2] += 1
+        fp4.fp4_grouped_expert_gemm(proj.x, proj.routing.row_ids, off, proj.bank.w,
+                                    proj.bank.sc, proj.bank.scale2, proj.bank.recipe)
+        assert fp4.fp4_get_device_error() & fp4.FP4_DEVERR_OFFSETS
+    finally:
+        fp4.fp4_force_path(fp4.PATH_AUTO)
+    # the context stays usable and the word is cleared
+    assert fp4.fp4_get_device_error() == 0
+    out, path = run_projection(proj)
+    grouped_sampled_check(proj, out, path, np.arange(proj.routing.P), "after errors")
+
+
+@pytest.mark.parametrize("scale2", [1.0 / 64.0, 5.9945243e-5])
+def test_grouped_decode_c3_full_size(scale2):
+    wl = synth.decode_c3(device=DEV, scale2_value=scale2)
+    rng = np.random.default_rng(3)
+    for proj in wl.projections:
+        out, path = run_projection(proj)
+        rows = np.arange(proj.routing.P)          # 64 routed rows: check them all
+        grouped_sampled_check(proj, out, path, rows, "c3 " + proj.name)
+    assert fp4.fp4_get_device_error() == 0
+    del rng
+
+
+@pytest.mark.parametrize("name", ["c4", "c5"])
+def test_grouped_prefill_full_size_sampled(name):
+    wl = synth.workload(name, device=DEV)
+    rng = np.random.default_rng(4)
+    for proj in wl.projections:
+        out, path = run_projection(proj)
+        rows = sample_rows(to_np(proj.routing.offsets).astype(np.int64), proj.routing.P, rng, 48)
+        grouped_sampled_check(proj, out, path, rows, "%s %s" % (name, proj.name))
+        del out
+    assert fp4.fp4_get_device_error() == 0

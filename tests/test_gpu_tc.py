@@ -1,0 +1,113 @@
+"""Parity of the tensor-core (tcgen05) path with the CPU oracle, through the C ABI.
+
+Small forced-path cases cover ragged weight-row blocks (n not a multiple of 128), ragged
+routed-row blocks (expert sizes around the 256-row block and the 16-row MMA step), empty
+experts and both recipes; the lossless special case must be bit-equal to a float64
+matmul.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import block_scaled_fp4_act_gb300 as fp4
+from block_scaled_fp4_act_gb300 import synth
+from parity_util import (check_gemm, expert_reference, gemm_bound, grouped_sampled_check,
+                         run_projection, to_np)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(autouse=True)
+def force_tc():
+    fp4.build.build()
+    fp4.fp4_force_path(fp4.PATH_TC)
+    yield
+    fp4.fp4_force_path(fp4.PATH_AUTO)
+
+
+def _projection(recipe, sizes, n, k, T=None, seed=0, scale2=5.9945243e-5):
+    """Grouped projection whose expert e has exactly sizes[e] routed rows (row ids drawn
+    at random from T tokens)."""
+    gen = torch.Generator().manual_seed(seed)
+    E = len(sizes)
+    P = int(sum(sizes))
+    T = T or max(P, 1)
+    offsets = torch.zeros(E + 1, dtype=torch.int32)
+    offsets[1:] = torch.cumsum(torch.tensor(sizes, dtype=torch.int64), 0).to(torch.int32)
+    row_ids = torch.randint(0, T, (P,), generator=gen, dtype=torch.int32)
+    bank = synth.make_bank(recipe, E, n, k, 900 + seed, "cpu", scale2_value=scale2)
+    x = torch.randn(T, k, generator=gen) * 3
+    return synth.Projection("tc", x.to(DEV), synth.Routing(offsets.to(DEV), row_ids.to(DEV)),
+                            synth.Bank(recipe, bank.w.to(DEV), bank.sc.to(DEV),
+                                       bank.scale2.to(DEV)))
+
+
+@pytest.mark.parametrize("recipe", [fp4.NVFP4, fp4.MXFP4])
+def test_tc_small_grouped_all_outputs(recipe):
+    proj = _projection(recipe, [5, 0, 16, 1, 33, 0, 17], n=136, k=512, T=40, seed=1)
+    out, path = run_projection(proj)
+    assert path == fp4.PATH_TC
+    worst, rel = grouped_sampled_check(proj, out, path, np.arange(proj.routing.P), "tc small")
+    assert fp4.fp4_get_device_error() == 0
+    print("tc small recipe %d: worst err/bound %.3g max_rel %.3g" % (recipe, worst, rel))
+
+
+@pytest.mark.parametrize("recipe", [fp4.NVFP4, fp4.MXFP4])
+def test_tc_multi_block_experts(recipe):
+    """Experts spanning several 256-row blocks with ragged tails, several weight blocks."""
+    proj = _projection(recipe, [257, 0, 512, 300, 15, 256], n=384, k=1024, T=600, seed=2)
+    out, path = run_projection(proj)
+    assert path == fp4.PATH_TC
+    worst, rel = grouped_sampled_check(proj, out, path, np.arange(proj.routing.P), "tc multi")
+    assert fp4.fp4_get_device_error() == 0
+    print("tc multi recipe %d: worst err/bound %.3g max_rel %.3g" % (recipe, worst, rel))
+
+
+@pytest.mark.parametrize("recipe", [fp4.NVFP4, fp4.MXFP4])
+def test_tc_exact_special_case(recipe, golden_dir):
+    """Lossless inputs: every partial sum is exact in f32, so the tensor-core result must
+    equal the float64 matmul bit for bit."""
+    from test_oracle_pins import _dense_weights, _exact_inputs, golden_e2m1
+    rng = np.random.default_rng(5 + recipe)
+    table = golden_e2m1(golden_dir)
+    for g, n, k in [(40, 128, 512), (300, 200, 2048)]:
+        x, w, sc = _exact_inputs(rng, g, n, k, recipe)
+        ws = fp4.workspace_for(g, g, n, k, recipe)
+        out = fp4.fp4_expert_gemm(torch.as_tensor(x).to(DEV), torch.as_tensor(w).to(DEV),
+                                  torch.as_tensor(sc).to(DEV), 1.0, recipe, workspace=ws)
+        want = x.astype(np.float64) @ _dense_weights(w, table).T
+        got = to_np(out).astype(np.float64)
+        bad = np.flatnonzero(got != want)
+        assert bad.size == 0, "first mismatch %d: got %r want %r" % (bad[0], got.reshape(-1)[bad[0]],
+                                                                    want.reshape(-1)[bad[0]])
+
+
+@pytest.mark.parametrize("recipe", [fp4.NVFP4, fp4.MXFP4])
+def test_tc_single_expert_with_workspace(recipe):
+    rng = np.random.default_rng(9 + recipe)
+    g, n, k = 100, 320, 2048
+    x = (rng.standard_normal((g, k)) * 2).astype(np.float32)
+    w = rng.integers(0, 256, (n, k // 2), dtype=np.uint8)
+    gs = fp4.group_size(recipe)
+    sc = (rng.integers(0x20, 0x41, (n, k // gs)) if recipe == fp4.NVFP4
+          else rng.integers(118, 135, (n, k // gs))).astype(np.uint8)
+    s2 = 1.0 / 64 if recipe == fp4.NVFP4 else 0.0
+    ws = fp4.workspace_for(g, g, n, k, recipe)
+    out = fp4.fp4_expert_gemm(torch.as_tensor(x).to(DEV), torch.as_tensor(w).to(DEV),
+                              torch.as_tensor(sc).to(DEV), s2, recipe, workspace=ws)
+    _, _, ref, absp = expert_reference(x, w, sc, s2, recipe)
+    worst, rel = check_gemm(to_np(out), ref, absp, gemm_bound(fp4.PATH_TC, recipe, k), "tc one")
+    print("tc single recipe %d: worst err/bound %.3g max_rel %.3g" % (recipe, worst, rel))
+
+
+def test_tc_matches_stream_path_closely():
+    """Both paths on the same inputs agree within the sum of their bounds."""
+    proj = _projection(fp4.NVFP4, [70, 3, 190], n=256, k=1024, T=100, seed=4)
+    out_tc, _ = run_projection(proj)
+    fp4.fp4_force_path(fp4.PATH_STREAM)
+    out_st, _ = run_projection(proj)
+    fp4.fp4_force_path(fp4.PATH_TC)
+    d = (out_tc - out_st).abs().max().item()
+    assert d <= 1e-3 * out_st.abs().max().item()
