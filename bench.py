@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--experts", type=int, default=0, help="override the workload's expert count")
+    ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count")
     ap.add_argument("--path", choices=["auto", "stream", "tc"], default="auto",
                     help="force a kernel path (default: the library's choice by shape)")
     return ap.parse_args()
@@ -356,7 +358,12 @@ def run_ours(args, world, rank, local):
     device = torch.device("cuda", torch.cuda.current_device())
     peaks, peak_src = load_peaks()
 
-    wl = synth.workload(args.workload, device=device)
+    kw = {}
+    if args.experts:
+        kw["E"] = args.experts
+    if args.tokens:
+        kw["T"] = args.tokens
+    wl = synth.workload(args.workload, device=device, **kw)
     calls = make_calls(fp4, wl, device)
     flops_step = sum(proj_flops(c["proj"]) for c in calls)
     bytes_step = sum(proj_bytes(c["proj"])[0] for c in calls)
@@ -412,7 +419,9 @@ def run_ours(args, world, rank, local):
               if tc else "e4m3 x e2m1 -> f32 (f16 operands, f32 accumulate)",
               "data": "synthetic (seeded; weights, routing and activations as the workload "
                       "recipe states)",
-              "config": {"workload": WORKLOAD_NAMES[args.workload], "paths": paths,
+              "config": {"workload": WORKLOAD_NAMES[args.workload] if not kw else
+                         "%s with overrides %s" % (WORKLOAD_NAMES[args.workload], kw),
+                         "paths": paths,
                          "flops_per_step": flops_step, "bytes_per_step": bytes_step,
                          "l2": "inputs larger than L2 (weights %.2f GB per step)" %
                                (sum(proj_bytes(c["proj"])[1] for c in calls) / 1e9),
