@@ -62,6 +62,9 @@ def lib():
         L.fp4_grouped_expert_gemm.argtypes = [P, i64, P, P, i32, i64, P, P, P, i32, P, i64, i64,
                                               P, sz, P]
         L.fp4_grouped_expert_gemm.restype = i32
+        L.fp4_grouped_expert_gemm_noalloc.argtypes = [P, i64, P, P, i32, i64, P, P, P, i32, P,
+                                                       i64, i64, P]
+        L.fp4_grouped_expert_gemm_noalloc.restype = i32
         L.fp4_gemm_path.argtypes = [i64, i32, i64, i64, i32, i32]
         L.fp4_gemm_path.restype = i32
         L.fp4_error_ops.argtypes = [i32, i32, i64]
@@ -186,6 +189,35 @@ def fp4_grouped_expert_gemm(x, row_ids, offsets, w, wscale, scale2, recipe, out=
                                          _ptr(wscale), _ptr(scale2), int(recipe), _ptr(out), n, k,
                                          _ptr(workspace), ws_bytes, _stream(stream)),
            "fp4_grouped_expert_gemm")
+    return out
+
+
+def fp4_grouped_expert_gemm_noalloc(x, row_ids, offsets, w, wscale, scale2, recipe, out=None,
+                                    stream=None):
+    """As fp4_grouped_expert_gemm, for callers that cannot allocate device memory: runs the
+    tensor-core path with the library's fixed 32 MiB scratch (total_rows*k*2+1024 bytes at
+    most) instead of a workspace. Calls that overlap on the GPU race on that scratch."""
+    import torch
+    T, k = x.shape
+    E, n = w.shape[0], w.shape[1]
+    _need(x, torch.float32, None, "x")
+    _need(offsets, torch.int32, (E + 1,), "offsets")
+    if row_ids is not None:
+        _need(row_ids, torch.int32, None, "row_ids")
+        P = row_ids.numel()
+    else:
+        P = T
+    _need(w, torch.uint8, (E, n, k // 2), "w")
+    _need(wscale, torch.uint8, (E, n, k // group_size(recipe)), "wscale")
+    if scale2 is not None:
+        _need(scale2, torch.float32, (E,), "scale2")
+    if out is None:
+        out = torch.empty((P, n), dtype=torch.float32, device=x.device)
+    _need(out, torch.float32, (P, n), "out")
+    _check(lib().fp4_grouped_expert_gemm_noalloc(_ptr(x), T, _ptr(row_ids), _ptr(offsets), E, P,
+                                                 _ptr(w), _ptr(wscale), _ptr(scale2), int(recipe),
+                                                 _ptr(out), n, k, _stream(stream)),
+           "fp4_grouped_expert_gemm_noalloc")
     return out
 
 

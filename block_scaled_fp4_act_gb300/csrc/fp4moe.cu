@@ -44,6 +44,12 @@ static int record(cudaError_t e)
     return FP4_ERR_LAUNCH;
 }
 
+// Lets other translation units report a message through fp4_last_error.
+void set_last_error(const char *msg)
+{
+    snprintf(g_last_error, sizeof(g_last_error), "%s", msg);
+}
+
 static bool aligned16(const void *p)
 {
     return (reinterpret_cast<uintptr_t>(p) & 15u) == 0u;

@@ -31,6 +31,9 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <mutex>
+#include <stdio.h>
+
 namespace fp4moe {
 namespace tc {
 
@@ -679,3 +682,120 @@ double tc_error_ops(int recipe, int64_t k)
 }
 
 } // namespace fp4moe
+
+// ------------------------------------------------------------------ allocation-free variant
+//
+// Some callers cannot call cudaMalloc: a host framework that owns every device byte and
+// forbids libraries to allocate, a real-time serving loop with a no-allocation rule after
+// start-up, or code whose allocator would synchronise the device at the wrong moment. For
+// them the tensor-core path can run with its workspace in a fixed, file-scope device
+// array instead of caller memory. The array is part of this library's image, so every
+// GPU that loads the library holds it until the process exits.
+
+namespace fp4moe {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)32 << 20;  // 32 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch array on the current device, looked up once per device
+// (in host code the array's name is only a stand-in, never a device address).
+static uint8_t *noalloc_scratch(cudaError_t *status)
+{
+    static std::mutex mu;
+    static uint8_t *addr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        *status = e != cudaSuccess ? e : cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) {
+            *status = e;
+            return nullptr;
+        }
+        addr[dev] = static_cast<uint8_t *>(p);
+    }
+    *status = cudaSuccess;
+    return addr[dev];
+}
+
+void set_last_error(const char *msg);
+
+} // namespace fp4moe
+
+extern "C" int fp4_grouped_expert_gemm_noalloc(const float *x, int64_t num_tokens,
+                                               const int32_t *row_ids, const int32_t *offsets,
+                                               int num_experts, int64_t total_rows,
+                                               const uint8_t *w, const uint8_t *wscale,
+                                               const float *scale2, int recipe, float *out,
+                                               int64_t n, int64_t k, void *stream)
+{
+    using namespace fp4moe;
+    if ((recipe != FP4_NVFP4 && recipe != FP4_MXFP4) || num_experts < 1 ||
+        num_experts > 65535 || num_tokens < 0 || total_rows < 0 || n < 0 || k < 0)
+        return FP4_ERR_ARG;
+    if (k == 0 || k % 128 != 0 || n == 0 || k > (1 << 20) || n > (1 << 24) ||
+        total_rows > ((int64_t)1 << 31))
+        return FP4_ERR_SHAPE;
+    if (total_rows == 0)
+        return FP4_OK;
+    if (!x || !offsets || !w || !wscale || !out || (recipe == FP4_NVFP4 && !scale2))
+        return FP4_ERR_ARG;
+    if (!row_ids && num_tokens < total_rows)
+        return FP4_ERR_SHAPE;
+    auto a16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0u; };
+    if (!a16(x) || !a16(w) || !a16(wscale) || !a16(out))
+        return FP4_ERR_ALIGN;
+    if (!tc_supported(n, k, recipe, num_experts))
+        return FP4_ERR_SHAPE;
+    const size_t need = tc_workspace_bytes(total_rows, k, recipe);
+    if (need > kNoAllocScratchBytes) {
+        char msg[256];
+        snprintf(msg, sizeof(msg),
+                 "fp4_grouped_expert_gemm_noalloc: total_rows*k*2+1024 = %zu bytes exceeds the "
+                 "fixed %zu-byte scratch",
+                 need, kNoAllocScratchBytes);
+        set_last_error(msg);
+        return FP4_ERR_WORKSPACE;
+    }
+    cudaError_t st = cudaSuccess;
+    uint8_t *scratch = noalloc_scratch(&st);
+    if (!scratch) {
+        char msg[256];
+        snprintf(msg, sizeof(msg), "scratch address lookup failed: %s", cudaGetErrorString(st));
+        set_last_error(msg);
+        return FP4_ERR_LAUNCH;
+    }
+    GroupedProblem p{};
+    p.x = x;
+    p.T = num_tokens;
+    p.row_ids = row_ids;
+    p.offsets = offsets;
+    p.E = num_experts;
+    p.P = total_rows;
+    p.w = w;
+    p.sc = wscale;
+    p.scale2 = recipe == FP4_NVFP4 ? scale2 : nullptr;
+    p.scale2_host = 1.0f;
+    p.recipe = recipe;
+    p.out = out;
+    p.n = (int)n;
+    p.k = (int)k;
+    p.codes_out = nullptr;
+    p.scales_out = nullptr;
+    p.err = device_error_word();
+    if (!p.err)
+        return FP4_ERR_LAUNCH;
+    const cudaError_t e = launch_tc_gemm(p, scratch, (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+        char msg[256];
+        snprintf(msg, sizeof(msg), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+        set_last_error(msg);
+        return FP4_ERR_LAUNCH;
+    }
+    return FP4_OK;
+}

@@ -114,6 +114,30 @@ int fp4_grouped_expert_gemm(const float *x, int64_t num_tokens, const int32_t *r
                             int recipe, float *out, int64_t n, int64_t k, void *workspace,
                             size_t workspace_bytes, void *stream);
 
+/*
+ * fp4_grouped_expert_gemm_noalloc -- the same computation as fp4_grouped_expert_gemm,
+ * on the tensor-core path, for callers that cannot allocate device memory (a host
+ * framework that owns all device memory and forbids libraries to allocate, a serving
+ * loop with a no-allocation rule after start-up, or code where an allocation would
+ * synchronise the device at the wrong time). It takes no workspace: its scratch is a
+ * fixed 32 MiB device array inside this library, which every GPU that loads the library
+ * holds until the process exits. The pages have no counterpart of this call.
+ *   Arguments: as fp4_grouped_expert_gemm without workspace/workspace_bytes.
+ *   Limit: total_rows * k * 2 + 1024 <= 32 MiB (e.g. 2048 routed rows at k = 7168);
+ *          larger calls return FP4_ERR_WORKSPACE (message in fp4_last_error), shapes the
+ *          tensor-core path does not take (k not a multiple of 16*gs, more than 1024
+ *          experts) return FP4_ERR_SHAPE. Nothing is allocated, freed or synchronised.
+ *   First call on a device: looks up the scratch array's device address for that
+ *          device (cudaGetSymbolAddress), so make it before any stream capture.
+ *   Sharing: every call uses the same array and leaves its contents behind; nothing in
+ *          it needs to start at zero. Calls whose kernels overlap on the GPU (other
+ *          streams, other threads) race on it: serialise them.
+ */
+int fp4_grouped_expert_gemm_noalloc(const float *x, int64_t num_tokens, const int32_t *row_ids,
+                                    const int32_t *offsets, int num_experts, int64_t total_rows,
+                                    const uint8_t *w, const uint8_t *wscale, const float *scale2,
+                                    int recipe, float *out, int64_t n, int64_t k, void *stream);
+
 /* Which path a grouped call of this shape takes (never FP4_PATH_AUTO). */
 int fp4_gemm_path(int64_t total_rows, int num_experts, int64_t n, int64_t k, int recipe,
                   int have_workspace);
