@@ -73,10 +73,11 @@ static int choose_path(int64_t P, int E, int64_t n, int64_t k, int recipe, bool 
     return FP4_PATH_STREAM;
 }
 
+// Rows the streaming kernel quantises per pass: 4 when experts average 3+ rows, else 2.
 static int stream_rows_per_pass(int64_t P, int E)
 {
     const int64_t avg = E > 0 ? (P + E - 1) / E : P;
-    return avg >= 3 ? 4 : (avg >= 2 ? 2 : 2);
+    return avg >= 3 ? 4 : 2;
 }
 
 // Shared shape checks; returns FP4_OK or the status to report.

@@ -11,13 +11,17 @@
 //   B (N side) = activations: bf16(e4m3 code * pow2 scale), written by the quantise pass
 //   D (TMEM)   = f32 [128 weight rows x N routed rows]; epilogue multiplies by scale2.
 //
-// Kernel structure: persistent, one CTA (10 warps) per SM, static round-robin over
+// Kernel structure: persistent, one CTA (23 warps) per SM, static round-robin over
 // tiles (expert, 256-row block of its routed rows, 128-row block of its weights),
 // weight-row block fastest so consecutive tiles share the activation block in L2.
-//   warp 0     TMA producer: activation tile (bf16, 128B swizzle), nibble tile, scales
-//   warp 1     TMEM owner and MMA issuer (one thread), 4 MMAs of K=16 per stage
-//   warps 2-5  converters: nibbles x scales -> bf16 A tile in the UMMA 128B-swizzle layout
-//   warps 6-9  epilogue: tcgen05.ld of the accumulator, x scale2, coalesced f32 stores
+// Three shared-memory rings decouple the streams: a 12-deep weight ring (nibbles +
+// scales, 6 KB a stage, ~72 KB in flight: weights stream from HBM once per tile), a
+// 3-deep ring of converted bf16 weight tiles and a 3-deep activation ring.
+//   warp 1      TMEM owner and MMA issuer (one thread), 4 MMAs of K=16 per stage
+//   warp 5      TMA producer of activation slots (bf16, 128B swizzle, k-block-major)
+//   warp 9      TMA producer of nibble and scale tiles
+//   16 warps    converters: nibbles x scales -> bf16 A tile in the UMMA 128B-swizzle layout
+//   4 warps     epilogue: tcgen05.ld of the accumulator, x scale2, coalesced f32 stores
 // Two accumulators (2 x 256 TMEM columns) let the epilogue of one tile overlap the
 // main loop of the next. The MMA N of a tile is its routed-row count rounded up to 16,
 // so an expert's ragged last block costs at most 15 padded rows.
@@ -40,22 +44,54 @@ namespace tc {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
+constexpr int W_STAGES = 12;  // weight ring (nibbles + scales): deep, it streams from HBM
+constexpr int A_STAGES = 3;   // converted bf16 weight tiles
+constexpr int B_STAGES = 3;   // activation tiles (mostly L2 hits: shared by a tile's neighbours)
 constexpr int kMaxExperts = 1024;
-constexpr int kThreads = 320;
+constexpr int kConvWarps = 16;
+constexpr int kThreads = 24 * 32;
+// Warp roles. Warp w issues on SM sub-partition w % 4, and the single MMA-issuing thread
+// must not compete for issue slots with busy converter warps, so sub-partition 1 holds
+// the MMA issuer, both TMA producers, one converter and one epilogue warp, and the other
+// 15 converters fill sub-partitions 0, 2 and 3. Epilogue warps 20, 17, 22, 23 cover the
+// four TMEM lane quarters (a warp reads lanes 32 * (w % 4) .. + 31).
+constexpr int kWarpMma = 1, kWarpB = 5, kWarpW = 9;
+enum { ROLE_IDLE, ROLE_MMA, ROLE_PROD, ROLE_CONV, ROLE_EPI };
+__device__ __forceinline__ int warp_role(int w)
+{
+    if (w == kWarpMma)
+        return ROLE_MMA;
+    if (w == kWarpB || w == kWarpW)
+        return ROLE_PROD;
+    if (w == 17 || w >= 20 && w != 21)
+        return ROLE_EPI;
+    if (w == 21)
+        return ROLE_IDLE;
+    return ROLE_CONV;
+}
+// Converter index 0..15 of converter warp w (rows 8 * index .. + 7).
+__device__ __forceinline__ int conv_index(int w)
+{
+    // converters: 0,2,3,4,6,7,8,10,11,12,13,14,15,16,18,19
+    return w == 0 ? 0 : w < 4 ? w - 1 : w < 5 ? 3 : w < 9 ? w - 2 : w < 13 ? w - 3 : w < 17 ? w - 3 : w - 4;
+}
+// Activation tiles are loaded k-block-major: one 32 KB TMA box holds up to 8 k-blocks of
+// a small tile (32 rows x 8, 64 x 4, 128 x 2, 256 x 1), so small tiles keep many k-stages
+// in flight in the same three ring slots.
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int NIB_BYTES = BM * BK / 2;
 constexpr int SC_BYTES = BM * 16;
-constexpr int STAGE_BYTES = B_BYTES + A_BYTES + NIB_BYTES + SC_BYTES;
-constexpr int TX_BYTES = B_BYTES + NIB_BYTES + SC_BYTES;
-constexpr int OFF_A = B_BYTES;
-constexpr int OFF_NIB = B_BYTES + A_BYTES;
-constexpr int OFF_SC = B_BYTES + A_BYTES + NIB_BYTES;
-constexpr int NUM_BARS = 3 * STAGES + 2 + 2 + 1;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + (kMaxExperts + 1) * 4;
+constexpr int W_BYTES = NIB_BYTES + SC_BYTES;
+constexpr int OFF_A = B_STAGES * B_BYTES;
+constexpr int OFF_W = OFF_A + A_STAGES * A_BYTES;
+constexpr int RING_BYTES = OFF_W + W_STAGES * W_BYTES;
+constexpr int NUM_BARS = 2 * (W_STAGES + A_STAGES + B_STAGES) + 2 + 2 + 1;
+constexpr int SMEM_BYTES = 1024 + RING_BYTES + NUM_BARS * 8 + 16 + (kMaxExperts + 1) * 4;
 constexpr long long kTimeoutCycles = 2000000000LL;
-static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
+static_assert(B_BYTES % 1024 == 0 && A_BYTES % 1024 == 0 && OFF_W % 1024 == 0,
+              "swizzled tiles need 1024-byte alignment");
+static_assert(kThreads <= 1024, "block size");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 struct Params {
@@ -113,6 +149,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep in hardware (up to ~10 ms) until the phase
+// completes instead of returning at once, so waiting warps do not take issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity), "r"(10000000u)
+                 : "memory");
+    return ok != 0;
+}
+
 // Bounded wait. Returns false if this CTA is aborting (flag set here or elsewhere).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                           unsigned *err)
@@ -120,17 +170,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     if (mbar_try_wait(bar, parity))
         return true;
     const long long t0 = clock64();
-    for (uint32_t spin = 1;; ++spin) {
-        if (mbar_try_wait(bar, parity))
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity))
             return true;
-        if ((spin & 255u) == 0u) {
-            if (*abort_flag)
-                return false;
-            if (clock64() - t0 > kTimeoutCycles) {
-                *abort_flag = 1;
-                raise_device_error(err, FP4_DEVERR_TIMEOUT);
-                return false;
-            }
+        if (*abort_flag)
+            return false;
+        if (clock64() - t0 > kTimeoutCycles) {
+            *abort_flag = 1;
+            raise_device_error(err, FP4_DEVERR_TIMEOUT);
+            return false;
         }
     }
 }
@@ -150,6 +198,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
     asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
                  " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
                  "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            int z, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
                  : "memory");
 }
 
@@ -250,6 +307,60 @@ __device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h)
     return __half22float2(v);
 }
 
+// prmt with the PTX default mode: a selector nibble with bit 3 set replicates the sign
+// bit of the selected byte (used below to turn E2M1 sign bits into 0xFF/0x80 bytes).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// e4m3 scale byte -> (s, s) as bf16x2, exact (4 significant bits).
+__device__ __forceinline__ uint32_t e4m3_to_bf16x2(uint32_t byte)
+{
+    const float f = e4m3_to_f32(byte);
+    return pack_bf16x2(f, f);
+}
+
+// e8m0 scale byte -> (2^(e-127), 2^(e-127)) as bf16x2 (bf16 keeps f32's exponent range;
+// e = 0 is the subnormal 2^-127 = 0x0040).
+__device__ __forceinline__ uint32_t e8m0_to_bf16x2(uint32_t e)
+{
+    const uint32_t v = e == 0u ? 0x0040u : (e << 7);
+    return v | (v << 16);
+}
+
+// Eight E2M1 nibbles (k order, low nibble first) -> eight bf16 values times the bf16x2
+// scale, exactly (<= 6 significant bits). The bf16 of an E2M1 magnitude m (0..7) has a
+// high byte from {00,3F,3F,3F,40,40,40,40} and a low byte from {00,00,80,C0,00,40,80,C0}:
+// two prmt table lookups per four nibbles, the sign bit added to the high byte, then two
+// prmt interleaves into bf16 pairs.
+__device__ __forceinline__ void e2m1x8_to_bf16x8(uint32_t w, uint32_t scale2, uint4 &out)
+{
+    constexpr uint32_t LT0 = 0xC0800000u, LT1 = 0xC0804000u;  // low bytes, m = 0..3 / 4..7
+    constexpr uint32_t HT0 = 0x3F3F3F00u, HT1 = 0x40404040u;  // high bytes
+    const uint32_t sel = w & 0x77777777u;
+    const uint32_t selh = sel >> 16, wh = w >> 16;
+    const uint32_t l0 = prmt(LT0, LT1, sel), l1 = prmt(LT0, LT1, selh);
+    uint32_t h0 = prmt(HT0, HT1, sel), h1 = prmt(HT0, HT1, selh);
+    const uint32_t s0 = prmt(0x80808080u, 0x80808080u, w);   // 0xFF where negative, else 0x80
+    const uint32_t s1 = prmt(0x80808080u, 0x80808080u, wh);
+    h0 |= (s0 << 1) & 0x80808080u;
+    h1 |= (s1 << 1) & 0x80808080u;
+    out.x = mul_bf16x2(prmt(l0, h0, 0x5140u), scale2);
+    out.y = mul_bf16x2(prmt(l0, h0, 0x7362u), scale2);
+    out.z = mul_bf16x2(prmt(l1, h1, 0x5140u), scale2);
+    out.w = mul_bf16x2(prmt(l1, h1, 0x7362u), scale2);
+}
+
 // ------------------------------------------------------------------ tile schedule
 
 struct Tile {
@@ -284,26 +395,56 @@ __device__ __forceinline__ Tile tile_at(int t, const int *prefix, const Params &
 
 // ------------------------------------------------------------------ the kernel
 
+// Ring cursor: slot index and phase parity of a stage sequence over an N-slot ring.
+template <int N>
+struct Ring {
+    int slot = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void next()
+    {
+        if (++slot == N) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+// Activation tensor maps for tiles of <= 32, 64, 128 and 256 rows: 3-D views {64 k,
+// rows, k-blocks} of the [P, k] bf16 workspace with boxes {64, 32 << i, 8 >> i}.
+struct BMaps {
+    CUtensorMap m[4];
+};
+
+__device__ __forceinline__ int bmap_index(int rows)
+{
+    return rows <= 32 ? 0 : rows <= 64 ? 1 : rows <= 128 ? 2 : 3;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmW,
+    tc_gemm_kernel(const __grid_constant__ BMaps tmB, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmS, const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + RING_BYTES);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *prefix = reinterpret_cast<int *>(tmem_slot + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t bar0 = smem_u32(bars);
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto conv_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
-    auto accf_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + b); };
-    auto acce_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (3 * STAGES + 4);
+    // barrier map: weight full/empty, A full/empty, B full/empty, accumulator full/empty, drain
+    auto wfull = [&](int s) { return bar0 + 8u * s; };
+    auto wempty = [&](int s) { return bar0 + 8u * (W_STAGES + s); };
+    auto afull = [&](int s) { return bar0 + 8u * (2 * W_STAGES + s); };
+    auto aempty = [&](int s) { return bar0 + 8u * (2 * W_STAGES + A_STAGES + s); };
+    auto bfull = [&](int s) { return bar0 + 8u * (2 * W_STAGES + 2 * A_STAGES + s); };
+    auto bempty = [&](int s) { return bar0 + 8u * (2 * W_STAGES + 2 * A_STAGES + B_STAGES + s); };
+    constexpr int kAcc = 2 * (W_STAGES + A_STAGES + B_STAGES);
+    auto accf = [&](int b) { return bar0 + 8u * (kAcc + b); };
+    auto acce = [&](int b) { return bar0 + 8u * (kAcc + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (kAcc + 4);
 
     // --- per-expert tile counts (validated offsets) and their prefix sums
     const int E = p.E;
@@ -321,21 +462,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefix[e + 1] = cnt;
     }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(conv_bar(s), 4);
-            mbar_init(empty_bar(s), 1);
+        for (int s = 0; s < W_STAGES; ++s) {
+            mbar_init(wfull(s), 1);
+            mbar_init(wempty(s), kConvWarps);
+        }
+        for (int s = 0; s < A_STAGES; ++s) {
+            mbar_init(afull(s), kConvWarps);
+            mbar_init(aempty(s), 1);
+        }
+        for (int s = 0; s < B_STAGES; ++s) {
+            mbar_init(bfull(s), 1);
+            mbar_init(bempty(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), 4);
+            mbar_init(accf(b), 1);
+            mbar_init(acce(b), 4);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         prefix[0] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1)
+    if (warp == kWarpMma)
         tmem_alloc(smem_u32(tmem_slot), 512);
     __syncthreads();
     if (warp == 0) {  // prefix scan: each lane sums a contiguous chunk, then a warp scan
@@ -364,47 +512,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int total = prefix[E];
     const int nkb = p.k / BK;
     const int gs = p.recipe == FP4_NVFP4 ? 16 : 32;
+    uint8_t *const ringB = smem;
+    uint8_t *const ringA = smem + OFF_A;
+    uint8_t *const ringW = smem + OFF_W;
 
-    if (warp == 0) {
-        // ---------------------------------------------------------- TMA producer
+    const int role = warp_role(warp);
+    if (role == ROLE_PROD) {
+        // ---------------------------------------------------------- TMA producers
+        // warp 0: activation slots into the B ring; warp 2: nibbles + scales into the W ring
         if (lane == 0) {
-            int stage = 0;
+            const bool is_b = warp == kWarpB;
+            const int nslots = is_b ? B_STAGES : W_STAGES;
+            int slot = 0;
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const Tile tl = tile_at(t, prefix, p);
                 const int yw = tl.e * p.n + tl.m * BM;
-                for (int kb = 0; kb < nkb; ++kb) {
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+                const int bi = bmap_index(tl.rows);
+                const int kbps = 8 >> bi;
+                const int nload = is_b ? (nkb + kbps - 1) / kbps : nkb;
+                for (int j = 0; j < nload; ++j) {
+                    const uint32_t emp = is_b ? bempty(slot) : wempty(slot);
+                    const uint32_t ful = is_b ? bfull(slot) : wfull(slot);
+                    if (!mbar_wait(emp, phase ^ 1u, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
-                    uint8_t *st = smem + stage * STAGE_BYTES;
-                    mbar_arrive_expect_tx(full_bar(stage), TX_BYTES);
-                    tma_load_2d(smem_u32(st), &tmB, kb * BK, (int)tl.row0, full_bar(stage));
-                    tma_load_2d(smem_u32(st + OFF_NIB), &tmW, kb * (BK / 2), yw, full_bar(stage));
-                    tma_load_2d(smem_u32(st + OFF_SC), &tmS, ((kb * BK) / gs) & ~15, yw,
-                                full_bar(stage));
-                    issued_mask |= 1u << stage;
-                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == STAGES) {
-                        stage = 0;
+                    if (is_b) {
+                        mbar_arrive_expect_tx(ful, B_BYTES);
+                        tma_load_3d(smem_u32(ringB + slot * B_BYTES), &tmB.m[bi], 0, (int)tl.row0,
+                                    j * kbps, ful);
+                    } else {
+                        uint8_t *dst = ringW + slot * W_BYTES;
+                        mbar_arrive_expect_tx(ful, W_BYTES);
+                        tma_load_2d(smem_u32(dst), &tmW, j * (BK / 2), yw, ful);
+                        tma_load_2d(smem_u32(dst + NIB_BYTES), &tmS, ((j * BK) / gs) & ~15, yw,
+                                    ful);
+                    }
+                    issued_mask |= 1u << slot;
+                    issued_parity = (issued_parity & ~(1u << slot)) | (phase << slot);
+                    if (++slot == nslots) {
+                        slot = 0;
                         phase ^= 1u;
                     }
                 }
             }
             if (*abort_flag) {  // let this CTA's own copies land before it exits
-                for (int s = 0; s < STAGES; ++s)
+                for (int s = 0; s < nslots; ++s)
                     if (issued_mask & (1u << s))
-                        mbar_drain(full_bar(s), (issued_parity >> s) & 1u);
+                        mbar_drain(is_b ? bfull(s) : wfull(s), (issued_parity >> s) & 1u);
             }
         }
-    } else if (warp == 1) {
+    } else if (role == ROLE_MMA) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
+            Ring<A_STAGES> ra;
+            Ring<B_STAGES> rb;
             bool ok = true;
             int it = 0;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
@@ -412,92 +577,88 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nt = max(16, (tl.rows + 15) & ~15);
                 const uint32_t idesc = idesc_bf16(BM, nt);
                 const int buf = it & 1;
-                if (!mbar_wait(acce_bar(buf), ((it >> 1) & 1) ^ 1u, abort_flag, p.err))
+                if (!mbar_wait(acce(buf), ((it >> 1) & 1) ^ 1u, abort_flag, p.err))
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+                const int bi = bmap_index(tl.rows);
+                const int kbps = 8 >> bi;
+                const int kb_bytes = (32 << bi) * 128;  // one k-block of the slot
                 for (int kb = 0; kb < nkb; ++kb) {
-                    if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err) ||
-                        !mbar_wait(conv_bar(stage), phase, abort_flag, p.err)) {
+                    const int j = kb % kbps;
+                    if ((j == 0 && !mbar_wait(bfull(rb.slot), rb.phase, abort_flag, p.err)) ||
+                        !mbar_wait(afull(ra.slot), ra.phase, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    uint8_t *st = smem + stage * STAGE_BYTES;
-                    const uint64_t adesc = sw128_desc(smem_u32(st + OFF_A));
-                    const uint64_t bdesc = sw128_desc(smem_u32(st));
+                    const uint64_t adesc = sw128_desc(smem_u32(ringA + ra.slot * A_BYTES));
+                    const uint64_t bdesc =
+                        sw128_desc(smem_u32(ringB + rb.slot * B_BYTES + j * kb_bytes));
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
                         mma_bf16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
                                  (kb | kk) != 0 ? 1u : 0u);
-                    mma_commit(empty_bar(stage));
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
+                    mma_commit(aempty(ra.slot));
+                    ra.next();
+                    if (j == kbps - 1 || kb == nkb - 1) {
+                        mma_commit(bempty(rb.slot));
+                        rb.next();
                     }
                 }
                 if (ok)
-                    mma_commit(accf_bar(buf));
+                    mma_commit(accf(buf));
             }
             mma_commit(drain_bar);  // completes once every MMA issued above has finished
             mbar_drain(drain_bar, 0);
         }
-    } else if (warp < 6) {
+    } else if (role == ROLE_CONV) {
         // ---------------------------------------------------------- converters
-        const int cw = warp - 2, c = lane & 7, rs = lane >> 3;
-        int stage = 0;
-        uint32_t phase = 0;
+        // Item = 16 weights of one row: lane -> (row rs, 16-weight chunk cp); warp cw owns
+        // rows [8 cw, 8 cw + 8).
+        const int cw = conv_index(warp), cp = lane & 3, rs = lane >> 2;
+        const int r = cw * 8 + rs;
+        Ring<W_STAGES> rw;
+        Ring<A_STAGES> ra;
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             for (int kb = 0; kb < nkb; ++kb) {
-                if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err)) {
+                if (!mbar_wait(wfull(rw.slot), rw.phase, abort_flag, p.err) ||
+                    !mbar_wait(aempty(ra.slot), ra.phase ^ 1u, abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
-                const uint8_t *st = smem + stage * STAGE_BYTES;
-                const uint8_t *nib = st + OFF_NIB;
-                const uint8_t *sc = st + OFF_SC;
-                uint8_t *a = const_cast<uint8_t *>(st) + OFF_A;
-                const int sidx = (gs == 16) ? (((kb * BK) >> 4) & 15) + (c >> 1)
-                                            : (((kb * BK) >> 5) & 15) + (c >> 2);
-#pragma unroll 4
-                for (int i = 0; i < 8; ++i) {
-                    const int r = cw * 32 + i * 4 + rs;
-                    const uint32_t wv = *reinterpret_cast<const uint32_t *>(nib + r * 32 + c * 4);
-                    const uint32_t sb = sc[r * 16 + sidx];
-                    const float s = (gs == 16) ? e4m3_to_f32(sb) : e8m0_to_f32(sb);
-                    uint32_t h[4];
-                    e2m1x8_to_f16x8(wv, h);
-                    uint4 o;
-                    float2 f;
-                    f = f16x2_to_f32x2(h[0]);
-                    o.x = pack_bf16x2(f.x * s, f.y * s);
-                    f = f16x2_to_f32x2(h[1]);
-                    o.y = pack_bf16x2(f.x * s, f.y * s);
-                    f = f16x2_to_f32x2(h[2]);
-                    o.z = pack_bf16x2(f.x * s, f.y * s);
-                    f = f16x2_to_f32x2(h[3]);
-                    o.w = pack_bf16x2(f.x * s, f.y * s);
-                    *reinterpret_cast<uint4 *>(a + r * 128 + ((c ^ (r & 7)) << 4)) = o;
-                }
+                const uint8_t *w = ringW + rw.slot * W_BYTES;
+                const int sidx = (gs == 16) ? (((kb * BK) >> 4) & 15) + cp
+                                            : (((kb * BK) >> 5) & 15) + (cp >> 1);
+                const uint2 wv = *reinterpret_cast<const uint2 *>(w + r * 32 + cp * 8);
+                const uint32_t sb = w[NIB_BYTES + r * 16 + sidx];
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(wempty(rw.slot));  // weight slot consumed
+                const uint32_t s2 = (gs == 16) ? e4m3_to_bf16x2(sb) : e8m0_to_bf16x2(sb);
+                uint4 o0, o1;
+                e2m1x8_to_bf16x8(wv.x, s2, o0);
+                e2m1x8_to_bf16x8(wv.y, s2, o1);
+                uint8_t *row = ringA + ra.slot * A_BYTES + r * 128;
+                *reinterpret_cast<uint4 *>(row + (((2 * cp) ^ (r & 7)) << 4)) = o0;
+                *reinterpret_cast<uint4 *>(row + (((2 * cp + 1) ^ (r & 7)) << 4)) = o1;
                 fence_proxy_async();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(conv_bar(stage));
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
+                    mbar_arrive(afull(ra.slot));
+                rw.next();
+                ra.next();
             }
         }
-    } else {
+    } else if (role == ROLE_EPI) {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;
         int it = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
             const Tile tl = tile_at(t, prefix, p);
             const int buf = it & 1;
-            if (!mbar_wait(accf_bar(buf), (it >> 1) & 1, abort_flag, p.err))
+            if (!mbar_wait(accf(buf), (it >> 1) & 1, abort_flag, p.err))
                 break;
             tc_fence_after();
             const int col = tl.m * BM + q * 32 + lane;
@@ -518,13 +679,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(acce_bar(buf));
+                mbar_arrive(acce(buf));
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem_base, 512);
     }
@@ -582,6 +743,22 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
     }
     return fn;
+}
+
+// 3-D map {64 k, rows, k-blocks} over a [rows, k] bf16 matrix, box {64, box_rows, box_kb}.
+static bool make_map_kblocks(CUtensorMap *m, const void *base, uint64_t k, uint64_t rows,
+                             uint32_t box_rows, uint32_t box_kb)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[3] = {(cuuint64_t)BK, rows, k / BK};
+    cuuint64_t strides[2] = {k * 2, (cuuint64_t)BK * 2};
+    cuuint32_t box[3] = {(cuuint32_t)BK, box_rows, box_kb};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 static bool make_map(CUtensorMap *m, CUtensorMapDataType dt, int elem_bytes, const void *base,
@@ -642,9 +819,12 @@ cudaError_t launch_tc_gemm(const GroupedProblem &p, void *workspace, cudaStream_
     }
     // 2. tensor maps and the persistent GEMM
     const int gs = p.recipe == FP4_NVFP4 ? 16 : 32;
-    alignas(64) CUtensorMap tmB, tmW, tmS;
-    if (!make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws, (uint64_t)p.k, (uint64_t)p.P, BK,
-                  BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    alignas(64) BMaps tmB;
+    alignas(64) CUtensorMap tmW, tmS;
+    for (int i = 0; i < 4; ++i)
+        if (!make_map_kblocks(&tmB.m[i], ws, (uint64_t)p.k, (uint64_t)p.P, 32u << i, 8u >> i))
+            return cudaErrorInvalidValue;
+    if (
         !make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w, (uint64_t)p.k / 2,
                   (uint64_t)p.E * p.n, BK / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sc, (uint64_t)p.k / gs,

@@ -5,7 +5,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/fp4moe.h"
+#include "fp4moe.h"  // include/ is on the compiler include path
 
 namespace fp4moe {
 
