@@ -208,9 +208,13 @@ def proj_bytes(proj):
 
 
 def launches_per_call(fp4, proj, have_ws):
+    """Kernels of ours one grouped call launches: the streaming kernel alone, or the
+    tensor-core path's quantise pass(es) + GEMM (NVFP4: f16 pass, conditional bf16 pass)."""
     path = fp4.fp4_gemm_path(proj.routing.P, proj.bank.E, proj.bank.n, proj.bank.k,
                              proj.bank.recipe, have_ws)
-    return path, (2 if path == fp4.PATH_TC else 1)
+    if path != fp4.PATH_TC:
+        return path, 1
+    return path, (3 if proj.bank.recipe == fp4.NVFP4 else 2)
 
 
 # ------------------------------------------------------------------ our arm

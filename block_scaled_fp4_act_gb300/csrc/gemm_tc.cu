@@ -106,6 +106,10 @@ struct Params {
     float scale2_host;
     float *out;
     unsigned *err;
+    // f16 route (NVFP4): route_flag == 0 after the quantise pass means the workspace holds
+    // f16(code * 2^(m - M_p)) and rowscale[p] = 2^M_p; nonzero (or no flag) means bf16.
+    const unsigned *route_flag;
+    const float *rowscale;
 };
 
 // CSR offset e, or the single-expert offsets {0, P} when the call has none.
@@ -287,10 +291,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr)
     return d;
 }
 
-// Instruction descriptor of kind::f16: f32 accumulator, bf16 A and B, both K-major.
-__device__ __forceinline__ uint32_t idesc_bf16(int m, int n)
+// Instruction descriptor of kind::f16: f32 accumulator, A and B both bf16 (fmt 1) or both
+// f16 (fmt 0), both K-major.
+__device__ __forceinline__ uint32_t idesc_f16kind(int m, int n, uint32_t fmt)
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(n >> 3) << 17) |
            ((uint32_t)(m >> 4) << 24);
 }
 
@@ -298,6 +303,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
 
@@ -324,6 +336,18 @@ __device__ __forceinline__ void e2m1x8_scaled_bf16(uint32_t w, float s, uint4 &o
     out.z = pack_bf16x2(f.x * s, f.y * s);
     f = f16x2_to_f32x2(h[3]);
     out.w = pack_bf16x2(f.x * s, f.y * s);
+}
+
+// Eight E2M1 nibbles times an e4m3 scale (as f16x2) -> eight f16, exactly: E2M1 x e4m3
+// has <= 6 significant bits and lies in [2^-10, 2688], inside f16's normal range.
+__device__ __forceinline__ void e2m1x8_scaled_f16(uint32_t w, uint32_t scale_h2, uint4 &out)
+{
+    uint32_t h[4];
+    e2m1x8_to_f16x8(w, h);
+    uint32_t *o = &out.x;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[j]) : "r"(h[j]), "r"(scale_h2));
 }
 
 // ------------------------------------------------------------------ tile schedule
@@ -475,6 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int total = prefix[E];
+    const bool f16_route = p.route_flag != nullptr && *((volatile const unsigned *)p.route_flag) == 0u;
     const int nkb = p.k / BK;
     const int gs = p.recipe == FP4_NVFP4 ? 16 : 32;
     uint8_t *const ringB = smem;
@@ -543,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
                 const Tile tl = tile_at(t, prefix, p);
                 const int nt = max(16, (tl.rows + 15) & ~15);
-                const uint32_t idesc = idesc_bf16(BM, nt);
+                const uint32_t idesc = idesc_f16kind(BM, nt, f16_route ? 0u : 1u);
                 const int buf = it & 1;
                 if (!mbar_wait(acce(buf), ((it >> 1) & 1) ^ 1u, abort_flag, p.err))
                     break;
@@ -604,10 +629,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(wempty(rw.slot));  // weight slot consumed
-                const float sf = (gs == 16) ? e4m3_to_f32(sb) : e8m0_to_f32(sb);
                 uint4 o0, o1;
-                e2m1x8_scaled_bf16(wv.x, sf, o0);
-                e2m1x8_scaled_bf16(wv.y, sf, o1);
+                if (f16_route) {  // NVFP4 only
+                    const uint32_t sh = e4m3x2_to_f16x2(sb | (sb << 8));
+                    e2m1x8_scaled_f16(wv.x, sh, o0);
+                    e2m1x8_scaled_f16(wv.y, sh, o1);
+                } else {
+                    const float sf = (gs == 16) ? e4m3_to_f32(sb) : e8m0_to_f32(sb);
+                    e2m1x8_scaled_bf16(wv.x, sf, o0);
+                    e2m1x8_scaled_bf16(wv.y, sf, o1);
+                }
                 uint8_t *row = ringA + ra.slot * A_BYTES + r * 128;
                 *reinterpret_cast<uint4 *>(row + (((2 * cp) ^ (r & 7)) << 4)) = o0;
                 *reinterpret_cast<uint4 *>(row + (((2 * cp + 1) ^ (r & 7)) << 4)) = o1;
@@ -637,11 +668,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c0 = 0; c0 < tl.rows; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c0), v);
-                if (colok) {
+                // f16 route: column (routed row) scale 2^M_p, exact; lane j holds row c0 + j
+                float rs = 1.0f;
+                if (f16_route && c0 + lane < tl.rows)
+                    rs = __ldg(p.rowscale + tl.row0 + c0 + lane);
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj)
-                        if (c0 + jj < tl.rows)
-                            orow[(int64_t)(c0 + jj) * p.n] = __uint_as_float(v[jj]) * s2;
+                for (int jj = 0; jj < 32; ++jj) {
+                    // f16_route is uniform over the CTA, so every lane takes the shuffle
+                    const float r = f16_route ? __shfl_sync(0xFFFFFFFFu, rs, jj) : 1.0f;
+                    if (colok && c0 + jj < tl.rows)
+                        orow[(int64_t)(c0 + jj) * p.n] = (__uint_as_float(v[jj]) * r) * s2;
                 }
             }
             tc_fence_before();
@@ -662,12 +698,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------ quantise pass
 
 // Routed row p of the workspace = bf16(e4m3 code * scale) of activation row x[row_ids[p]]
-// (fn quant_rows of dsv4_native_gemm_gate.rs; bf16 holds code * 2^m exactly).
+// (fn quant_rows of dsv4_native_gemm_gate.rs; bf16 holds code * 2^m exactly). With
+// only_if set, the kernel runs only when *only_if is nonzero (the f16 quantise pass found a
+// row whose block scales span more than f16 can hold exactly) and then replaces the whole
+// f16 workspace by bf16.
 __global__ void __launch_bounds__(256) quant_ws_kernel(const float *__restrict__ x, int64_t T,
                                                        const int32_t *__restrict__ row_ids,
                                                        int64_t P, int k,
-                                                       uint2 *__restrict__ ws, unsigned *err)
+                                                       uint2 *__restrict__ ws, unsigned *err,
+                                                       const unsigned *only_if)
 {
+    if (only_if && *((volatile const unsigned *)only_if) == 0u)
+        return;
     const int lane = threadIdx.x & 31;
     const int kq = k >> 7;
     const int64_t groups = P * kq;
@@ -694,6 +736,88 @@ __global__ void __launch_bounds__(256) quant_ws_kernel(const float *__restrict__
             raise_device_error(err, FP4_DEVERR_ROW_ID);
         }
         ws[(pr * k + g * 128) / 4 + lane] = o;
+    }
+}
+
+// Largest exponent gap between a row's block scales that f16 still holds exactly: codes
+// are multiples of 2^-9, so code * 2^-15 is a multiple of 2^-24, f16's finest spacing.
+constexpr int kF16MaxScaleGap = 15;
+
+// f16 quantise pass (NVFP4): one CTA (8 warps) per routed row. Pass 1 finds the row's
+// block scales 2^m_b (warps split the 128-groups) and, through shared memory, their
+// largest exponent M_p; pass 2 (re-reading the row from L1) writes f16(code * 2^(m_b - M_p))
+// (exact when every m_b >= M_p - 15) and rowscale[p] = 2^M_p, which the GEMM epilogue
+// applies per routed row. A row with a wider gap sets *route_flag; the bf16 pass then
+// rewrites the whole workspace.
+__global__ void __launch_bounds__(256) quant_ws_f16_kernel(const float *__restrict__ x, int64_t T,
+                                                           const int32_t *__restrict__ row_ids,
+                                                           int64_t P, int k,
+                                                           uint2 *__restrict__ ws,
+                                                           float *__restrict__ rowscale,
+                                                           unsigned *route_flag, unsigned *err)
+{
+    extern __shared__ uint32_t sexp[];  // [k/128] biased exponent of each block scale
+    __shared__ uint32_t red[2][8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kq = k >> 7;
+    for (int64_t pr = blockIdx.x; pr < P; pr += gridDim.x) {
+        const int64_t t = row_ids ? (int64_t)__ldg(row_ids + pr) : pr;
+        if (t < 0 || t >= T) {  // uniform over the CTA
+            if (threadIdx.x == 0) {
+                raise_device_error(err, FP4_DEVERR_ROW_ID);
+                rowscale[pr] = 1.0f;
+            }
+            for (int g = warp; g < kq; g += 8)
+                ws[(pr * k + g * 128) / 4 + lane] = make_uint2(0u, 0u);
+            continue;
+        }
+        const float4 *xr = reinterpret_cast<const float4 *>(x + t * k);
+        uint32_t emax = 0u, emin = 255u;
+        for (int g = warp; g < kq; g += 8) {
+            const float4 v = __ldg(xr + g * 32 + lane);
+            float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+            amax = warp_max(amax);
+            const uint32_t e = __float_as_uint(group_scale(amax)) >> 23;
+            if (lane == 0)
+                sexp[g] = e;
+            emax = max(emax, e);
+            emin = min(emin, e);
+        }
+        if (lane == 0) {
+            red[0][warp] = emax;
+            red[1][warp] = emin;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            emax = max(emax, red[0][w]);
+            emin = min(emin, red[1][w]);
+        }
+        const bool wide = emin + kF16MaxScaleGap < emax;
+        if (wide) {
+            if (threadIdx.x == 0)
+                atomicOr(route_flag, 1u);  // the bf16 pass rewrites every row
+        } else {
+            if (threadIdx.x == 0)
+                rowscale[pr] = __uint_as_float(emax << 23);
+            for (int g = warp; g < kq; g += 8) {
+                const float4 v = __ldg(xr + g * 32 + lane);
+                const uint32_t e = sexp[g];
+                const float sc = __uint_as_float(e << 23);
+                const float inv = pow2_reciprocal(sc);
+                const uint32_t q = e4m3x4(scaled_clamped(v.x, inv), scaled_clamped(v.y, inv),
+                                          scaled_clamped(v.z, inv), scaled_clamped(v.w, inv));
+                // 2^(m_b - M_p) in [2^-15, 1], exact in f32
+                const float rel = __uint_as_float((e + 127u - emax) << 23);
+                const float2 lo = f16x2_to_f32x2(e4m3x2_to_f16x2(q & 0xFFFFu));
+                const float2 hi = f16x2_to_f32x2(e4m3x2_to_f16x2(q >> 16));
+                uint2 o;
+                o.x = pack_f16x2(lo.x * rel, lo.y * rel);
+                o.y = pack_f16x2(hi.x * rel, hi.y * rel);
+                ws[(pr * k + g * 128) / 4 + lane] = o;
+            }
+        }
+        __syncthreads();  // sexp and red are reused by the next row
     }
 }
 
@@ -747,10 +871,16 @@ static bool make_map(CUtensorMap *m, CUtensorMapDataType dt, int elem_bytes, con
 
 } // namespace tc
 
+// Workspace: [activations P x k x 2 B, 1024-aligned][rowscale P x 4 B][route flag 16 B].
+static size_t ws_act_bytes(int64_t total_rows, int64_t k)
+{
+    return ((size_t)total_rows * (size_t)k * 2 + 1023) & ~(size_t)1023;
+}
+
 size_t tc_workspace_bytes(int64_t total_rows, int64_t k, int recipe)
 {
     (void)recipe;
-    return (size_t)total_rows * (size_t)k * 2 + 1024;
+    return 1024 + ws_act_bytes(total_rows, k) + (size_t)total_rows * 4 + 16;
 }
 
 bool tc_supported(int64_t n, int64_t k, int recipe, int E)
@@ -774,13 +904,37 @@ cudaError_t launch_tc_gemm(const GroupedProblem &p, void *workspace, cudaStream_
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
 
-    // 1. quantise the routed rows into the bf16 workspace [P, k]
+    float *rowscale = reinterpret_cast<float *>(ws + ws_act_bytes(p.P, p.k));
+    unsigned *route_flag = reinterpret_cast<unsigned *>(rowscale + p.P);
+    const bool nvfp4 = p.recipe == FP4_NVFP4;
+
+    // 1. quantise the routed rows into the workspace [P, k]: NVFP4 first tries f16 with a
+    //    per-row power-of-two scale (cheaper weight conversion in the GEMM); if any row's
+    //    block scales span more than f16 holds exactly, the bf16 pass rewrites all rows.
+    //    MXFP4 weights times 2^(e-127) need bf16's range, so MXFP4 always takes bf16.
     {
         const int64_t groups = p.P * (p.k / 128);
         const int64_t want = (groups + 7) / 8;
         const int blocks = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
+        if (nvfp4) {
+            cudaError_t e = cudaMemsetAsync(route_flag, 0, sizeof(unsigned), s);
+            if (e != cudaSuccess)
+                return e;
+            const int rblocks = (int)(p.P < (int64_t)sms * 8 ? p.P : (int64_t)sms * 8);
+            const size_t qsmem = (size_t)(p.k / 128) * sizeof(uint32_t);
+            if (qsmem > 48 * 1024) {
+                e = cudaFuncSetAttribute(quant_ws_f16_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)qsmem);
+                if (e != cudaSuccess)
+                    return e;
+            }
+            quant_ws_f16_kernel<<<rblocks, 256, qsmem, s>>>(p.x, p.T, p.row_ids, p.P, p.k,
+                                                       reinterpret_cast<uint2 *>(ws), rowscale,
+                                                       route_flag, p.err);
+        }
         quant_ws_kernel<<<blocks, 256, 0, s>>>(p.x, p.T, p.row_ids, p.P, p.k,
-                                              reinterpret_cast<uint2 *>(ws), p.err);
+                                              reinterpret_cast<uint2 *>(ws), p.err,
+                                              nvfp4 ? route_flag : nullptr);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
             return e;
@@ -808,6 +962,8 @@ cudaError_t launch_tc_gemm(const GroupedProblem &p, void *workspace, cudaStream_
     kp.mt = (p.n + BM - 1) / BM;
     kp.scale2 = p.scale2;
     kp.scale2_host = p.scale2_host;
+    kp.route_flag = nvfp4 ? route_flag : nullptr;
+    kp.rowscale = rowscale;
     kp.out = p.out;
     kp.err = p.err;
     cudaError_t e =

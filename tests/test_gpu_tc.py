@@ -111,3 +111,43 @@ def test_tc_matches_stream_path_closely():
     fp4.fp4_force_path(fp4.PATH_TC)
     d = (out_tc - out_st).abs().max().item()
     assert d <= 1e-3 * out_st.abs().max().item()
+
+
+def _scaled_rows_projection(recipe, gaps, n=256, k=1024, seed=7):
+    """One expert; routed row r has its 128-blocks scaled by 2^-u, u uniform in [0, gaps[r]]
+    (block scale spread of about 2^gaps[r] within the row)."""
+    rng = np.random.default_rng(seed)
+    rows = len(gaps)
+    x = rng.standard_normal((rows, k))
+    for r, gmax in enumerate(gaps):
+        u = rng.uniform(0, gmax, k // 128)
+        u[0], u[-1] = 0.0, gmax
+        x[r] *= np.repeat(np.exp2(-u), 128)
+    x = x.astype(np.float32)
+    return _projection_from(recipe, x, n, k, seed)
+
+
+def _projection_from(recipe, x, n, k, seed):
+    rows = x.shape[0]
+    offsets = torch.tensor([0, rows], dtype=torch.int32)
+    row_ids = torch.arange(rows, dtype=torch.int32)
+    bank = synth.make_bank(recipe, 1, n, k, 910 + seed, "cpu", scale2_value=5.9945243e-5)
+    return synth.Projection("scaled", torch.as_tensor(x).to(DEV),
+                            synth.Routing(offsets.to(DEV), row_ids.to(DEV)),
+                            synth.Bank(recipe, bank.w.to(DEV), bank.sc.to(DEV),
+                                       bank.scale2.to(DEV)))
+
+
+@pytest.mark.parametrize("recipe", [fp4.NVFP4, fp4.MXFP4])
+def test_tc_rows_with_wide_block_scale_spread(recipe):
+    """Block scales spread up to about 2^12 within a row keep the NVFP4 f16 activation route
+    (small codes become f16 subnormals); a row spread over 2^30 sends the whole call to the
+    bf16 route. Both must stay within the bound."""
+    for gaps, tag in [([0, 6, 10, 12] * 10, "f16"), ([0, 6, 30, 3] * 10, "bf16")]:
+        proj = _scaled_rows_projection(recipe, gaps)
+        out, path = run_projection(proj)
+        assert path == fp4.PATH_TC
+        worst, rel = grouped_sampled_check(proj, out, path, np.arange(proj.routing.P),
+                                           "spread %s" % tag)
+        assert fp4.fp4_get_device_error() == 0
+        print("spread %s recipe %d: worst err/bound %.3g max_rel %.3g" % (tag, recipe, worst, rel))
