@@ -17,7 +17,10 @@
 // Three shared-memory rings decouple the streams: a 12-deep weight ring (nibbles +
 // scales, 6 KB a stage, ~72 KB in flight: weights stream from HBM once per tile), a
 // 3-deep ring of converted bf16 weight tiles and a 3-deep activation ring.
-//   warp 1      TMEM owner and MMA issuer (one thread), 4 MMAs of K=16 per stage
+//   warp 1      TMEM owner and MMA issuer (whole warp, one elected lane issues), 4 MMAs
+//               of K=16 per stage
+//   warp 21     relay: does the MMA side's mbarrier waits and releases each A slot to
+//               warp 1 through a hardware named barrier
 //   warp 5      TMA producer of activation slots (bf16, 128B swizzle, k-block-major)
 //   warp 9      TMA producer of nibble and scale tiles
 //   16 warps    converters: nibbles x scales -> bf16 A tile in the UMMA 128B-swizzle layout
@@ -26,9 +29,20 @@
 // main loop of the next. The MMA N of a tile is its routed-row count rounded up to 16,
 // so an expert's ragged last block costs at most 15 padded rows.
 //
+// The MMA warp touches no mbarrier and no shared memory inside a tile. A wait or load
+// issued behind queued MMAs completes only once those MMAs have been handed to the tensor
+// core, so a per-stage mbarrier wait in the issuing warp idles the tensor pipe for about
+// 130 cycles a stage (measured on GB300: 340 cycles per 4-MMA stage at N <= 128 against
+// 256 without it). The relay warp takes those waits and passes readiness on with
+// bar.arrive / bar.sync, which do not go through that queue.
+//
 // Every mbarrier wait is bounded (about a second of clock64 cycles); on expiry the CTA
 // sets the TIMEOUT bit of the device error word, stops all roles, waits (bounded) for
-// its own copies and MMAs in flight, frees its tensor memory and returns.
+// its own copies and MMAs in flight, frees its tensor memory and returns. The MMA warp's
+// named-barrier waits cannot time out, so on abort the relay keeps releasing slots to the
+// end of the current tile, each only after the MMA warp has consumed the slot's previous
+// use (a bounded wait on the slot's empty barrier); the MMA warp checks the abort flag at
+// every tile start.
 #include "common.cuh"
 
 #include <cuda.h>
@@ -56,7 +70,8 @@ constexpr int kThreads = 24 * 32;
 // 15 converters fill sub-partitions 0, 2 and 3. Epilogue warps 20, 17, 22, 23 cover the
 // four TMEM lane quarters (a warp reads lanes 32 * (w % 4) .. + 31).
 constexpr int kWarpMma = 1, kWarpB = 5, kWarpW = 9;
-enum { ROLE_IDLE, ROLE_MMA, ROLE_PROD, ROLE_CONV, ROLE_EPI };
+constexpr int kWarpRelay = 21;
+enum { ROLE_RELAY, ROLE_MMA, ROLE_PROD, ROLE_CONV, ROLE_EPI };
 __device__ __forceinline__ int warp_role(int w)
 {
     if (w == kWarpMma)
@@ -65,8 +80,8 @@ __device__ __forceinline__ int warp_role(int w)
         return ROLE_PROD;
     if (w == 17 || w >= 20 && w != 21)
         return ROLE_EPI;
-    if (w == 21)
-        return ROLE_IDLE;
+    if (w == kWarpRelay)
+        return ROLE_RELAY;
     return ROLE_CONV;
 }
 // Converter index 0..15 of converter warp w (rows 8 * index .. + 7).
@@ -87,6 +102,11 @@ constexpr int OFF_A = B_STAGES * B_BYTES;
 constexpr int OFF_W = OFF_A + A_STAGES * A_BYTES;
 constexpr int RING_BYTES = OFF_W + W_STAGES * W_BYTES;
 constexpr int NUM_BARS = 2 * (W_STAGES + A_STAGES + B_STAGES) + 2 + 2 + 1;
+// Hardware named barriers (0 is __syncthreads): A slot s is released to the MMA warp
+// through barrier kNamedAReady + s, joined by the relay and the MMA warp.
+constexpr int kNamedAReady = 1;
+constexpr int kNamedThreads = 64;
+static_assert(kNamedAReady + A_STAGES <= 16, "named barrier ids");
 constexpr int SMEM_BYTES = 1024 + RING_BYTES + NUM_BARS * 8 + 16 + (kMaxExperts + 1) * 4;
 constexpr long long kTimeoutCycles = 2000000000LL;
 static_assert(B_BYTES % 1024 == 0 && A_BYTES % 1024 == 0 && OFF_W % 1024 == 0,
@@ -188,12 +208,43 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // Bounded wait that ignores the abort flag (used to drain in-flight work on abort).
-__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity)
+// Returns false if the phase did not complete in time.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity)
 {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity))
         if (clock64() - t0 > kTimeoutCycles / 4)
-            return;
+            return false;
+    return true;
+}
+
+// Whole-warp forms: lane 0 waits, the warp takes its answer (keeps the warp converged).
+__device__ __forceinline__ bool warp_mbar_wait(uint32_t bar, uint32_t parity,
+                                               volatile int *abort_flag, unsigned *err)
+{
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0)
+        ok = mbar_wait(bar, parity, abort_flag, err);
+    return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+}
+
+__device__ __forceinline__ bool warp_mbar_drain(uint32_t bar, uint32_t parity)
+{
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0)
+        ok = mbar_drain(bar, parity);
+    return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+}
+
+// Hardware named barriers, executed by whole converged warps.
+__device__ __forceinline__ void named_sync(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ void named_arrive(int id, int threads)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
@@ -252,6 +303,28 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
                  "setp.ne.b32 p, %4, 0;\n\t"
                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
                  "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// Warp-collective forms for a converged warp: one elected lane issues. Operands computed
+// by the whole warp stay warp-uniform, which keeps the issue loop short.
+__device__ __forceinline__ void mma_f16kind_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "elect.sync r|e, 0xffffffff;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_warp(uint32_t bar)
+{
+    asm volatile("{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
+                 "elect.sync r|e, 0xffffffff;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 "\n\t}" ::"r"(bar)
                  : "memory");
 }
 
@@ -557,53 +630,89 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (role == ROLE_MMA) {
         // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            Ring<A_STAGES> ra;
-            Ring<B_STAGES> rb;
-            bool ok = true;
-            int it = 0;
-            // descriptors of ring slot 0; other slots and k-blocks only move the start address
-            const uint64_t adesc0 = sw128_desc(smem_u32(ringA));
-            const uint64_t bdesc0 = sw128_desc(smem_u32(ringB));
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-                const Tile tl = tile_at(t, prefix, p);
-                const int nt = max(16, (tl.rows + 15) & ~15);
-                const uint32_t idesc = idesc_f16kind(BM, nt, f16_route ? 0u : 1u);
-                const int buf = it & 1;
-                if (!mbar_wait(acce(buf), ((it >> 1) & 1) ^ 1u, abort_flag, p.err))
-                    break;
+        // The whole warp runs the loop; one elected lane issues each MMA and commit. Inside
+        // a tile it only joins named barriers (see the header on why it never waits on an
+        // mbarrier or reads shared memory there).
+        Ring<A_STAGES> ra;
+        Ring<B_STAGES> rb;
+        int it = 0;
+        // descriptors of ring slot 0; other slots and k-blocks only move the start address
+        const uint64_t adesc0 = sw128_desc(smem_u32(ringA));
+        const uint64_t bdesc0 = sw128_desc(smem_u32(ringB));
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+            const Tile tl = tile_at(t, prefix, p);
+            if (*abort_flag)
+                break;
+            const int nt = max(16, (tl.rows + 15) & ~15);
+            const uint32_t idesc = idesc_f16kind(BM, nt, f16_route ? 0u : 1u);
+            const int buf = it & 1;
+            const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+            const int bi = bmap_index(tl.rows);
+            const int kbmask = (8 >> bi) - 1;
+            const uint32_t kb_desc = (uint32_t)((32 << bi) * 128) >> 4;  // one k-block
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int j = kb & kbmask;
+                // the relay has seen: accumulator free (kb 0), activation slot full (j 0),
+                // converted weight slot full
+                named_sync(kNamedAReady + ra.slot, kNamedThreads);
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
-                const int bi = bmap_index(tl.rows);
-                const int kbmask = (8 >> bi) - 1;
-                const uint32_t kb_desc = (uint32_t)((32 << bi) * 128) >> 4;  // one k-block
-                for (int kb = 0; kb < nkb; ++kb) {
-                    const int j = kb & kbmask;
-                    if ((j == 0 && !mbar_wait(bfull(rb.slot), rb.phase, abort_flag, p.err)) ||
-                        !mbar_wait(afull(ra.slot), ra.phase, abort_flag, p.err)) {
-                        ok = false;
+                const uint64_t adesc = adesc0 + (uint64_t)(ra.slot * (A_BYTES >> 4));
+                const uint64_t bdesc =
+                    bdesc0 + (uint64_t)(rb.slot * (B_BYTES >> 4) + (uint32_t)j * kb_desc);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    mma_f16kind_warp(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+                                     (kb | kk) != 0 ? 1u : 0u);
+                mma_commit_warp(aempty(ra.slot));
+                ra.next();
+                if (j == kbmask || kb == nkb - 1) {
+                    mma_commit_warp(bempty(rb.slot));
+                    rb.next();
+                }
+            }
+            mma_commit_warp(accf(buf));
+        }
+        mma_commit_warp(drain_bar);  // completes once every MMA issued above has finished
+        warp_mbar_drain(drain_bar, 0);
+    } else if (role == ROLE_RELAY) {
+        // ---------------------------------------------------------- relay
+        // Walks the MMA warp's stage sequence, waits for what each stage needs and
+        // releases its A slot with bar.arrive. A slot's next use is full only after the
+        // converters saw the MMAs of its previous use complete, so the relay can never
+        // lap the MMA warp on a named barrier.
+        Ring<A_STAGES> ra;
+        Ring<B_STAGES> rb;
+        int it = 0;
+        bool aborted = false, stuck = false;
+        for (int t = blockIdx.x; t < total && !aborted; t += gridDim.x, ++it) {
+            const Tile tl = tile_at(t, prefix, p);
+            const int buf = it & 1;
+            bool ok = warp_mbar_wait(acce(buf), ((it >> 1) & 1) ^ 1u, abort_flag, p.err);
+            const int kbmask = (8 >> bmap_index(tl.rows)) - 1;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int j = kb & kbmask;
+                if (ok && j == 0)
+                    ok = warp_mbar_wait(bfull(rb.slot), rb.phase, abort_flag, p.err);
+                if (ok)
+                    ok = warp_mbar_wait(afull(ra.slot), ra.phase, abort_flag, p.err);
+                if (!ok) {
+                    // Aborting: keep the MMA warp moving to the end of this tile (it checks
+                    // the abort flag at tile starts). Release a slot only after the MMAs
+                    // of its previous use completed, so that no barrier generation pairs
+                    // two arrivals of the relay.
+                    aborted = true;
+                    if (!warp_mbar_drain(aempty(ra.slot), ra.phase ^ 1u)) {
+                        stuck = true;
                         break;
                     }
-                    tc_fence_after();
-                    const uint64_t adesc = adesc0 + (uint64_t)(ra.slot * (A_BYTES >> 4));
-                    const uint64_t bdesc =
-                        bdesc0 + (uint64_t)(rb.slot * (B_BYTES >> 4) + (uint32_t)j * kb_desc);
-#pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        mma_bf16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
-                                 (kb | kk) != 0 ? 1u : 0u);
-                    mma_commit(aempty(ra.slot));
-                    ra.next();
-                    if (j == kbmask || kb == nkb - 1) {
-                        mma_commit(bempty(rb.slot));
-                        rb.next();
-                    }
                 }
-                if (ok)
-                    mma_commit(accf(buf));
+                named_arrive(kNamedAReady + ra.slot, kNamedThreads);
+                ra.next();
+                if (j == kbmask || kb == nkb - 1)
+                    rb.next();
             }
-            mma_commit(drain_bar);  // completes once every MMA issued above has finished
-            mbar_drain(drain_bar, 0);
+            if (stuck)
+                break;
         }
     } else if (role == ROLE_CONV) {
         // ---------------------------------------------------------- converters
@@ -616,8 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             for (int kb = 0; kb < nkb; ++kb) {
-                if (!mbar_wait(wfull(rw.slot), rw.phase, abort_flag, p.err) ||
-                    !mbar_wait(aempty(ra.slot), ra.phase ^ 1u, abort_flag, p.err)) {
+                if (!mbar_wait(wfull(rw.slot), rw.phase, abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
@@ -626,9 +734,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             : (((kb * BK) >> 5) & 15) + (cp >> 1);
                 const uint2 wv = *reinterpret_cast<const uint2 *>(w + r * 32 + cp * 8);
                 const uint32_t sb = w[NIB_BYTES + r * 16 + sidx];
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(wempty(rw.slot));  // weight slot consumed
                 uint4 o0, o1;
                 if (f16_route) {  // NVFP4 only
                     const uint32_t sh = e4m3x2_to_f16x2(sb | (sb << 8));
@@ -639,13 +744,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     e2m1x8_scaled_bf16(wv.x, sf, o0);
                     e2m1x8_scaled_bf16(wv.y, sf, o1);
                 }
+                // convert first, then wait for the A slot: the conversion overlaps the
+                // MMAs still reading the slot's previous use
+                if (!mbar_wait(aempty(ra.slot), ra.phase ^ 1u, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
                 uint8_t *row = ringA + ra.slot * A_BYTES + r * 128;
                 *reinterpret_cast<uint4 *>(row + (((2 * cp) ^ (r & 7)) << 4)) = o0;
                 *reinterpret_cast<uint4 *>(row + (((2 * cp + 1) ^ (r & 7)) << 4)) = o1;
+                // The proxy fence also orders this warp's reads of the weight slot before
+                // the TMA (async proxy) refill that the wempty arrival allows. Arriving
+                // right after issuing those reads let the refill land before they had
+                // read shared memory (seen as wrong weight rows on GB300).
                 fence_proxy_async();
                 __syncwarp();
-                if (lane == 0)
+                if (lane == 0) {
+                    mbar_arrive(wempty(rw.slot));
                     mbar_arrive(afull(ra.slot));
+                }
                 rw.next();
                 ra.next();
             }

@@ -151,3 +151,35 @@ def test_tc_rows_with_wide_block_scale_spread(recipe):
                                            "spread %s" % tag)
         assert fp4.fp4_get_device_error() == 0
         print("spread %s recipe %d: worst err/bound %.3g max_rel %.3g" % (tag, recipe, worst, rel))
+
+
+def test_tc_full_size_prefill_repeatable_and_matches_stream():
+    """Every output of both prefill projections (256 NVFP4 experts, 4096 tokens top-8,
+    Zipf routing), several runs. The tensor-core path computes each output in one fixed
+    MMA sequence, so runs must agree bit for bit: a pipeline race (a ring slot reused
+    before its reader finished) shows up as run-to-run changes in a few weight rows of a
+    tile. Each run must also agree with the streaming path to 1e-3 of the output's
+    magnitude (floored at 1e-2 of the projection's largest output); the race gave errors
+    of 10-30%."""
+    wl = synth.workload("c4", device=DEV)
+    for proj in wl.projections:
+        fp4.fp4_force_path(fp4.PATH_STREAM)
+        ref, _ = run_projection(proj)
+        fp4.fp4_force_path(fp4.PATH_TC)
+        floor = 1e-2 * ref.abs().max()
+        first = None
+        for rep in range(4):
+            out, path = run_projection(proj)
+            assert path == fp4.PATH_TC
+            assert fp4.fp4_get_device_error() == 0
+            bad = (out - ref).abs() > 1e-3 * (ref.abs() + floor)
+            nbad = int(bad.sum().item())
+            assert nbad == 0, "%s run %d: %d outputs off the streaming path, first at %s" % (
+                proj.name, rep, nbad, tuple(bad.nonzero()[0].tolist()))
+            if first is None:
+                first = out
+            else:
+                diff = int((out != first).sum().item())
+                assert diff == 0, "%s run %d: %d outputs differ from run 0" % (proj.name, rep, diff)
+            del out
+        del ref, first
