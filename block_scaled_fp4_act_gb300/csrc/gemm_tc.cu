@@ -6,26 +6,31 @@
 // kind that accepts FP8 A operands has only ue8m0 scales per 32, and the kind with e4m3
 // scales per 16 wants FP4 on both sides, so the exact route on this hardware is the bf16
 // MMA (kind::f16): both operands carry their scales and stay exact in bf16.
-//   A (M side) = weights:     bf16(E2M1 * e4m3 scale)  NVFP4 (<= 6 significant bits)
+//   A (M side) = weights:     bf16(E2M1 * e4m3 scale)  NVFP4 (<= 6 significant bits;
+//                             f16 on the f16 route below)
 //                             bf16(E2M1 * 2^(e-127))   MXFP4
 //   B (N side) = activations: bf16(e4m3 code * pow2 scale), written by the quantise pass
 //   D (TMEM)   = f32 [128 weight rows x N routed rows]; epilogue multiplies by scale2.
 //
-// Kernel structure: persistent, one CTA (23 warps) per SM, static round-robin over
-// tiles (expert, 256-row block of its routed rows, 128-row block of its weights),
+// Kernel structure: persistent, one CTA (24 warps) per SM, static round-robin over
+// tiles (expert, 192-row block of its routed rows, 128-row block of its weights),
 // weight-row block fastest so consecutive tiles share the activation block in L2.
-// Three shared-memory rings decouple the streams: a 12-deep weight ring (nibbles +
-// scales, 6 KB a stage, ~72 KB in flight: weights stream from HBM once per tile), a
-// 3-deep ring of converted bf16 weight tiles and a 3-deep activation ring.
+// Rings decouple the streams: a 14-deep shared-memory weight ring (nibbles + scales,
+// 6 KB a stage: weights stream from HBM once per tile), a 4-deep activation ring in
+// shared memory and a 4-deep ring of converted weight tiles in tensor memory. The MMA
+// reads its A operand (the converted weights) from tensor memory: shared memory then
+// carries only the activation tiles, the raw weights and their TMA writes, and its
+// bandwidth (about 70% busy when the converted weights went through it too) stops
+// being the limit.
 //   warp 1      TMEM owner and MMA issuer (whole warp, one elected lane issues), 4 MMAs
 //               of K=16 per stage
-//   warp 21     relay: does the MMA side's mbarrier waits and releases each A slot to
+//   warp 3      relay: does the MMA side's mbarrier waits and releases each A slot to
 //               warp 1 through a hardware named barrier
-//   warp 5      TMA producer of activation slots (bf16, 128B swizzle, k-block-major)
-//   warp 9      TMA producer of nibble and scale tiles
-//   16 warps    converters: nibbles x scales -> bf16 A tile in the UMMA 128B-swizzle layout
-//   4 warps     epilogue: tcgen05.ld of the accumulator, x scale2, coalesced f32 stores
-// Two accumulators (2 x 256 TMEM columns) let the epilogue of one tile overlap the
+//   warp 0      TMA producer of activation slots (bf16, 128B swizzle, k-block-major)
+//   warp 2      TMA producer of nibble (32-byte swizzle) and scale tiles
+//   warps 8-23  converters: nibbles x scales -> 16-bit A operand, tcgen05.st into TMEM
+//   warps 4-7   epilogue: tcgen05.ld of the accumulator, x scale2, coalesced f32 stores
+// Two accumulators (2 x 192 TMEM columns) let the epilogue of one tile overlap the
 // main loop of the next. The MMA N of a tile is its routed-row count rounded up to 16,
 // so an expert's ragged last block costs at most 15 padded rows.
 //
@@ -56,21 +61,19 @@ namespace fp4moe {
 namespace tc {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BN = 192;       // routed rows per tile (MMA N, rounded up to 16 per tile)
 constexpr int BK = 64;
-constexpr int W_STAGES = 12;  // weight ring (nibbles + scales): deep, it streams from HBM
-constexpr int A_STAGES = 3;   // converted bf16 weight tiles
-constexpr int B_STAGES = 3;   // activation tiles (mostly L2 hits: shared by a tile's neighbours)
+constexpr int W_STAGES = 14;  // weight ring (nibbles + scales): deep, it streams from HBM
+constexpr int A_STAGES = 4;   // converted weight tiles, in tensor memory
+constexpr int B_STAGES = 4;   // activation tiles (mostly L2 hits: shared by a tile's neighbours)
 constexpr int kMaxExperts = 1024;
-constexpr int kConvWarps = 16;
+constexpr int kConvPerStage = 8;  // two converter warps per TMEM lane quarter per k-stage
 constexpr int kThreads = 24 * 32;
-// Warp roles. Warp w issues on SM sub-partition w % 4, and the single MMA-issuing thread
-// must not compete for issue slots with busy converter warps, so sub-partition 1 holds
-// the MMA issuer, both TMA producers, one converter and one epilogue warp, and the other
-// 15 converters fill sub-partitions 0, 2 and 3. Epilogue warps 20, 17, 22, 23 cover the
-// four TMEM lane quarters (a warp reads lanes 32 * (w % 4) .. + 31).
-constexpr int kWarpMma = 1, kWarpB = 5, kWarpW = 9;
-constexpr int kWarpRelay = 21;
+// Warp roles. Warp w issues on SM sub-partition w % 4 and reaches TMEM lanes 32 * (w % 4)
+// .. + 31 only, so every sub-partition holds one epilogue warp and four converter warps
+// for its lane quarter, plus one of: the activation producer (0), the MMA issuer (1), the
+// weight producer (2) and the relay (3).
+constexpr int kWarpB = 0, kWarpMma = 1, kWarpW = 2, kWarpRelay = 3;
 enum { ROLE_RELAY, ROLE_MMA, ROLE_PROD, ROLE_CONV, ROLE_EPI };
 __device__ __forceinline__ int warp_role(int w)
 {
@@ -78,28 +81,23 @@ __device__ __forceinline__ int warp_role(int w)
         return ROLE_MMA;
     if (w == kWarpB || w == kWarpW)
         return ROLE_PROD;
-    if (w == 17 || w >= 20 && w != 21)
-        return ROLE_EPI;
     if (w == kWarpRelay)
         return ROLE_RELAY;
-    return ROLE_CONV;
+    return w < 8 ? ROLE_EPI : ROLE_CONV;
 }
-// Converter index 0..15 of converter warp w (rows 8 * index .. + 7).
-__device__ __forceinline__ int conv_index(int w)
-{
-    // converters: 0,2,3,4,6,7,8,10,11,12,13,14,15,16,18,19
-    return w == 0 ? 0 : w < 4 ? w - 1 : w < 5 ? 3 : w < 9 ? w - 2 : w < 13 ? w - 3 : w < 17 ? w - 3 : w - 4;
-}
-// Activation tiles are loaded k-block-major: one 32 KB TMA box holds up to 8 k-blocks of
-// a small tile (32 rows x 8, 64 x 4, 128 x 2, 256 x 1), so small tiles keep many k-stages
-// in flight in the same three ring slots.
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int A_BYTES = BM * BK * 2;
+// Tensor memory (512 columns x 128 lanes of 32 bit): two f32 accumulators of BN columns,
+// then the A ring: weight row r in lane r, k-pair j of a stage in column j (16-bit
+// elements, even k in the low half), 32 columns per 64-k stage.
+constexpr int kACol = 2 * BN;
+static_assert(kACol + A_STAGES * (BK / 2) <= 512, "tensor memory budget");
+// Activation tiles are loaded k-block-major: one TMA box holds up to 8 k-blocks of a small
+// tile (32 rows x 8, 64 x 4, 128 x 2 k-blocks, or BN rows x 1), so small tiles keep many
+// k-stages in flight in the same ring slots.
+constexpr int B_BYTES = 32 * 8 * BK * 2;  // one ring slot (the largest box)
 constexpr int NIB_BYTES = BM * BK / 2;
 constexpr int SC_BYTES = BM * 16;
 constexpr int W_BYTES = NIB_BYTES + SC_BYTES;
-constexpr int OFF_A = B_STAGES * B_BYTES;
-constexpr int OFF_W = OFF_A + A_STAGES * A_BYTES;
+constexpr int OFF_W = B_STAGES * B_BYTES;
 constexpr int RING_BYTES = OFF_W + W_STAGES * W_BYTES;
 constexpr int NUM_BARS = 2 * (W_STAGES + A_STAGES + B_STAGES) + 2 + 2 + 1;
 // Hardware named barriers (0 is __syncthreads): A slot s is released to the MMA warp
@@ -109,8 +107,9 @@ constexpr int kNamedThreads = 64;
 static_assert(kNamedAReady + A_STAGES <= 16, "named barrier ids");
 constexpr int SMEM_BYTES = 1024 + RING_BYTES + NUM_BARS * 8 + 16 + (kMaxExperts + 1) * 4;
 constexpr long long kTimeoutCycles = 2000000000LL;
-static_assert(B_BYTES % 1024 == 0 && A_BYTES % 1024 == 0 && OFF_W % 1024 == 0,
+static_assert(B_BYTES % 1024 == 0 && W_BYTES % 1024 == 0 && OFF_W % 1024 == 0,
               "swizzled tiles need 1024-byte alignment");
+static_assert(BN * BK * 2 <= B_BYTES && BN % 16 == 0 && BN <= 256, "activation box");
 static_assert(kThreads <= 1024, "block size");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
@@ -319,6 +318,31 @@ __device__ __forceinline__ void mma_f16kind_warp(uint32_t d_tmem, uint64_t a_des
                  : "memory");
 }
 
+// As mma_f16kind_warp with the A operand in tensor memory (a_tmem: lane 0, first column).
+__device__ __forceinline__ void mma_f16kind_tmem_a_warp(uint32_t d_tmem, uint32_t a_tmem,
+                                                        uint64_t b_desc, uint32_t idesc,
+                                                        uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "elect.sync r|e, 0xffffffff;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// Sixteen 32-bit columns of this warp's 32 TMEM lanes (thread i -> lane base + i).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, "
+                 "%9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                 "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
+                 "r"(v[14]), "r"(v[15])
+                 : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void mma_commit_warp(uint32_t bar)
 {
     asm volatile("{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
@@ -482,6 +506,10 @@ __device__ __forceinline__ int bmap_index(int rows)
     return rows <= 32 ? 0 : rows <= 64 ? 1 : rows <= 128 ? 2 : 3;
 }
 
+// Rows and k-blocks of activation box bi.
+__host__ __device__ constexpr int bmap_rows(int bi) { return bi < 3 ? 32 << bi : BN; }
+__host__ __device__ constexpr int bmap_kblocks(int bi) { return 8 >> bi; }
+
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ BMaps tmB, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmS, const Params p)
@@ -526,10 +554,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < W_STAGES; ++s) {
             mbar_init(wfull(s), 1);
-            mbar_init(wempty(s), kConvWarps);
+            mbar_init(wempty(s), kConvPerStage);
         }
         for (int s = 0; s < A_STAGES; ++s) {
-            mbar_init(afull(s), kConvWarps);
+            mbar_init(afull(s), kConvPerStage);
             mbar_init(aempty(s), 1);
         }
         for (int s = 0; s < B_STAGES; ++s) {
@@ -576,13 +604,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nkb = p.k / BK;
     const int gs = p.recipe == FP4_NVFP4 ? 16 : 32;
     uint8_t *const ringB = smem;
-    uint8_t *const ringA = smem + OFF_A;
     uint8_t *const ringW = smem + OFF_W;
 
     const int role = warp_role(warp);
     if (role == ROLE_PROD) {
         // ---------------------------------------------------------- TMA producers
-        // warp 0: activation slots into the B ring; warp 2: nibbles + scales into the W ring
+        // kWarpB: activation slots into the B ring; kWarpW: nibbles + scales into the W ring
         if (lane == 0) {
             const bool is_b = warp == kWarpB;
             const int nslots = is_b ? B_STAGES : W_STAGES;
@@ -594,7 +621,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Tile tl = tile_at(t, prefix, p);
                 const int yw = tl.e * p.n + tl.m * BM;
                 const int bi = bmap_index(tl.rows);
-                const int kbps = 8 >> bi;
+                const int kbps = bmap_kblocks(bi);
+                const uint32_t box_bytes = (uint32_t)(bmap_rows(bi) * kbps * BK * 2);
                 const int nload = is_b ? (nkb + kbps - 1) / kbps : nkb;
                 for (int j = 0; j < nload; ++j) {
                     const uint32_t emp = is_b ? bempty(slot) : wempty(slot);
@@ -604,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     if (is_b) {
-                        mbar_arrive_expect_tx(ful, B_BYTES);
+                        mbar_arrive_expect_tx(ful, box_bytes);
                         tma_load_3d(smem_u32(ringB + slot * B_BYTES), &tmB.m[bi], 0, (int)tl.row0,
                                     j * kbps, ful);
                     } else {
@@ -636,9 +664,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         Ring<A_STAGES> ra;
         Ring<B_STAGES> rb;
         int it = 0;
-        // descriptors of ring slot 0; other slots and k-blocks only move the start address
-        const uint64_t adesc0 = sw128_desc(smem_u32(ringA));
+        // B descriptor of ring slot 0; other slots and k-blocks only move the start address
         const uint64_t bdesc0 = sw128_desc(smem_u32(ringB));
+        const uint32_t a_tmem0 = tmem_base + (uint32_t)kACol;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
             const Tile tl = tile_at(t, prefix, p);
             if (*abort_flag)
@@ -648,21 +676,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int buf = it & 1;
             const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
             const int bi = bmap_index(tl.rows);
-            const int kbmask = (8 >> bi) - 1;
-            const uint32_t kb_desc = (uint32_t)((32 << bi) * 128) >> 4;  // one k-block
+            const int kbmask = bmap_kblocks(bi) - 1;
+            const uint32_t kb_desc = (uint32_t)(bmap_rows(bi) * BK * 2) >> 4;  // one k-block
             for (int kb = 0; kb < nkb; ++kb) {
                 const int j = kb & kbmask;
                 // the relay has seen: accumulator free (kb 0), activation slot full (j 0),
                 // converted weight slot full
                 named_sync(kNamedAReady + ra.slot, kNamedThreads);
                 tc_fence_after();
-                const uint64_t adesc = adesc0 + (uint64_t)(ra.slot * (A_BYTES >> 4));
+                const uint32_t a_tmem = a_tmem0 + (uint32_t)(ra.slot * (BK / 2));
                 const uint64_t bdesc =
                     bdesc0 + (uint64_t)(rb.slot * (B_BYTES >> 4) + (uint32_t)j * kb_desc);
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
-                    mma_f16kind_warp(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
-                                     (kb | kk) != 0 ? 1u : 0u);
+                    mma_f16kind_tmem_a_warp(d_tmem, a_tmem + 8u * kk, bdesc + 2u * kk, idesc,
+                                            (kb | kk) != 0 ? 1u : 0u);
                 mma_commit_warp(aempty(ra.slot));
                 ra.next();
                 if (j == kbmask || kb == nkb - 1) {
@@ -688,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Tile tl = tile_at(t, prefix, p);
             const int buf = it & 1;
             bool ok = warp_mbar_wait(acce(buf), ((it >> 1) & 1) ^ 1u, abort_flag, p.err);
-            const int kbmask = (8 >> bmap_index(tl.rows)) - 1;
+            const int kbmask = bmap_kblocks(bmap_index(tl.rows)) - 1;
             for (int kb = 0; kb < nkb; ++kb) {
                 const int j = kb & kbmask;
                 if (ok && j == 0)
@@ -716,56 +744,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (role == ROLE_CONV) {
         // ---------------------------------------------------------- converters
-        // Item = 16 weights of one row: lane -> (row rs, 16-weight chunk cp); warp cw owns
-        // rows [8 cw, 8 cw + 8).
-        const int cw = conv_index(warp), cp = lane & 3, rs = lane >> 2;
-        const int r = cw * 8 + rs;
+        // Warp w writes TMEM lane quarter q = w % 4 (the only lanes its tcgen05.st reaches):
+        // lane i converts weight row 32 q + i. The four converter warps of a quarter take
+        // turns: h = 0, 1 convert the even k-stages, h = 2, 3 the odd ones, each the 32-k
+        // half c = h & 1 of the stage (one 16-byte nibble chunk, 16 TMEM columns).
+        const int q = warp & 3, h = (warp - 8) >> 2, c = h & 1;
+        const int r = q * 32 + lane;
+        // the nibble tile arrives with the 32-byte TMA swizzle: the 16-byte chunk c of row r
+        // sits at chunk c ^ bit 2 of r, so a warp's 32 rows read conflict-free
+        const int nib_off = r * 32 + ((c ^ ((r >> 2) & 1)) << 4);
+        const uint32_t a_lane = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(kACol + c * 16);
         Ring<W_STAGES> rw;
         Ring<A_STAGES> ra;
-        bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            for (int kb = 0; kb < nkb; ++kb) {
-                if (!mbar_wait(wfull(rw.slot), rw.phase, abort_flag, p.err)) {
-                    ok = false;
-                    break;
-                }
-                const uint8_t *w = ringW + rw.slot * W_BYTES;
-                const int sidx = (gs == 16) ? (((kb * BK) >> 4) & 15) + cp
-                                            : (((kb * BK) >> 5) & 15) + (cp >> 1);
-                const uint2 wv = *reinterpret_cast<const uint2 *>(w + r * 32 + cp * 8);
-                const uint32_t sb = w[NIB_BYTES + r * 16 + sidx];
-                uint4 o0, o1;
-                if (f16_route) {  // NVFP4 only
-                    const uint32_t sh = e4m3x2_to_f16x2(sb | (sb << 8));
-                    e2m1x8_scaled_f16(wv.x, sh, o0);
-                    e2m1x8_scaled_f16(wv.y, sh, o1);
+        if (h >> 1) {
+            rw.next();
+            ra.next();
+        }
+        const int ntiles = (int)blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+        const int nst = ntiles * nkb;
+        for (int g = h >> 1; g < nst; g += 2) {
+            const int kb = g % nkb;
+            if (!mbar_wait(wfull(rw.slot), rw.phase, abort_flag, p.err))
+                break;
+            const uint8_t *w = ringW + rw.slot * W_BYTES;
+            const uint4 nv = *reinterpret_cast<const uint4 *>(w + nib_off);
+            uint32_t o[16];
+            uint4 *o4 = reinterpret_cast<uint4 *>(o);
+            if (gs == 16) {
+                // scales of k-groups 2c and 2c + 1 of this stage (16 per slab row)
+                const uint32_t s01 = *reinterpret_cast<const uint16_t *>(
+                    w + NIB_BYTES + r * 16 + (((kb * BK) >> 4) & 15) + 2 * c);
+                if (f16_route) {
+                    const uint32_t h0 = e4m3x2_to_f16x2((s01 & 0xFFu) * 0x101u);
+                    const uint32_t h1 = e4m3x2_to_f16x2((s01 >> 8) * 0x101u);
+                    e2m1x8_scaled_f16(nv.x, h0, o4[0]);
+                    e2m1x8_scaled_f16(nv.y, h0, o4[1]);
+                    e2m1x8_scaled_f16(nv.z, h1, o4[2]);
+                    e2m1x8_scaled_f16(nv.w, h1, o4[3]);
                 } else {
-                    const float sf = (gs == 16) ? e4m3_to_f32(sb) : e8m0_to_f32(sb);
-                    e2m1x8_scaled_bf16(wv.x, sf, o0);
-                    e2m1x8_scaled_bf16(wv.y, sf, o1);
+                    const float f0 = e4m3_to_f32(s01 & 0xFFu), f1 = e4m3_to_f32(s01 >> 8);
+                    e2m1x8_scaled_bf16(nv.x, f0, o4[0]);
+                    e2m1x8_scaled_bf16(nv.y, f0, o4[1]);
+                    e2m1x8_scaled_bf16(nv.z, f1, o4[2]);
+                    e2m1x8_scaled_bf16(nv.w, f1, o4[3]);
                 }
-                // convert first, then wait for the A slot: the conversion overlaps the
-                // MMAs still reading the slot's previous use
-                if (!mbar_wait(aempty(ra.slot), ra.phase ^ 1u, abort_flag, p.err)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t *row = ringA + ra.slot * A_BYTES + r * 128;
-                *reinterpret_cast<uint4 *>(row + (((2 * cp) ^ (r & 7)) << 4)) = o0;
-                *reinterpret_cast<uint4 *>(row + (((2 * cp + 1) ^ (r & 7)) << 4)) = o1;
-                // The proxy fence also orders this warp's reads of the weight slot before
-                // the TMA (async proxy) refill that the wempty arrival allows. Arriving
-                // right after issuing those reads let the refill land before they had
-                // read shared memory (seen as wrong weight rows on GB300).
-                fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(wempty(rw.slot));
-                    mbar_arrive(afull(ra.slot));
-                }
-                rw.next();
-                ra.next();
+            } else {
+                const float f = e8m0_to_f32(w[NIB_BYTES + r * 16 + (((kb * BK) >> 5) & 15) + c]);
+                e2m1x8_scaled_bf16(nv.x, f, o4[0]);
+                e2m1x8_scaled_bf16(nv.y, f, o4[1]);
+                e2m1x8_scaled_bf16(nv.z, f, o4[2]);
+                e2m1x8_scaled_bf16(nv.w, f, o4[3]);
             }
+            // Release the weight slot once its values are consumed, behind an async-proxy
+            // fence that orders these reads before the TMA refill. (Arriving right after
+            // issuing the reads let the refill land first: wrong weight rows on GB300.)
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(wempty(rw.slot));
+            // then wait for the A slot: the conversion overlapped the MMAs still reading it
+            if (!mbar_wait(aempty(ra.slot), ra.phase ^ 1u, abort_flag, p.err))
+                break;
+            tc_fence_after();
+            tmem_st16(a_lane + (uint32_t)(ra.slot * (BK / 2)), o);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(afull(ra.slot));
+            rw.next();
+            rw.next();
+            ra.next();
+            ra.next();
         }
     } else if (role == ROLE_EPI) {
         // ---------------------------------------------------------- epilogue
@@ -1061,11 +1110,12 @@ cudaError_t launch_tc_gemm(const GroupedProblem &p, void *workspace, cudaStream_
     alignas(64) BMaps tmB;
     alignas(64) CUtensorMap tmW, tmS;
     for (int i = 0; i < 4; ++i)
-        if (!make_map_kblocks(&tmB.m[i], ws, (uint64_t)p.k, (uint64_t)p.P, 32u << i, 8u >> i))
+        if (!make_map_kblocks(&tmB.m[i], ws, (uint64_t)p.k, (uint64_t)p.P, (uint32_t)bmap_rows(i),
+                              (uint32_t)bmap_kblocks(i)))
             return cudaErrorInvalidValue;
     if (
         !make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w, (uint64_t)p.k / 2,
-                  (uint64_t)p.E * p.n, BK / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                  (uint64_t)p.E * p.n, BK / 2, BM, CU_TENSOR_MAP_SWIZZLE_32B) ||
         !make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sc, (uint64_t)p.k / gs,
                   (uint64_t)p.E * p.n, 16, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
