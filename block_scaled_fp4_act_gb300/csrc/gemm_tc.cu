@@ -522,7 +522,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *prefix = reinterpret_cast<int *>(tmem_slot + 4);
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Values that feed tcgen05 operands are broadcast from lane 0: the compiler then knows
+    // they are warp-uniform and issues each tcgen05 instruction once, instead of once per
+    // distinct operand value among the lanes.
+    const int warp = __shfl_sync(0xFFFFFFFFu, (int)(threadIdx.x >> 5), 0), lane = threadIdx.x & 31;
     const uint32_t bar0 = smem_u32(bars);
     // barrier map: weight full/empty, A full/empty, B full/empty, accumulator full/empty, drain
     auto wfull = [&](int s) { return bar0 + 8u * s; };
@@ -598,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t tmem_base = __shfl_sync(0xFFFFFFFFu, *tmem_slot, 0);
     const int total = prefix[E];
     const bool f16_route = p.route_flag != nullptr && *((volatile const unsigned *)p.route_flag) == 0u;
     const int nkb = p.k / BK;
@@ -667,15 +670,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // B descriptor of ring slot 0; other slots and k-blocks only move the start address
         const uint64_t bdesc0 = sw128_desc(smem_u32(ringB));
         const uint32_t a_tmem0 = tmem_base + (uint32_t)kACol;
+        const uint32_t ab_fmt = __shfl_sync(0xFFFFFFFFu, f16_route ? 0u : 1u, 0);
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
             const Tile tl = tile_at(t, prefix, p);
             if (*abort_flag)
                 break;
-            const int nt = max(16, (tl.rows + 15) & ~15);
-            const uint32_t idesc = idesc_f16kind(BM, nt, f16_route ? 0u : 1u);
+            const int rows = __shfl_sync(0xFFFFFFFFu, tl.rows, 0);
+            const int nt = max(16, (rows + 15) & ~15);
+            const uint32_t idesc = idesc_f16kind(BM, nt, ab_fmt);
             const int buf = it & 1;
             const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
-            const int bi = bmap_index(tl.rows);
+            const int bi = bmap_index(rows);
             const int kbmask = bmap_kblocks(bi) - 1;
             const uint32_t kb_desc = (uint32_t)(bmap_rows(bi) * BK * 2) >> 4;  // one k-block
             for (int kb = 0; kb < nkb; ++kb) {
