@@ -46,8 +46,8 @@
 // its own copies and MMAs in flight, frees its tensor memory and returns. The MMA warp's
 // named-barrier waits cannot time out, so on abort the relay keeps releasing slots to the
 // end of the current tile, each only after the MMA warp has consumed the slot's previous
-// use (a bounded wait on the slot's empty barrier); the MMA warp checks the abort flag at
-// every tile start.
+// use (a bounded wait on the slot's empty barrier), and then releases the next tile's
+// first stage with a row count of -1, which stops the MMA warp.
 #include "common.cuh"
 
 #include <cuda.h>
@@ -67,8 +67,12 @@ constexpr int W_STAGES = 14;  // weight ring (nibbles + scales): deep, it stream
 constexpr int A_STAGES = 4;   // converted weight tiles, in tensor memory
 constexpr int B_STAGES = 4;   // activation tiles (mostly L2 hits: shared by a tile's neighbours)
 constexpr int kMaxExperts = 1024;
+// Converter warps per TMEM lane quarter; two of them (one per 32-k half) convert each
+// k-stage, so kConvPerQuarter / 2 pairs take turns over the stages.
+constexpr int kConvPerQuarter = 4;
+constexpr int kConvTurns = kConvPerQuarter / 2;
 constexpr int kConvPerStage = 8;  // two converter warps per TMEM lane quarter per k-stage
-constexpr int kThreads = 24 * 32;
+constexpr int kThreads = (8 + 4 * kConvPerQuarter) * 32;
 // Warp roles. Warp w issues on SM sub-partition w % 4 and reaches TMEM lanes 32 * (w % 4)
 // .. + 31 only, so every sub-partition holds one epilogue warp and four converter warps
 // for its lane quarter, plus one of: the activation producer (0), the MMA issuer (1), the
@@ -105,7 +109,14 @@ constexpr int NUM_BARS = 2 * (W_STAGES + A_STAGES + B_STAGES) + 2 + 2 + 1;
 constexpr int kNamedAReady = 1;
 constexpr int kNamedThreads = 64;
 static_assert(kNamedAReady + A_STAGES <= 16, "named barrier ids");
-constexpr int SMEM_BYTES = 1024 + RING_BYTES + NUM_BARS * 8 + 16 + (kMaxExperts + 1) * 4;
+// Tile row counts the relay publishes to the MMA warp. The relay writes tile i's entry
+// after releasing every stage of tiles i - kTileInfo .. i - 1 (at least 2 stages each, as
+// k >= 128) and runs at most A_STAGES stages ahead, so with 2 kTileInfo > A_STAGES the
+// MMA warp has read the entry's previous tile by then.
+constexpr int kTileInfo = A_STAGES;
+static_assert(2 * kTileInfo > A_STAGES, "tile info ring depth");
+constexpr int SMEM_BYTES =
+    1024 + RING_BYTES + NUM_BARS * 8 + 16 + (kMaxExperts + 1) * 4 + kTileInfo * 4;
 constexpr long long kTimeoutCycles = 2000000000LL;
 static_assert(B_BYTES % 1024 == 0 && W_BYTES % 1024 == 0 && OFF_W % 1024 == 0,
               "swizzled tiles need 1024-byte alignment");
@@ -521,6 +532,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *prefix = reinterpret_cast<int *>(tmem_slot + 4);
+    // tile it's routed-row count (or -1: stop) at tile_info[it % kTileInfo], written by the
+    // relay before its first release of the tile's first stage
+    volatile int *tile_info = prefix + kMaxExperts + 1;
 
     // Values that feed tcgen05 operands are broadcast from lane 0: the compiler then knows
     // they are warp-uniform and issues each tcgen05 instruction once, instead of once per
@@ -661,21 +675,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (role == ROLE_MMA) {
         // ---------------------------------------------------------- MMA issuer
-        // The whole warp runs the loop; one elected lane issues each MMA and commit. Inside
-        // a tile it only joins named barriers (see the header on why it never waits on an
-        // mbarrier or reads shared memory there).
-        Ring<A_STAGES> ra;
-        Ring<B_STAGES> rb;
+        // The whole warp runs the loop; one elected lane issues each MMA and commit. It never
+        // waits on an mbarrier, and it reads shared memory once per tile (the row count the
+        // relay published), right after the tile's first named barrier (see the header).
+        unsigned st = 0;  // A stages issued (A slot = st % A_STAGES, the relay's order)
+        int bslot = 0;  // activation ring slot
         int it = 0;
         // B descriptor of ring slot 0; other slots and k-blocks only move the start address
         const uint64_t bdesc0 = sw128_desc(smem_u32(ringB));
         const uint32_t a_tmem0 = tmem_base + (uint32_t)kACol;
         const uint32_t ab_fmt = __shfl_sync(0xFFFFFFFFu, f16_route ? 0u : 1u, 0);
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-            const Tile tl = tile_at(t, prefix, p);
-            if (*abort_flag)
-                break;
-            const int rows = __shfl_sync(0xFFFFFFFFu, tl.rows, 0);
+            named_sync(kNamedAReady + (int)(st % A_STAGES), kNamedThreads);  // tile's first stage
+            const int rows = __shfl_sync(0xFFFFFFFFu, tile_info[it % kTileInfo], 0);
+            if (rows < 0)
+                break;  // the relay is aborting
             const int nt = max(16, (rows + 15) & ~15);
             const uint32_t idesc = idesc_f16kind(BM, nt, ab_fmt);
             const int buf = it & 1;
@@ -683,25 +697,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int bi = bmap_index(rows);
             const int kbmask = bmap_kblocks(bi) - 1;
             const uint32_t kb_desc = (uint32_t)(bmap_rows(bi) * BK * 2) >> 4;  // one k-block
-            for (int kb = 0; kb < nkb; ++kb) {
+            // one k-stage; the relay has seen: accumulator free (kb 0), activation slot full
+            // (j 0), converted weight slot full
+            auto stage = [&](int kb) {
                 const int j = kb & kbmask;
-                // the relay has seen: accumulator free (kb 0), activation slot full (j 0),
-                // converted weight slot full
-                named_sync(kNamedAReady + ra.slot, kNamedThreads);
+                const int as = (int)(st % A_STAGES);
                 tc_fence_after();
-                const uint32_t a_tmem = a_tmem0 + (uint32_t)(ra.slot * (BK / 2));
+                const uint32_t a_tmem = a_tmem0 + (uint32_t)(as * (BK / 2));
                 const uint64_t bdesc =
-                    bdesc0 + (uint64_t)(rb.slot * (B_BYTES >> 4) + (uint32_t)j * kb_desc);
+                    bdesc0 + (uint64_t)(bslot * (B_BYTES >> 4) + (uint32_t)j * kb_desc);
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
                     mma_f16kind_tmem_a_warp(d_tmem, a_tmem + 8u * kk, bdesc + 2u * kk, idesc,
                                             (kb | kk) != 0 ? 1u : 0u);
-                mma_commit_warp(aempty(ra.slot));
-                ra.next();
+                mma_commit_warp(aempty(as));
+                ++st;
                 if (j == kbmask || kb == nkb - 1) {
-                    mma_commit_warp(bempty(rb.slot));
-                    rb.next();
+                    mma_commit_warp(bempty(bslot));
+                    bslot = bslot + 1 == B_STAGES ? 0 : bslot + 1;
                 }
+            };
+            stage(0);
+            for (int kb = 1; kb < nkb; ++kb) {
+                named_sync(kNamedAReady + (int)(st % A_STAGES), kNamedThreads);
+                stage(kb);
             }
             mma_commit_warp(accf(buf));
         }
@@ -720,6 +739,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = blockIdx.x; t < total && !aborted; t += gridDim.x, ++it) {
             const Tile tl = tile_at(t, prefix, p);
             const int buf = it & 1;
+            // published before the arrival that releases the tile's first stage
+            tile_info[it % kTileInfo] = tl.rows;
             bool ok = warp_mbar_wait(acce(buf), ((it >> 1) & 1) ^ 1u, abort_flag, p.err);
             const int kbmask = bmap_kblocks(bmap_index(tl.rows)) - 1;
             for (int kb = 0; kb < nkb; ++kb) {
@@ -729,10 +750,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok)
                     ok = warp_mbar_wait(afull(ra.slot), ra.phase, abort_flag, p.err);
                 if (!ok) {
-                    // Aborting: keep the MMA warp moving to the end of this tile (it checks
-                    // the abort flag at tile starts). Release a slot only after the MMAs
-                    // of its previous use completed, so that no barrier generation pairs
-                    // two arrivals of the relay.
+                    // Aborting: keep the MMA warp moving to the end of this tile, then stop
+                    // it at the next tile start. Release a slot only after the MMAs of its
+                    // previous use completed, so that no barrier generation pairs two
+                    // arrivals of the relay.
                     aborted = true;
                     if (!warp_mbar_drain(aempty(ra.slot), ra.phase ^ 1u)) {
                         stuck = true;
@@ -746,6 +767,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (stuck)
                 break;
+            if (aborted && t + (int)gridDim.x < total) {
+                // the MMA warp would start another tile: release its first stage with a
+                // row count of -1, which makes it stop
+                tile_info[(it + 1) % kTileInfo] = -1;
+                if (warp_mbar_drain(aempty(ra.slot), ra.phase ^ 1u))
+                    named_arrive(kNamedAReady + ra.slot, kNamedThreads);
+            }
         }
     } else if (role == ROLE_CONV) {
         // ---------------------------------------------------------- converters
@@ -761,13 +789,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a_lane = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(kACol + c * 16);
         Ring<W_STAGES> rw;
         Ring<A_STAGES> ra;
-        if (h >> 1) {
+        for (int i = 0; i < (h >> 1); ++i) {
             rw.next();
             ra.next();
         }
         const int ntiles = (int)blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
         const int nst = ntiles * nkb;
-        for (int g = h >> 1; g < nst; g += 2) {
+        for (int g = h >> 1; g < nst; g += kConvTurns) {
             const int kb = g % nkb;
             if (!mbar_wait(wfull(rw.slot), rw.phase, abort_flag, p.err))
                 break;
@@ -816,10 +844,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(afull(ra.slot));
-            rw.next();
-            rw.next();
-            ra.next();
-            ra.next();
+            for (int i = 0; i < kConvTurns; ++i) {
+                rw.next();
+                ra.next();
+            }
         }
     } else if (role == ROLE_EPI) {
         // ---------------------------------------------------------- epilogue
