@@ -163,18 +163,28 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
-def source_hash():
+# Source files each measured kernel is built from: a traffic figure stays valid only while
+# these are unchanged.
+KERNEL_SOURCES = {
+    "tc_grouped_gemm": ["gemm_tc.cu", "common.cuh", "internal.h", "tma_host.h"],
+    "stream_gemm": ["gemm_stream.cu", "common.cuh", "internal.h"],
+}
+
+
+def source_hash(kernel=None):
+    """Short hash of a kernel's source files (all of csrc/ when kernel is None)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_scaled_fp4_act_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    names = KERNEL_SOURCES[kernel] if kernel else sorted(os.listdir(csrc))
+    for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel_key):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on the
-    current kernel sources (else None)."""
+    """Per-step DRAM bytes from the committed ncu summary, if it was taken on the current
+    sources of that kernel (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -182,7 +192,7 @@ def ncu_traffic(kernel_key):
     except (OSError, ValueError):
         return None
     e = d.get(kernel_key)
-    if not e or e.get("source_hash") != source_hash():
+    if not e or e.get("source_hash") != source_hash(kernel_key.split("/")[0]):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -405,7 +415,10 @@ def run_ours(args, world, rank, local):
                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "kernel": "tc_grouped_gemm",
                     "traffic": ncu_traffic("tc_grouped_gemm/%s" % args.workload),
                     "traffic_basis": "DRAM bytes per step (all grouped calls)",
-                    "peak_source": peak_src + " bf16 dense (burst)"}
+                    "peak_source": peak_src + " bf16 dense (burst)",
+                    # the FP8 dense rate (2x bf16, nominal ratio) for comparison with an
+                    # FP8-MMA design; this path's exact products need 16-bit operands
+                    "fp8_peak": round(2 * peak, 1), "frac_of_fp8": round(achieved / (2 * peak), 4)}
     else:
         # the streaming path is bound by HBM reads of the weights
         kbytes = sum(proj_bytes(c["proj"])[0] for c in calls)

@@ -16,8 +16,10 @@
 // 8 weight rows; lane l reads k in chunks [32 l + 1024 i, +32): 16 B of nibbles per
 // weight row per chunk, so a warp reads 512 contiguous bytes of each row per step.
 // Activation rows of the expert are quantised by the CTA in a prologue (fused
-// act_quant), RB rows at a time, into shared memory as exact f16 code values plus the
-// per-128 f32 scales; the weights of the CTA are re-read (from L2) once per RB rows.
+// act_quant), up to 4 rows a pass, into shared memory as exact f16 code values plus the
+// per-128 f32 scales; the weights of the CTA are re-read (from L2) once per pass. Each
+// pass runs code specialised for its row count (1..4): at decode most experts hold one
+// or two routed rows, and a fixed pass size would spend arithmetic on empty rows.
 #include "common.cuh"
 
 #include <algorithm>
@@ -74,14 +76,151 @@ __device__ __forceinline__ void quantize_chunk(const GroupedProblem &p, int64_t 
     }
 }
 
+// Weights and scales of one 32-wide k chunk for the warp's 8 weight rows.
+template <int GS>
+__device__ __forceinline__ void load_chunk(const uint8_t *wexp, const uint8_t *sexp, size_t wrow,
+                                           size_t srow, int col_base, int n, int kb,
+                                           uint4 (&wv)[kRowsPerWarp],
+                                           uint32_t (&sb)[kRowsPerWarp])
+{
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int col = col_base + i;
+        if (col < n) {
+            wv[i] = ld_stream_v4(wexp + (size_t)col * wrow + (kb >> 1));
+            if (GS == 16)
+                sb[i] = *reinterpret_cast<const uint16_t *>(sexp + (size_t)col * srow + (kb >> 4));
+            else
+                sb[i] = sexp[(size_t)col * srow + (kb >> 5)];
+        } else {
+            wv[i] = make_uint4(0u, 0u, 0u, 0u);
+            sb[i] = 0u;
+        }
+    }
+}
+
+// One pass over the CTA's weight rows for RB quantised activation rows in shared memory.
+// PF: load chunk i + 1 of the weights while chunk i is being multiplied (two register
+// buffers; only where the RB-row accumulators leave room for them).
+template <int RB, int GS, bool PF>
+__device__ __forceinline__ void stream_pass(const GroupedProblem &p, const __half *act,
+                                            const float *ascale, const int *rowok, int64_t c0,
+                                            int rows, const uint8_t *wexp, const uint8_t *sexp,
+                                            int col_base, float s2)
+{
+    const int k = p.k, n = p.n, kq = k >> 7;
+    const int lane = threadIdx.x & 31;
+    const size_t wrow = (size_t)k / 2, srow = (size_t)k / GS;
+
+    float acc[kRowsPerWarp][RB];
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i)
+#pragma unroll
+        for (int r = 0; r < RB; ++r)
+            acc[i][r] = 0.0f;
+
+    uint4 nwv[kRowsPerWarp];
+    uint32_t nsb[kRowsPerWarp];
+    if (PF && lane * 32 < k)
+        load_chunk<GS>(wexp, sexp, wrow, srow, col_base, n, lane * 32, nwv, nsb);
+    for (int kb = lane * 32; kb < k; kb += 1024) {
+        uint4 wv[kRowsPerWarp];
+        uint32_t sb[kRowsPerWarp];
+        if (PF) {
+#pragma unroll
+            for (int i = 0; i < kRowsPerWarp; ++i) {
+                wv[i] = nwv[i];
+                sb[i] = nsb[i];
+            }
+            if (kb + 1024 < k)
+                load_chunk<GS>(wexp, sexp, wrow, srow, col_base, n, kb + 1024, nwv, nsb);
+        } else {
+            load_chunk<GS>(wexp, sexp, wrow, srow, col_base, n, kb, wv, sb);
+        }
+        float asv[RB];
+#pragma unroll
+        for (int r = 0; r < RB; ++r)
+            asv[r] = ascale[r * kq + (kb >> 7)];
+
+        float subm[kRowsPerWarp][RB];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t a[RB][8];
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+                const uint4 *ap = reinterpret_cast<const uint4 *>(act + (size_t)r * k + kb + 16 * h);
+                const uint4 a0 = ap[0], a1 = ap[1];
+                a[r][0] = a0.x; a[r][1] = a0.y; a[r][2] = a0.z; a[r][3] = a0.w;
+                a[r][4] = a1.x; a[r][5] = a1.y; a[r][6] = a1.z; a[r][7] = a1.w;
+            }
+#pragma unroll
+            for (int i = 0; i < kRowsPerWarp; ++i) {
+                uint32_t wh[8];
+                uint32_t lo[4], hi[4];
+                e2m1x8_to_f16x8(h ? wv[i].z : wv[i].x, lo);
+                e2m1x8_to_f16x8(h ? wv[i].w : wv[i].y, hi);
+                wh[0] = lo[0]; wh[1] = lo[1]; wh[2] = lo[2]; wh[3] = lo[3];
+                wh[4] = hi[0]; wh[5] = hi[1]; wh[6] = hi[2]; wh[7] = hi[3];
+#pragma unroll
+                for (int r = 0; r < RB; ++r) {
+                    float sub = (GS == 32 && h == 1) ? subm[i][r] : 0.0f;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        sub = fma2_f16_f32(wh[j], a[r][j], sub);
+                    if (GS == 16) {
+                        const float ws = e4m3_to_f32((sb[i] >> (8 * h)) & 0xFFu) * s2;
+                        acc[i][r] = fmaf(sub, ws * asv[r], acc[i][r]);
+                    } else if (h == 1) {
+                        const float ws = e8m0_to_f32(sb[i]);
+                        acc[i][r] = fmaf(sub, ws * asv[r], acc[i][r]);
+                    } else {
+                        subm[i][r] = sub;
+                    }
+                }
+            }
+        }
+    }
+
+    // Reduce over the 32 lanes; lane i ends up writing column col_base + i.
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+        float mine = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+            const float v = warp_sum(acc[i][r]);
+            if (lane == i)
+                mine = v;
+        }
+        if (r < rows && lane < kRowsPerWarp && col_base + lane < n && rowok[r])
+            p.out[(c0 + r) * (int64_t)n + col_base + lane] = mine;
+    }
+}
+
+// Quantise the next `rows` (= RB) activation rows into shared memory, then stream.
 template <int RB, int GS>
-__global__ void __launch_bounds__(kStreamThreads) stream_gemm_kernel(const GroupedProblem p)
+__device__ __forceinline__ void stream_rows(const GroupedProblem &p, __half *act, float *ascale,
+                                            int *rowok, int64_t c0, const uint8_t *wexp,
+                                            const uint8_t *sexp, int col_base, float s2,
+                                            bool write_codes)
+{
+    __syncthreads();
+    quantize_chunk<RB>(p, c0, RB, act, ascale, rowok, write_codes);
+    __syncthreads();
+    stream_pass<RB, GS, false>(p, act, ascale, rowok, c0, RB, wexp, sexp, col_base, s2);
+}
+
+// RBMAX: most activation rows the shared-memory buffer holds (by k). Each pass takes
+// min(rows left, RBMAX) rows with code specialised for that count, so an expert with one
+// routed row does one row's arithmetic, and an expert with up to RBMAX rows reads its
+// weights once.
+template <int RBMAX, int GS>
+__global__ void __launch_bounds__(kStreamThreads, 2) stream_gemm_kernel(const GroupedProblem p)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     const int k = p.k, n = p.n, kq = k >> 7;
     __half *act = reinterpret_cast<__half *>(smem);
-    float *ascale = reinterpret_cast<float *>(smem + (size_t)RB * k * 2);
-    int *rowok = reinterpret_cast<int *>(ascale + RB * kq);
+    float *ascale = reinterpret_cast<float *>(smem + (size_t)RBMAX * k * 2);
+    int *rowok = reinterpret_cast<int *>(ascale + RBMAX * kq);
 
     const int e = blockIdx.y;
     int64_t r0 = 0, r1 = p.P;
@@ -99,102 +238,30 @@ __global__ void __launch_bounds__(kStreamThreads) stream_gemm_kernel(const Group
     if (r0 >= r1)
         return;
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
     const int col_base = blockIdx.x * kColsPerCta + warp * kRowsPerWarp;
     const float s2 = (GS == 16) ? (p.scale2 ? p.scale2[e] : p.scale2_host) : 1.0f;
-    const size_t wrow = (size_t)k / 2, srow = (size_t)k / GS;
-    const uint8_t *wexp = p.w + (size_t)e * n * wrow;
-    const uint8_t *sexp = p.sc + (size_t)e * n * srow;
+    const uint8_t *wexp = p.w + (size_t)e * n * ((size_t)k / 2);
+    const uint8_t *sexp = p.sc + (size_t)e * n * ((size_t)k / GS);
     const bool write_codes = p.codes_out != nullptr && blockIdx.x == 0;
 
-    for (int64_t c0 = r0; c0 < r1; c0 += RB) {
-        const int rows = (int)((r1 - c0) < RB ? (r1 - c0) : RB);
-        __syncthreads();
-        quantize_chunk<RB>(p, c0, rows, act, ascale, rowok, write_codes);
-        __syncthreads();
-
-        float acc[kRowsPerWarp][RB];
-#pragma unroll
-        for (int i = 0; i < kRowsPerWarp; ++i)
-#pragma unroll
-            for (int r = 0; r < RB; ++r)
-                acc[i][r] = 0.0f;
-
-        for (int kb = lane * 32; kb < k; kb += 1024) {
-            uint4 wv[kRowsPerWarp];
-            uint32_t sb[kRowsPerWarp];
-#pragma unroll
-            for (int i = 0; i < kRowsPerWarp; ++i) {
-                const int col = col_base + i;
-                if (col < n) {
-                    wv[i] = ld_stream_v4(wexp + (size_t)col * wrow + (kb >> 1));
-                    if (GS == 16)
-                        sb[i] = *reinterpret_cast<const uint16_t *>(sexp + (size_t)col * srow +
-                                                                     (kb >> 4));
-                    else
-                        sb[i] = sexp[(size_t)col * srow + (kb >> 5)];
-                } else {
-                    wv[i] = make_uint4(0u, 0u, 0u, 0u);
-                    sb[i] = 0u;
-                }
-            }
-            float asv[RB];
-#pragma unroll
-            for (int r = 0; r < RB; ++r)
-                asv[r] = ascale[r * kq + (kb >> 7)];
-
-            float subm[kRowsPerWarp][RB];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t a[RB][8];
-#pragma unroll
-                for (int r = 0; r < RB; ++r) {
-                    const uint4 *ap =
-                        reinterpret_cast<const uint4 *>(act + (size_t)r * k + kb + 16 * h);
-                    const uint4 a0 = ap[0], a1 = ap[1];
-                    a[r][0] = a0.x; a[r][1] = a0.y; a[r][2] = a0.z; a[r][3] = a0.w;
-                    a[r][4] = a1.x; a[r][5] = a1.y; a[r][6] = a1.z; a[r][7] = a1.w;
-                }
-#pragma unroll
-                for (int i = 0; i < kRowsPerWarp; ++i) {
-                    uint32_t wh[8];
-                    uint32_t lo[4], hi[4];
-                    e2m1x8_to_f16x8(h ? wv[i].z : wv[i].x, lo);
-                    e2m1x8_to_f16x8(h ? wv[i].w : wv[i].y, hi);
-                    wh[0] = lo[0]; wh[1] = lo[1]; wh[2] = lo[2]; wh[3] = lo[3];
-                    wh[4] = hi[0]; wh[5] = hi[1]; wh[6] = hi[2]; wh[7] = hi[3];
-#pragma unroll
-                    for (int r = 0; r < RB; ++r) {
-                        float sub = (GS == 32 && h == 1) ? subm[i][r] : 0.0f;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            sub = fma2_f16_f32(wh[j], a[r][j], sub);
-                        if (GS == 16) {
-                            const float ws = e4m3_to_f32((sb[i] >> (8 * h)) & 0xFFu) * s2;
-                            acc[i][r] = fmaf(sub, ws * asv[r], acc[i][r]);
-                        } else if (h == 1) {
-                            const float ws = e8m0_to_f32(sb[i]);
-                            acc[i][r] = fmaf(sub, ws * asv[r], acc[i][r]);
-                        } else {
-                            subm[i][r] = sub;
-                        }
-                    }
-                }
-            }
-        }
-
-        // Reduce over the 32 lanes; lane i ends up writing column col_base + i.
-#pragma unroll
-        for (int r = 0; r < RB; ++r) {
-            float mine = 0.0f;
-#pragma unroll
-            for (int i = 0; i < kRowsPerWarp; ++i) {
-                const float v = warp_sum(acc[i][r]);
-                if (lane == i)
-                    mine = v;
-            }
-            if (r < rows && lane < kRowsPerWarp && col_base + lane < n && rowok[r])
-                p.out[(c0 + r) * (int64_t)n + col_base + lane] = mine;
+    for (int64_t c0 = r0; c0 < r1;) {
+        const int left = (int)((r1 - c0) < RBMAX ? (r1 - c0) : RBMAX);
+        if (RBMAX >= 4 && left >= 4) {
+            stream_rows<(RBMAX >= 4 ? 4 : 1), GS>(p, act, ascale, rowok, c0, wexp, sexp, col_base,
+                                                   s2, write_codes);
+            c0 += 4;
+        } else if (RBMAX >= 3 && left == 3) {
+            stream_rows<(RBMAX >= 3 ? 3 : 1), GS>(p, act, ascale, rowok, c0, wexp, sexp, col_base,
+                                                   s2, write_codes);
+            c0 += 3;
+        } else if (RBMAX >= 2 && left == 2) {
+            stream_rows<(RBMAX >= 2 ? 2 : 1), GS>(p, act, ascale, rowok, c0, wexp, sexp, col_base,
+                                                   s2, write_codes);
+            c0 += 2;
+        } else {
+            stream_rows<1, GS>(p, act, ascale, rowok, c0, wexp, sexp, col_base, s2, write_codes);
+            c0 += 1;
         }
     }
 }
@@ -204,11 +271,11 @@ static size_t stream_smem_bytes(int rb, int k)
     return (size_t)rb * k * 2 + (size_t)rb * (k / 128) * 4 + (size_t)rb * 4;
 }
 
-template <int RB, int GS>
+template <int RBMAX, int GS>
 static cudaError_t launch_rb(const GroupedProblem &p, cudaStream_t s)
 {
-    const size_t smem = stream_smem_bytes(RB, p.k);
-    auto kern = stream_gemm_kernel<RB, GS>;
+    const size_t smem = stream_smem_bytes(RBMAX, p.k);
+    auto kern = stream_gemm_kernel<RBMAX, GS>;
     if (smem > 48 * 1024) {
         cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

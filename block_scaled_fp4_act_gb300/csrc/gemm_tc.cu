@@ -49,6 +49,7 @@
 // use (a bounded wait on the slot's empty barrier), and then releases the next tile's
 // first stage with a row count of -1, which stops the MMA warp.
 #include "common.cuh"
+#include "tma_host.h"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -117,7 +118,6 @@ constexpr int kTileInfo = A_STAGES;
 static_assert(2 * kTileInfo > A_STAGES, "tile info ring depth");
 constexpr int SMEM_BYTES =
     1024 + RING_BYTES + NUM_BARS * 8 + 16 + (kMaxExperts + 1) * 4 + kTileInfo * 4;
-constexpr long long kTimeoutCycles = 2000000000LL;
 static_assert(B_BYTES % 1024 == 0 && W_BYTES % 1024 == 0 && OFF_W % 1024 == 0,
               "swizzled tiles need 1024-byte alignment");
 static_assert(BN * BK * 2 <= B_BYTES && BN % 16 == 0 && BN <= 256, "activation box");
@@ -155,79 +155,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
     return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok)
-                 : "r"(bar), "r"(parity)
-                 : "memory");
-    return ok != 0;
-}
-
-// As mbar_try_wait, but the thread may sleep in hardware (up to ~10 ms) until the phase
-// completes instead of returning at once, so waiting warps do not take issue slots.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok)
-                 : "r"(bar), "r"(parity), "r"(10000000u)
-                 : "memory");
-    return ok != 0;
-}
-
-// Bounded wait. Returns false if this CTA is aborting (flag set here or elsewhere).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          unsigned *err)
-{
-    if (mbar_try_wait(bar, parity))
-        return true;
-    const long long t0 = clock64();
-    for (;;) {
-        if (mbar_try_wait_sleep(bar, parity))
-            return true;
-        if (*abort_flag)
-            return false;
-        if (clock64() - t0 > kTimeoutCycles) {
-            *abort_flag = 1;
-            raise_device_error(err, FP4_DEVERR_TIMEOUT);
-            return false;
-        }
-    }
-}
-
-// Bounded wait that ignores the abort flag (used to drain in-flight work on abort).
-// Returns false if the phase did not complete in time.
-__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity)
-{
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity))
-        if (clock64() - t0 > kTimeoutCycles / 4)
-            return false;
-    return true;
-}
-
 // Whole-warp forms: lane 0 waits, the warp takes its answer (keeps the warp converged).
 __device__ __forceinline__ bool warp_mbar_wait(uint32_t bar, uint32_t parity,
                                                volatile int *abort_flag, unsigned *err)
@@ -246,26 +173,6 @@ __device__ __forceinline__ bool warp_mbar_drain(uint32_t bar, uint32_t parity)
     return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
 }
 
-// Hardware named barriers, executed by whole converged warps.
-__device__ __forceinline__ void named_sync(int id, int threads)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-__device__ __forceinline__ void named_arrive(int id, int threads)
-{
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            uint32_t bar)
-{
-    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                 " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-                 : "memory");
-}
-
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y,
                                             int z, uint32_t bar)
 {
@@ -273,11 +180,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
                  " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
                  "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
                  : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before()
@@ -1022,20 +924,6 @@ __global__ void __launch_bounds__(256) quant_ws_f16_kernel(const float *__restri
 
 // ------------------------------------------------------------------ host side
 
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }
-    return fn;
-}
-
 // 3-D map {64 k, rows, k-blocks} over a [rows, k] bf16 matrix, box {64, box_rows, box_kb}.
 static bool make_map_kblocks(CUtensorMap *m, const void *base, uint64_t k, uint64_t rows,
                              uint32_t box_rows, uint32_t box_kb)
@@ -1050,22 +938,6 @@ static bool make_map_kblocks(CUtensorMap *m, const void *base, uint64_t k, uint6
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-static bool make_map(CUtensorMap *m, CUtensorMapDataType dt, int elem_bytes, const void *base,
-                     uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
-                     CUtensorMapSwizzle swz)
-{
-    auto fn = encode_fn();
-    if (!fn)
-        return false;
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * (uint64_t)elem_bytes};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t es[2] = {1, 1};
-    return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 } // namespace tc
