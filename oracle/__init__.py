@@ -10,6 +10,8 @@ Functions and the page passages they follow (memra-engine docs.rs source pages):
   grouped_ref_sampled quant_rows + f64_ref per routed row (CSR expert offsets as in
                       0.71.0 src/bin/kernel_check.rs, grouped MoE GEMM section)
   e4m3_decode         0.71.0 src/bin/kernel_check.rs, F8-E4M3 MMVQ section's decoder
+  swiglu              0.98.0 dsv4_native_gemm_gate.rs, swiglu_limit saturation cell and
+                      the f64 check of main: h = min(g,L) * sigmoid(min(g,L)) * clamp(u,-L,L)
   within_bound        the error model stated in the header comment of
                       dsv4_native_gemm_gate.rs and applied in its f64 comparison:
                       |gpu - f64| <= n_ops * 2^-24 * sum|p_scaled|
@@ -52,6 +54,8 @@ def _load():
         lib.orc_act_quant.restype = None
         lib.orc_gemm_ref.argtypes = [P, P, P, P, f32, i32, i64, i64, i64, P, P]
         lib.orc_gemm_ref.restype = None
+        lib.orc_swiglu.argtypes = [P, P, i64, i64, i64, f32, P]
+        lib.orc_swiglu.restype = None
         lib.orc_grouped_ref_sampled.argtypes = [P, i64, i64, P, P, i32, i64, P, P, P, i32, i64,
                                                 P, P, i64, P, P, P, P]
         lib.orc_grouped_ref_sampled.restype = i32
@@ -140,6 +144,18 @@ def act_quant(x):
     scales = np.empty((rows, k // 128), dtype=np.float32)
     _load().orc_act_quant(_ptr(x), rows, k, _ptr(codes), _ptr(scales))
     return codes, scales
+
+
+def swiglu(gate, up, limit):
+    """gate, up f32 [rows, inter] -> h f64 [rows, inter] (the SwiGLU of the page, with
+    the swiglu_limit clamps: up on both sides, gate from above, before the sigmoid)."""
+    gate = _c(gate, np.float32)
+    up = _c(up, np.float32)
+    assert gate.shape == up.shape and gate.ndim == 2
+    rows, inter = gate.shape
+    h = np.empty((rows, inter), dtype=np.float64)
+    _load().orc_swiglu(_ptr(gate), _ptr(up), inter, rows, inter, float(limit), _ptr(h))
+    return h
 
 
 def gemm_ref(codes, scales, w, sc, scale2, recipe):

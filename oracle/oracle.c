@@ -16,6 +16,9 @@
  *        exponent 0 -> subnormal, exponent 15 with mantissa 7 -> NaN).
  *   [S]  same page as [Q]: struct ExpertRaw (nibble pairs [n,k/2], low nibble = even k;
  *        e4m3 scale per 16 (NVFP4) or e8m0 scale per 32 (MXFP4); f32 scale2 for NVFP4).
+ *   [G]  same page as [Q], the swiglu_limit saturation cell and the f64 check of main:
+ *        h = g * (1 / (1 + exp(-g))) * u with u = clamp(up, -L, L) and g = min(gate, L)
+ *        (up clamped on both sides, gate on one side, both before the sigmoid).
  *
  * Readings where the pages import a helper without printing it (each is a plain
  * definition written out here):
@@ -30,6 +33,8 @@
  *
  * Precision: [Q] fixes f32 arithmetic (amax, amax*inv, v/s, clamp) and it is kept in
  * f32 here; [R] is f64 with the per-group weight scale first rounded in f32, kept too.
+ * [G] is evaluated in f64 (the page's f32 evaluation differs from it by a few ulps, the
+ * class its GPU check allows).
  * Build with -O2 -ffp-contract=off (no fused multiply-add contraction).
  */
 #include <math.h>
@@ -268,4 +273,25 @@ int orc_grouped_ref_sampled(const float *x, int64_t T, int64_t k, const int32_t 
                 s2, recipe, k, col, out + s, absp + s);
     }
     return 0;
+}
+
+/* ------------------------------------------------------------------ SwiGLU [G] */
+
+void orc_swiglu(const float *gate, const float *up, int64_t ld, int64_t rows, int64_t inter,
+                float limit, double *h)
+{
+    const double L = (double)limit;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t i = 0; i < inter; ++i) {
+            double u = (double)up[r * ld + i];
+            if (u < -L)
+                u = -L;
+            if (u > L)
+                u = L;
+            double g = (double)gate[r * ld + i];
+            if (g > L)
+                g = L;
+            h[r * inter + i] = g * (1.0 / (1.0 + exp(-g))) * u;
+        }
+    }
 }

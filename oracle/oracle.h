@@ -34,6 +34,11 @@ int orc_grouped_ref_sampled(const float *x, int64_t T, int64_t k, const int32_t 
                             const int64_t *sample_p, const int64_t *sample_col, int64_t ns,
                             double *out, double *absp, uint8_t *tmp_codes, float *tmp_scales);
 
+/* SwiGLU with the swiglu_limit clamps, in f64: gate/up rows of stride ld (elements),
+ * h [rows, inter]. */
+void orc_swiglu(const float *gate, const float *up, int64_t ld, int64_t rows, int64_t inter,
+                float limit, double *h);
+
 #ifdef __cplusplus
 }
 #endif

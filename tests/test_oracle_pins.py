@@ -409,3 +409,68 @@ def test_bound_checker_catches_planted_error():
     ok, ratio, i = oracle.within_bound(ref + np.array([0, 0, 1e-3]), ref, absp, 4.0)
     assert not ok and i == 2
     assert oracle.max_rel(ref + 3e-3, ref) == pytest.approx(1e-3)
+
+
+# ---------------------------------------------------------------- SwiGLU (next row)
+# The page (dsv4_native_gemm_gate.rs, swiglu_limit saturation cell and the f64 check of
+# main) defines h = g * sigmoid(g) * u with u = clamp(up, -L, L) and g = min(gate, L).
+
+def _silu_tanh(x):
+    # logistic through tanh, an identity independent of the oracle's exp form:
+    # sigmoid(x) = (1 + tanh(x / 2)) / 2
+    x = np.asarray(x, dtype=np.float64)
+    return x * 0.5 * (1.0 + np.tanh(0.5 * x))
+
+
+def test_swiglu_matches_tanh_form_inside_the_clamps():
+    rng = np.random.default_rng(11)
+    L = 7.0
+    gate = rng.uniform(-L, L, (4, 256)).astype(np.float32)
+    up = rng.uniform(-L, L, (4, 256)).astype(np.float32)
+    h = oracle.swiglu(gate, up, L)
+    want = _silu_tanh(gate) * up.astype(np.float64)
+    assert np.max(np.abs(h - want)) <= 1e-13 * np.max(np.abs(want))
+
+
+def test_swiglu_odd_part_identity():
+    # silu(x) - silu(-x) = x, so h(g, u) - h(-g, u) = g * u for |g| <= L
+    rng = np.random.default_rng(12)
+    L = 10.0
+    g = rng.uniform(-L, L, (2, 512)).astype(np.float32)
+    u = rng.uniform(-L, L, (2, 512)).astype(np.float32)
+    d = oracle.swiglu(g, u, L) - oracle.swiglu(-g, u, L)
+    want = g.astype(np.float64) * u.astype(np.float64)
+    assert np.max(np.abs(d - want)) <= 1e-12 * np.max(np.abs(want))
+
+
+def test_swiglu_clamp_semantics():
+    L = 7.0
+    one = np.ones((1, 1), np.float32)
+
+    def h(g, u):
+        return oracle.swiglu(np.full((1, 1), g, np.float32), np.full((1, 1), u, np.float32), L)[0, 0]
+
+    # gate clamped from above, before the sigmoid: min(silu(2L), L) would give L instead
+    assert h(2 * L, 1.0) == h(L, 1.0)
+    assert abs(h(L, 1.0) - _silu_tanh(L)) < 1e-12 and h(L, 1.0) < L
+    # gate not clamped from below: silu(-3L) is far smaller than silu(-L)
+    assert abs(h(-3 * L, 1.0) - _silu_tanh(-3 * L)) < 1e-15
+    assert abs(h(-3 * L, 1.0)) < abs(h(-L, 1.0)) / 100
+    # up clamped on both sides
+    assert h(1.0, 5 * L) == h(1.0, L)
+    assert h(1.0, -5 * L) == h(1.0, -L)
+    assert h(1.0, -5 * L) == -h(1.0, 5 * L)
+    # silu(0) = 0 whatever the up value
+    assert h(0.0, 3.0) == 0.0
+    del one
+
+
+def test_swiglu_row_stride_and_shape():
+    rng = np.random.default_rng(13)
+    gate = rng.standard_normal((3, 128)).astype(np.float32) * 4
+    up = rng.standard_normal((3, 128)).astype(np.float32) * 4
+    h = oracle.swiglu(gate, up, 6.0)
+    assert h.shape == (3, 128) and h.dtype == np.float64
+    # rows are independent
+    h1 = oracle.swiglu(gate[1:2], up[1:2], 6.0)
+    assert np.array_equal(h1[0], h[1])
