@@ -46,6 +46,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["c3", "c4", "c5"], default="c4")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-swiglu", action="store_true",
+                    help="skip the SwiGLU + requantisation line (the step after gate/up)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--experts", type=int, default=0, help="override the workload's expert count")
@@ -477,6 +479,10 @@ def run_ours(args, world, rank, local):
             "gpu_launches": dsteps * sum(c["launches"] for c in dcalls)}
         del dcalls, wd, flush
 
+    # the step after the gate/up projection: SwiGLU + e4m3 requantisation of its output
+    if args.workload == "c4" and not args.no_swiglu:
+        result["swiglu_quant"] = measure_swiglu(fp4, device, peaks, peak_src)
+
     # end to end through the public API with host buffers
     if not args.no_e2e:
         e2e_steps = min(steps, 10)
@@ -525,6 +531,42 @@ def run_reference(args, world, rank):
                              "sample": desc},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+
+
+def measure_swiglu(fp4, device, peaks, peak_src, rows=32768, inter=1024, limit=7.0, iters=50):
+    """Time fp4_swiglu_quant on the prefill gate/up output shape (fused [rows, 2*inter]
+    layout, inputs 268 MB: larger than L2). HBM-bound: algorithmic bytes = 8 B read +
+    1 B of code per element + 4 B of scale per 128."""
+    import torch
+    gen = torch.Generator(device=device).manual_seed(21)
+    gu = torch.randn(rows, 2 * inter, generator=gen, device=device) * 3.0
+    gu[::97] *= 50.0
+    gate, up = gu[:, :inter], gu[:, inter:]
+    codes = torch.empty(rows, inter, dtype=torch.uint8, device=device)
+    scales = torch.empty(rows, inter // 128, dtype=torch.float32, device=device)
+    call = lambda: fp4.fp4_swiglu_quant(gate, up, limit, codes=codes, scales=scales)
+    for _ in range(3):
+        call()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(iters):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / iters
+    nbytes = rows * inter * (4 + 4 + 1) + rows * (inter // 128) * 4
+    gbs = nbytes / (us * 1e-6) / 1e9
+    del gu, codes, scales
+    return {"workload": "SwiGLU (swiglu_limit %g) + e4m3 requantisation of the prefill gate/up "
+                        "output [%d, 2x%d] f32" % (limit, rows, inter),
+            "us_per_call": round(us, 2), "calls": iters,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                         "bytes_per_call": nbytes, "kernel": "swiglu_quant",
+                         "peak_source": peak_src},
+            "gpu_launches": iters}
 
 
 def main():

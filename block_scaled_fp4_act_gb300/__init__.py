@@ -65,6 +65,8 @@ def lib():
         L.fp4_grouped_expert_gemm_noalloc.argtypes = [P, i64, P, P, i32, i64, P, P, P, i32, P,
                                                        i64, i64, P]
         L.fp4_grouped_expert_gemm_noalloc.restype = i32
+        L.fp4_swiglu_quant.argtypes = [P, P, i64, f32, i64, i64, P, P, P, P]
+        L.fp4_swiglu_quant.restype = i32
         L.fp4_gemm_path.argtypes = [i64, i32, i64, i64, i32, i32]
         L.fp4_gemm_path.restype = i32
         L.fp4_error_ops.argtypes = [i32, i32, i64]
@@ -219,6 +221,38 @@ def fp4_grouped_expert_gemm_noalloc(x, row_ids, offsets, w, wscale, scale2, reci
                                                  _ptr(out), n, k, _stream(stream)),
            "fp4_grouped_expert_gemm_noalloc")
     return out
+
+
+def fp4_swiglu_quant(gate, up, limit, want_h=False, codes=None, scales=None, h_out=None,
+                     stream=None):
+    """SwiGLU with the swiglu_limit clamps, fused with the e4m3 requantisation of h.
+
+    gate, up: f32 CUDA tensors [rows, inter] with unit column stride and the same row
+    stride (e.g. the two halves of a fused gate/up output). Returns (codes [rows, inter]
+    u8, scales [rows, inter/128] f32, h [rows, inter] f32 or None)."""
+    import torch
+    if gate.dtype != torch.float32 or up.dtype != torch.float32 or not gate.is_cuda:
+        raise ValueError("gate and up must be f32 CUDA tensors")
+    if gate.shape != up.shape or gate.dim() != 2:
+        raise ValueError("gate and up must have the same 2-D shape")
+    if gate.stride(1) != 1 or up.stride(1) != 1 or gate.stride(0) != up.stride(0):
+        raise ValueError("gate and up need unit column stride and one row stride")
+    rows, inter = gate.shape
+    ld = gate.stride(0) if rows > 1 else inter
+    if codes is None:
+        codes = torch.empty((rows, inter), dtype=torch.uint8, device=gate.device)
+    if scales is None:
+        scales = torch.empty((rows, inter // 128), dtype=torch.float32, device=gate.device)
+    _need(codes, torch.uint8, (rows, inter), "codes")
+    _need(scales, torch.float32, (rows, inter // 128), "scales")
+    if want_h and h_out is None:
+        h_out = torch.empty((rows, inter), dtype=torch.float32, device=gate.device)
+    if h_out is not None:
+        _need(h_out, torch.float32, (rows, inter), "h_out")
+    _check(lib().fp4_swiglu_quant(_ptr(gate), _ptr(up), ld, float(limit), rows, inter,
+                                  _ptr(h_out), _ptr(codes), _ptr(scales), _stream(stream)),
+           "fp4_swiglu_quant")
+    return codes, scales, h_out
 
 
 def fp4_gemm_path(total_rows, num_experts, n, k, recipe, have_workspace=True):

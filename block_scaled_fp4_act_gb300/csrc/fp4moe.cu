@@ -137,6 +137,24 @@ int act_quant_fp8(const float *x, uint8_t *codes, float *scales, int64_t rows, i
     return record(launch_act_quant(x, codes, scales, rows, k, (cudaStream_t)stream));
 }
 
+int fp4_swiglu_quant(const float *gate, const float *up, int64_t ld, float limit, int64_t rows,
+                     int64_t inter, float *h_out, uint8_t *codes, float *scales, void *stream)
+{
+    if (rows < 0 || inter < 0 || !(limit > 0.0f) || !(limit < 3.0e38f))
+        return FP4_ERR_ARG;
+    if (inter == 0 || inter % 128 != 0 || ld < inter || ld % 4 != 0)
+        return FP4_ERR_SHAPE;
+    if (rows == 0)
+        return FP4_OK;
+    if (!gate || !up || !codes || !scales)
+        return FP4_ERR_ARG;
+    if (!aligned16(gate) || !aligned16(up) || !aligned16(codes) || !aligned16(scales) ||
+        (h_out && !aligned16(h_out)))
+        return FP4_ERR_ALIGN;
+    return record(launch_swiglu_quant(gate, up, ld, limit, rows, inter, h_out, codes, scales,
+                                      (cudaStream_t)stream));
+}
+
 int fp4_expert_gemm(const float *x, const uint8_t *w, const uint8_t *wscale, float scale2,
                     int recipe, float *out, int64_t g, int64_t n, int64_t k, uint8_t *codes_out,
                     float *scales_out, void *workspace, size_t workspace_bytes, void *stream)

@@ -37,6 +37,9 @@ unsigned *device_error_word();
 // Kernel launchers; each returns cudaSuccess or the launch error.
 cudaError_t launch_act_quant(const float *x, uint8_t *codes, float *scales, int64_t rows,
                              int64_t k, cudaStream_t s);
+cudaError_t launch_swiglu_quant(const float *gate, const float *up, int64_t ld, float limit,
+                                int64_t rows, int64_t inter, float *h_out, uint8_t *codes,
+                                float *scales, cudaStream_t s);
 cudaError_t launch_stream_gemm(const GroupedProblem &p, int rows_per_pass, cudaStream_t s);
 
 // Error-model constants of each path (n_ops of |err| <= n_ops 2^-24 sum|p|).

@@ -138,6 +138,25 @@ int fp4_grouped_expert_gemm_noalloc(const float *x, int64_t num_tokens, const in
                                     const uint8_t *w, const uint8_t *wscale, const float *scale2,
                                     int recipe, float *out, int64_t n, int64_t k, void *stream);
 
+/*
+ * fp4_swiglu_quant -- the step after the gate/up projection: SwiGLU with the
+ * swiglu_limit clamps (dsv4_native_gemm_gate.rs, swiglu_limit saturation cell and the f64
+ * check of main), fused with fn quant_rows of its output (the down projection's input):
+ *   u = clamp(up, -limit, limit), g = min(gate, limit), h = g * (1 / (1 + exp(-g))) * u,
+ *   then per 128 elements of h: pow2 scale and e4m3 codes exactly as act_quant_fp8.
+ *   gate, up  rows of `inter` f32 at a row stride of `ld` elements (ld >= inter,
+ *             ld % 4 == 0): separate [rows, inter] tensors (ld = inter), or the two halves
+ *             of a fused gate/up output [rows, 2*inter] (up = gate + inter, ld = 2*inter)
+ *   limit     the swiglu_limit, finite and > 0
+ *   h_out     nullable [rows, inter] f32: h itself (within a few ulps of exact: expf)
+ *   codes     [rows, inter] e4m3 bytes, scales [rows, inter/128] f32 (powers of two);
+ *             equal, bit for bit, to act_quant_fp8 of the h this call computed
+ * inter must be a positive multiple of 128; rows == 0 is a no-op returning FP4_OK.
+ * Inputs are finite (as everywhere in this library).
+ */
+int fp4_swiglu_quant(const float *gate, const float *up, int64_t ld, float limit, int64_t rows,
+                     int64_t inter, float *h_out, uint8_t *codes, float *scales, void *stream);
+
 /* Which path a grouped call of this shape takes (never FP4_PATH_AUTO). */
 int fp4_gemm_path(int64_t total_rows, int num_experts, int64_t n, int64_t k, int recipe,
                   int have_workspace);

@@ -74,6 +74,19 @@ def test_host_side_argument_checks(lib):
     assert G(a16, 8, None, a16, 2, 8, odd, a16, a16, 1, a16, 4, 128, None, 0, None) == \
         fp4.FP4_ERR_ALIGN
     assert G(a16, 8, None, a16, 2, 0, a16, a16, a16, 1, a16, 4, 128, None, 0, None) == fp4.FP4_OK
+    # fp4_swiglu_quant(gate, up, ld, limit, rows, inter, h_out, codes, scales, stream)
+    S = lib.fp4_swiglu_quant
+    assert S(a16, a16, 256, 0.0, 2, 256, None, a16, a16, None) == fp4.FP4_ERR_ARG     # limit <= 0
+    assert S(a16, a16, 256, float("inf"), 2, 256, None, a16, a16, None) == fp4.FP4_ERR_ARG
+    assert S(a16, a16, 256, float("nan"), 2, 256, None, a16, a16, None) == fp4.FP4_ERR_ARG
+    assert S(a16, a16, 200, 7.0, 2, 200, None, a16, a16, None) == fp4.FP4_ERR_SHAPE   # inter % 128
+    assert S(a16, a16, 128, 7.0, 2, 256, None, a16, a16, None) == fp4.FP4_ERR_SHAPE   # ld < inter
+    assert S(a16, a16, 258, 7.0, 2, 256, None, a16, a16, None) == fp4.FP4_ERR_SHAPE   # ld % 4
+    assert S(None, a16, 256, 7.0, 2, 256, None, a16, a16, None) == fp4.FP4_ERR_ARG
+    assert S(a16, a16, 256, 7.0, 2, 256, None, None, a16, None) == fp4.FP4_ERR_ARG
+    assert S(odd, a16, 256, 7.0, 2, 256, None, a16, a16, None) == fp4.FP4_ERR_ALIGN
+    assert S(a16, a16, 256, 7.0, 2, 256, odd, a16, a16, None) == fp4.FP4_ERR_ALIGN
+    assert S(None, None, 256, 7.0, 0, 256, None, None, None, None) == fp4.FP4_OK      # empty
 
 
 def test_status_strings_and_error_model(lib):
