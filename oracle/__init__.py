@@ -10,6 +10,8 @@ Functions and the page passages they follow (memra-engine docs.rs source pages):
   grouped_ref_sampled quant_rows + f64_ref per routed row (CSR expert offsets as in
                       0.71.0 src/bin/kernel_check.rs, grouped MoE GEMM section)
   e4m3_decode         0.71.0 src/bin/kernel_check.rs, F8-E4M3 MMVQ section's decoder
+  mirror_gemm         same page, fn mirror_gemm: the page's own kernel order in f32
+                      (128 strided partials per output + a fixed halving tree)
   swiglu              0.98.0 dsv4_native_gemm_gate.rs, swiglu_limit saturation cell and
                       the f64 check of main: h = min(g,L) * sigmoid(min(g,L)) * clamp(u,-L,L)
   within_bound        the error model stated in the header comment of
@@ -54,6 +56,8 @@ def _load():
         lib.orc_act_quant.restype = None
         lib.orc_gemm_ref.argtypes = [P, P, P, P, f32, i32, i64, i64, i64, P, P]
         lib.orc_gemm_ref.restype = None
+        lib.orc_mirror_gemm.argtypes = [P, P, P, P, f32, i32, i64, i64, i64, P]
+        lib.orc_mirror_gemm.restype = None
         lib.orc_swiglu.argtypes = [P, P, i64, i64, i64, f32, P]
         lib.orc_swiglu.restype = None
         lib.orc_grouped_ref_sampled.argtypes = [P, i64, i64, P, P, i32, i64, P, P, P, i32, i64,
@@ -144,6 +148,21 @@ def act_quant(x):
     scales = np.empty((rows, k // 128), dtype=np.float32)
     _load().orc_act_quant(_ptr(x), rows, k, _ptr(codes), _ptr(scales))
     return codes, scales
+
+
+def mirror_gemm(codes, scales, w, sc, scale2, recipe):
+    """The page's mirror order in f32: codes [g,k] u8, scales [g,k/128] f32, w [n,k/2],
+    sc [n,k/gs] -> out f32 [g,n]."""
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.float32)
+    w = _c(w, np.uint8)
+    sc = _c(sc, np.uint8)
+    g, k = codes.shape
+    n = w.shape[0]
+    out = np.empty((g, n), dtype=np.float32)
+    _load().orc_mirror_gemm(_ptr(codes), _ptr(scales), _ptr(w), _ptr(sc), float(scale2),
+                            int(recipe), g, n, k, _ptr(out))
+    return out
 
 
 def swiglu(gate, up, limit):

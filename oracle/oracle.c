@@ -16,6 +16,10 @@
  *        exponent 0 -> subnormal, exponent 15 with mantissa 7 -> NaN).
  *   [S]  same page as [Q]: struct ExpertRaw (nibble pairs [n,k/2], low nibble = even k;
  *        e4m3 scale per 16 (NVFP4) or e8m0 scale per 32 (MXFP4); f32 scale2 for NVFP4).
+ *   [M]  same page as [Q], fn mirror_gemm: the order of the page's own GPU kernel, in f32:
+ *        128 partials per output, partial t takes groups t, t+128, ..., each group's
+ *        sum of gs products accumulated in order, times f32(ws * as), added to the
+ *        partial; then a fixed halving tree (offsets 64, 32, ..., 1).
  *   [G]  same page as [Q], the swiglu_limit saturation cell and the f64 check of main:
  *        h = g * (1 / (1 + exp(-g))) * u with u = clamp(up, -L, L) and g = min(gate, L)
  *        (up clamped on both sides, gate on one side, both before the sigmoid).
@@ -292,6 +296,51 @@ void orc_swiglu(const float *gate, const float *up, int64_t ld, int64_t rows, in
             if (g > L)
                 g = L;
             h[r * inter + i] = g * (1.0 / (1.0 + exp(-g))) * u;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ mirror order [M] */
+
+#define ORC_MIRROR_THREADS 128
+
+void orc_mirror_gemm(const uint8_t *codes, const float *scales, const uint8_t *w,
+                     const uint8_t *sc, float scale2, int recipe, int64_t g, int64_t n, int64_t k,
+                     float *out)
+{
+    init_tables();
+    const int gs = group_size(recipe);
+    const int64_t ngroups = k / gs, kq = k / 128;
+    float part[ORC_MIRROR_THREADS];
+    for (int64_t r = 0; r < g; ++r) {
+        const uint8_t *arow = codes + r * k;
+        const float *asrow = scales + r * kq;
+        for (int64_t c = 0; c < n; ++c) {
+            const uint8_t *wrow = w + c * (k / 2);
+            const uint8_t *srow = sc + c * ngroups;
+            for (int t = 0; t < ORC_MIRROR_THREADS; ++t) {
+                float acc = 0.0f;
+                for (int64_t j = t; j < ngroups; j += ORC_MIRROR_THREADS) {
+                    const int64_t k0 = j * gs;
+                    float sub = 0.0f;
+                    for (int i = 0; i < gs; ++i) {
+                        const int64_t kk = k0 + i;
+                        const uint8_t byte = wrow[kk >> 1];
+                        const uint8_t nib = (kk & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0x0F);
+                        const float prod = (float)g_e4m3[arow[kk]] * (float)g_e2m1[nib];
+                        sub = sub + prod;
+                    }
+                    const float ws = weight_scale(recipe, srow[j], scale2);
+                    const float scl = ws * asrow[k0 / 128];
+                    const float term = sub * scl;
+                    acc = acc + term;
+                }
+                part[t] = acc;
+            }
+            for (int off = ORC_MIRROR_THREADS >> 1; off > 0; off >>= 1)
+                for (int t = 0; t < off; ++t)
+                    part[t] = part[t] + part[t + off];
+            out[r * n + c] = part[0];
         }
     }
 }

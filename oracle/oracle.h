@@ -34,6 +34,11 @@ int orc_grouped_ref_sampled(const float *x, int64_t T, int64_t k, const int32_t 
                             const int64_t *sample_p, const int64_t *sample_col, int64_t ns,
                             double *out, double *absp, uint8_t *tmp_codes, float *tmp_scales);
 
+/* The page's mirror order in f32 (128 strided partials + halving tree): out [g,n]. */
+void orc_mirror_gemm(const uint8_t *codes, const float *scales, const uint8_t *w,
+                     const uint8_t *sc, float scale2, int recipe, int64_t g, int64_t n, int64_t k,
+                     float *out);
+
 /* SwiGLU with the swiglu_limit clamps, in f64: gate/up rows of stride ld (elements),
  * h [rows, inter]. */
 void orc_swiglu(const float *gate, const float *up, int64_t ld, int64_t rows, int64_t inter,

@@ -474,3 +474,70 @@ def test_swiglu_row_stride_and_shape():
     # rows are independent
     h1 = oracle.swiglu(gate[1:2], up[1:2], 6.0)
     assert np.array_equal(h1[0], h[1])
+
+
+# ---------------------------------------------------------------- mirror order (next row)
+# fn mirror_gemm of dsv4_native_gemm_gate.rs: the page's kernel order in f32.
+
+@pytest.mark.parametrize("recipe", [oracle.NVFP4, oracle.MXFP4])
+def test_mirror_lossless_case_is_plain_matmul(recipe, golden_dir):
+    # every partial sum is exact in f32 here (half-integers, |sum| <= k * 448 * 2 * 6
+    # < 2^23 for k <= 1024), so any order gives the exact matmul
+    rng = np.random.default_rng(41 + recipe)
+    table = golden_e2m1(golden_dir)
+    for g, n, k in [(3, 5, 256), (4, 9, 1024)]:
+        x, w, sc = _exact_inputs(rng, g, n, k, recipe)
+        codes, scales = oracle.act_quant(x)
+        got = oracle.mirror_gemm(codes, scales, w, sc, 1.0, recipe).astype(np.float64)
+        want = x.astype(np.float64) @ _dense_weights(w, table).T
+        assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("recipe", [oracle.NVFP4, oracle.MXFP4])
+def test_mirror_within_the_pages_bound(recipe):
+    # the page states |mirror-order kernel - f64| <= n_ops 2^-24 sum|p| with
+    # n_ops = (gs - 1) + ceil((k/gs)/128) + 7, for exactly this summation structure
+    rng = np.random.default_rng(43 + recipe)
+    gs = 16 if recipe == oracle.NVFP4 else 32
+    for g, n, k in [(4, 32, 512), (3, 16, 8192)]:
+        x = (rng.standard_normal((g, k)) * 3).astype(np.float32)
+        w = rng.integers(0, 256, (n, k // 2), dtype=np.uint8)
+        sc = (rng.integers(0x20, 0x41, (n, k // gs)) if recipe == oracle.NVFP4
+              else rng.integers(118, 135, (n, k // gs))).astype(np.uint8)
+        s2 = 1.0 / 64 if recipe == oracle.NVFP4 else 0.0
+        codes, scales = oracle.act_quant(x)
+        ref, absp = oracle.gemm_ref(codes, scales, w, sc, s2, recipe)
+        got = oracle.mirror_gemm(codes, scales, w, sc, s2, recipe)
+        n_ops = (gs - 1) + int(np.ceil((k / gs) / 128)) + 7
+        ok, worst, _ = oracle.within_bound(got, ref, absp, n_ops)
+        assert ok, worst
+        assert np.any(got.astype(np.float64) != ref)  # it does round
+
+
+def test_mirror_halving_tree_order():
+    """Worked example, k = 2048 (128 NVFP4 groups: partial t holds group t alone).
+    Group 0 gives 32, groups 1 and 65 give 32 * 2^-24 each. The halving tree adds
+    groups 1 and 65 first (offset 64), then that 2^-18 to 32 (offset 1): 32 + 2^-18,
+    exact in f32. Adding left to right would give 32 (each 2^-19 is a tie to even)."""
+    k, gs = 2048, 16
+    codes = np.zeros((1, k), np.uint8)
+    scales = np.ones((1, k // 128), np.float32)
+    w = np.zeros((1, k // 2), np.uint8)
+    sc = np.full((1, k // gs), 0x38, np.uint8)          # weight scale e4m3 1.0
+    # group 0: a = 2 (0x40), w = 4 (E2M1 code 6, even k -> low nibble), ws = 4 (0x48): 32
+    codes[0, 0] = 0x40
+    w[0, 0] = 0x06
+    sc[0, 0] = 0x48
+    # groups 1 and 65: a = 2^-9 (0x01), w = 0.5 (code 1), ws = 2^-9 (0x01): 2^-19 each
+    for grp in (1, 65):
+        codes[0, grp * gs] = 0x01
+        w[0, grp * gs // 2] = 0x01
+        sc[0, grp] = 0x01
+    got = oracle.mirror_gemm(codes, scales, w, sc, 1.0, oracle.NVFP4)[0, 0]
+    assert got == np.float32(32.0 + 2.0 ** -18)
+    seq = np.float32(32.0)
+    for _ in range(2):
+        seq = np.float32(seq + np.float32(2.0 ** -19))
+    assert seq == np.float32(32.0)          # the order matters for this input
+    ref, _ = oracle.gemm_ref(codes, scales, w, sc, 1.0, oracle.NVFP4)
+    assert ref[0, 0] == 32.0 + 2.0 ** -18   # and the tree result is the exact sum
