@@ -65,6 +65,8 @@ def lib():
         L.fp4_grouped_expert_gemm_noalloc.argtypes = [P, i64, P, P, i32, i64, P, P, P, i32, P,
                                                        i64, i64, P]
         L.fp4_grouped_expert_gemm_noalloc.restype = i32
+        L.fp4_gemm_mirror.argtypes = [P, P, P, P, f32, i32, P, i64, i64, i64, P]
+        L.fp4_gemm_mirror.restype = i32
         L.fp4_swiglu_quant.argtypes = [P, P, i64, f32, i64, i64, P, P, P, P]
         L.fp4_swiglu_quant.restype = i32
         L.fp4_gemm_path.argtypes = [i64, i32, i64, i64, i32, i32]
@@ -220,6 +222,25 @@ def fp4_grouped_expert_gemm_noalloc(x, row_ids, offsets, w, wscale, scale2, reci
                                                  _ptr(w), _ptr(wscale), _ptr(scale2), int(recipe),
                                                  _ptr(out), n, k, _stream(stream)),
            "fp4_grouped_expert_gemm_noalloc")
+    return out
+
+
+def fp4_gemm_mirror(codes, scales, w, wscale, scale2, recipe, out=None, stream=None):
+    """One expert from quantised activations in the page's own kernel order, bit for bit:
+    codes [g,k] u8, scales [g,k/128] f32, w [n,k/2] u8, wscale [n,k/gs] u8 -> out [g,n]."""
+    import torch
+    g, k = codes.shape
+    n = w.shape[0]
+    _need(codes, torch.uint8, (g, k), "codes")
+    _need(scales, torch.float32, (g, k // 128), "scales")
+    _need(w, torch.uint8, (n, k // 2), "w")
+    _need(wscale, torch.uint8, (n, k // group_size(recipe)), "wscale")
+    if out is None:
+        out = torch.empty((g, n), dtype=torch.float32, device=codes.device)
+    _need(out, torch.float32, (g, n), "out")
+    _check(lib().fp4_gemm_mirror(_ptr(codes), _ptr(scales), _ptr(w), _ptr(wscale), float(scale2),
+                                 int(recipe), _ptr(out), g, n, k, _stream(stream)),
+           "fp4_gemm_mirror")
     return out
 
 

@@ -137,6 +137,25 @@ int act_quant_fp8(const float *x, uint8_t *codes, float *scales, int64_t rows, i
     return record(launch_act_quant(x, codes, scales, rows, k, (cudaStream_t)stream));
 }
 
+int fp4_gemm_mirror(const uint8_t *codes, const float *scales, const uint8_t *w,
+                    const uint8_t *wscale, float scale2, int recipe, float *out, int64_t g,
+                    int64_t n, int64_t k, void *stream)
+{
+    if (!recipe_ok(recipe))
+        return FP4_ERR_ARG;
+    int st = check_shape(g, n, k);
+    if (st != FP4_OK)
+        return st;
+    if (n > 0x7FFFFFFF)
+        return FP4_ERR_SHAPE;
+    if (g == 0)
+        return FP4_OK;
+    if (!codes || !scales || !w || !wscale || !out)
+        return FP4_ERR_ARG;
+    return record(launch_mirror_gemm(codes, scales, w, wscale, scale2, recipe, out, g, n, k,
+                                     (cudaStream_t)stream));
+}
+
 int fp4_swiglu_quant(const float *gate, const float *up, int64_t ld, float limit, int64_t rows,
                      int64_t inter, float *h_out, uint8_t *codes, float *scales, void *stream)
 {

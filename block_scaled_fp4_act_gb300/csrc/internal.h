@@ -37,6 +37,9 @@ unsigned *device_error_word();
 // Kernel launchers; each returns cudaSuccess or the launch error.
 cudaError_t launch_act_quant(const float *x, uint8_t *codes, float *scales, int64_t rows,
                              int64_t k, cudaStream_t s);
+cudaError_t launch_mirror_gemm(const uint8_t *codes, const float *scales, const uint8_t *w,
+                               const uint8_t *wscale, float scale2, int recipe, float *out,
+                               int64_t g, int64_t n, int64_t k, cudaStream_t s);
 cudaError_t launch_swiglu_quant(const float *gate, const float *up, int64_t ld, float limit,
                                 int64_t rows, int64_t inter, float *h_out, uint8_t *codes,
                                 float *scales, cudaStream_t s);

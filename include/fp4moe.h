@@ -139,6 +139,22 @@ int fp4_grouped_expert_gemm_noalloc(const float *x, int64_t num_tokens, const in
                                     int recipe, float *out, int64_t n, int64_t k, void *stream);
 
 /*
+ * fp4_gemm_mirror -- one expert's GEMM from already-quantised activations, in the page's
+ * own kernel order (dsv4_native_gemm_gate.rs, fn mirror_gemm), bit for bit: per output,
+ * 128 partials (partial t takes weight groups t, t+128, ...; a group's gs products summed
+ * in k order, times f32(ws * as), added), then a fixed halving tree; every operation a
+ * separately rounded f32 multiply or add. Arguments as the page's memra_dsv4_fp4_gemm:
+ *   codes  [g, k] e4m3 bytes, scales [g, k/128] f32 (as act_quant_fp8 writes them)
+ *   w      [n, k/2] nibble pairs, wscale [n, k/gs] scale bytes, scale2 (NVFP4)
+ *   out    [g, n] f32
+ * An instrument for bit-identity with the pages' mirror, not a fast path (one 128-thread
+ * CTA per output). k must be a positive multiple of 128; g == 0 is a no-op.
+ */
+int fp4_gemm_mirror(const uint8_t *codes, const float *scales, const uint8_t *w,
+                    const uint8_t *wscale, float scale2, int recipe, float *out, int64_t g,
+                    int64_t n, int64_t k, void *stream);
+
+/*
  * fp4_swiglu_quant -- the step after the gate/up projection: SwiGLU with the
  * swiglu_limit clamps (dsv4_native_gemm_gate.rs, swiglu_limit saturation cell and the f64
  * check of main), fused with fn quant_rows of its output (the down projection's input):

@@ -74,6 +74,12 @@ def test_host_side_argument_checks(lib):
     assert G(a16, 8, None, a16, 2, 8, odd, a16, a16, 1, a16, 4, 128, None, 0, None) == \
         fp4.FP4_ERR_ALIGN
     assert G(a16, 8, None, a16, 2, 0, a16, a16, a16, 1, a16, 4, 128, None, 0, None) == fp4.FP4_OK
+    # fp4_gemm_mirror(codes, scales, w, wscale, scale2, recipe, out, g, n, k, stream)
+    M = lib.fp4_gemm_mirror
+    assert M(a16, a16, a16, a16, 1.0, 5, a16, 2, 4, 128, None) == fp4.FP4_ERR_ARG      # recipe
+    assert M(a16, a16, a16, a16, 1.0, 0, a16, 2, 4, 100, None) == fp4.FP4_ERR_SHAPE    # k % 128
+    assert M(a16, None, a16, a16, 1.0, 0, a16, 2, 4, 128, None) == fp4.FP4_ERR_ARG
+    assert M(None, None, None, None, 1.0, 0, None, 0, 4, 128, None) == fp4.FP4_OK     # empty
     # fp4_swiglu_quant(gate, up, ld, limit, rows, inter, h_out, codes, scales, stream)
     S = lib.fp4_swiglu_quant
     assert S(a16, a16, 256, 0.0, 2, 256, None, a16, a16, None) == fp4.FP4_ERR_ARG     # limit <= 0
