@@ -278,10 +278,15 @@ def time_steps(calls, steps, flush=None):
 
 
 def run_e2e(fp4, calls, steps):
-    """Same step through the public API with host buffers: pinned host inputs copied in,
-    outputs copied back, inside the timed region."""
+    """Same step through the public API with host buffers: every step copies its inputs
+    in from pinned host memory and its outputs back, inside the timed region. Pipelined as
+    a user would run it: host->device copies on one stream, the grouped calls on the
+    compute stream, device->host copies on a third, with two sets of device buffers so
+    step i+1's inputs arrive and step i-1's outputs leave while step i computes. Events
+    order every reuse of a buffer."""
     import torch
-    host_in, host_out, dev_in = [], [], []
+    dev = calls[0]["out"].device
+    host_in, host_out, dev_in, dev_out = [], [], [[], []], [[], []]
     h2d = d2h = 0
     for c in calls:
         p = c["proj"]
@@ -289,37 +294,70 @@ def run_e2e(fp4, calls, steps):
         hr = p.routing.row_ids.cpu().pin_memory()
         ho = p.routing.offsets.cpu().pin_memory()
         host_in.append((hx, hr, ho))
-        dev_in.append((torch.empty_like(p.x), torch.empty_like(p.routing.row_ids),
-                       torch.empty_like(p.routing.offsets)))
+        for b in range(2):
+            dev_in[b].append((torch.empty_like(p.x), torch.empty_like(p.routing.row_ids),
+                              torch.empty_like(p.routing.offsets)))
+            dev_out[b].append(torch.empty_like(c["out"]))
         host_out.append(torch.empty(c["out"].shape, dtype=torch.float32).pin_memory())
         h2d += hx.numel() * 4 + (hr.numel() * 4 if p.row_ids_used else 0) + ho.numel() * 4
         d2h += c["out"].numel() * 4
-    stream = torch.cuda.current_stream()
+    comp = torch.cuda.current_stream()
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event()
+    inputs_read = [ev(), ev()]    # compute done with input buffer b
+    outputs_read = [ev(), ev()]   # device->host copies done with output buffer b
+    for b in range(2):
+        inputs_read[b].record(comp)
+        outputs_read[b].record(comp)
 
-    def step():
-        for c, (hx, hr, ho), (dx, dr, do), hout in zip(calls, host_in, dev_in, host_out):
+    def step(i):
+        b = i & 1
+        arrived = ev()
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(inputs_read[b])
+            for c, (hx, hr, ho), (dx, dr, do) in zip(calls, host_in, dev_in[b]):
+                dx.copy_(hx, non_blocking=True)
+                do.copy_(ho, non_blocking=True)
+                if c["proj"].row_ids_used:
+                    dr.copy_(hr, non_blocking=True)
+            arrived.record(s_in)
+        comp.wait_event(arrived)
+        comp.wait_event(outputs_read[b])
+        done = []
+        for c, (dx, dr, do), dout in zip(calls, dev_in[b], dev_out[b]):
             p = c["proj"]
-            dx.copy_(hx, non_blocking=True)
-            do.copy_(ho, non_blocking=True)
-            rid = None
-            if p.row_ids_used:
-                dr.copy_(hr, non_blocking=True)
-                rid = dr
-            fp4.fp4_grouped_expert_gemm(dx, rid, do, p.bank.w, p.bank.sc, p.bank.scale2,
-                                        p.bank.recipe, out=c["out"], workspace=c["ws"])
-            hout.copy_(c["out"], non_blocking=True)
+            fp4.fp4_grouped_expert_gemm(dx, dr if p.row_ids_used else None, do, p.bank.w,
+                                        p.bank.sc, p.bank.scale2, p.bank.recipe, out=dout,
+                                        workspace=c["ws"])
+            e = ev()
+            e.record(comp)
+            done.append(e)
+        inputs_read[b].record(comp)
+        with torch.cuda.stream(s_out):
+            for e, dout, hout in zip(done, dev_out[b], host_out):
+                s_out.wait_event(e)
+                hout.copy_(dout, non_blocking=True)
+            outputs_read[b].record(s_out)
 
-    for _ in range(2):
-        step()
+    for i in range(2):
+        step(i)
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(steps):
-        step()
-    t1.record(stream)
+    t0.record(comp)
+    s_in.wait_event(t0)
+    s_out.wait_event(t0)
+    for i in range(steps):
+        step(i)
+    last = ev()
+    last.record(s_out)
+    comp.wait_event(last)
+    t1.record(comp)
     torch.cuda.synchronize()
-    return t0.elapsed_time(t1) / steps, h2d, d2h
+    # the host holds the last step's outputs
+    ok = all(torch.equal(hout, dout.cpu()) for hout, dout in zip(host_out, dev_out[(steps - 1) & 1]))
+    return t0.elapsed_time(t1) / steps, h2d, d2h, ok
 
 
 def cpu_oracle_sample(wl, budget_s, rows_cap=None, seed=0):
@@ -492,12 +530,14 @@ def run_ours(args, world, rank, local):
     # end to end through the public API with host buffers
     if not args.no_e2e:
         e2e_steps = min(steps, 10)
-        e2e_ms, h2d, d2h = run_e2e(fp4, calls, e2e_steps)
+        e2e_ms, h2d, d2h, e2e_ok = run_e2e(fp4, calls, e2e_steps)
         e2e_ms = max_over_ranks(e2e_ms, world)
         result["e2e"] = {"value": round(world * flops_step / (e2e_ms * 1e-3) / 1e12, 3),
                          "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                          "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
-                         "steps": e2e_steps}
+                         "steps": e2e_steps, "outputs_match": e2e_ok,
+                         "schedule": "copies in / grouped calls / copies out on three "
+                                     "streams, double-buffered device inputs and outputs"}
 
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         fl, secs, desc = cpu_oracle_sample(wl, 12.0)
