@@ -82,6 +82,16 @@ static int stream_rows_per_pass(int64_t P, int E)
     return 4;
 }
 
+// The path that needs no workspace: the warp-MMA decode kernel wherever 8 activation rows
+// of length k fit in shared memory (8 rows per pass once experts average more than 4),
+// the FMA streaming kernel beyond that.
+static cudaError_t launch_streaming(const GroupedProblem &p, cudaStream_t s)
+{
+    if (decode_fits(p.k))
+        return launch_decode_gemm(p, p.P > 4 * (int64_t)p.E ? 8 : 4, s);
+    return launch_stream_gemm(p, stream_rows_per_pass(p.P, p.E), s);
+}
+
 // Shared shape checks; returns FP4_OK or the status to report.
 static int check_shape(int64_t rows, int64_t n, int64_t k)
 {
@@ -112,7 +122,7 @@ static int run_grouped(GroupedProblem p, void *workspace, size_t ws_bytes, cudaS
             return FP4_ERR_WORKSPACE;
         return record(launch_tc_gemm(p, workspace, s));
     }
-    return record(launch_stream_gemm(p, stream_rows_per_pass(p.P, p.E), s));
+    return record(launch_streaming(p, s));
 }
 
 } // namespace fp4moe
@@ -212,7 +222,7 @@ int fp4_expert_gemm(const float *x, const uint8_t *w, const uint8_t *wscale, flo
         p.err = device_error_word();
         if (!p.err)
             return record(cudaErrorInvalidDevice);
-        return record(launch_stream_gemm(p, stream_rows_per_pass(g, 1), (cudaStream_t)stream));
+        return record(launch_streaming(p, (cudaStream_t)stream));
     }
     return run_grouped(p, workspace, workspace_bytes, (cudaStream_t)stream);
 }
@@ -277,7 +287,7 @@ double fp4_error_ops(int path, int recipe, int64_t k)
 {
     if (path == FP4_PATH_TC)
         return tc_error_ops(recipe, k);
-    return stream_error_ops(recipe, k);
+    return decode_fits(k) ? decode_error_ops(recipe, k) : stream_error_ops(recipe, k);
 }
 
 void fp4_force_path(int path)

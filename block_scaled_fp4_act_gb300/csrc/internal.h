@@ -44,8 +44,13 @@ cudaError_t launch_swiglu_quant(const float *gate, const float *up, int64_t ld, 
                                 int64_t rows, int64_t inter, float *h_out, uint8_t *codes,
                                 float *scales, cudaStream_t s);
 cudaError_t launch_stream_gemm(const GroupedProblem &p, int rows_per_pass, cudaStream_t s);
+// Decode kernel (warp-level MMA); rows_per_pass 4 or 8. decode_fits(k): its shared memory
+// holds 8 activation rows of length k.
+cudaError_t launch_decode_gemm(const GroupedProblem &p, int rows_per_pass, cudaStream_t s);
+bool decode_fits(int64_t k);
 
 // Error-model constants of each path (n_ops of |err| <= n_ops 2^-24 sum|p|).
 double stream_error_ops(int recipe, int64_t k);
+double decode_error_ops(int recipe, int64_t k);
 
 } // namespace fp4moe

@@ -168,6 +168,46 @@ def test_expert_gemm_shapes(recipe, g, n, k):
 
 
 @pytest.mark.parametrize("recipe", [fp4.NVFP4, fp4.MXFP4])
+@pytest.mark.parametrize("spreads", [(0, 15, 3, 0), (16, 0, 0, 0), (15, 15, 40, 7), (60, 0, 0, 0)])
+def test_expert_gemm_block_scale_spread(recipe, spreads):
+    """Rows whose 128-blocks have act scales 2^j far apart: within 2^15 of the row's
+    largest, the decode kernel takes f16 activations scaled by the row's largest block;
+    a wider spread in any row of the pass takes bf16 for the whole pass. Block amax is
+    448 * 2^j exactly, so the scale is 2^j, and every block keeps codes down to 2^-9."""
+    rng = np.random.default_rng(91 + recipe + sum(spreads))
+    g, n, k = len(spreads), 96, 2048
+    x = rng.uniform(-1.0, 1.0, (g, k)).astype(np.float32)
+    x[:, ::128] = 1.0                                            # amax exactly 448 * 2^j
+    x[:, 1::128] = 2.0 ** -9 / 448.0                             # the smallest e4m3 code
+    for r, spread in enumerate(spreads):
+        j = np.full(k // 128, -10.0 + rng.integers(-3, 4))     # above the 1e-4 amax floor
+        j[::2] += spread
+        x[r] *= np.repeat(448.0 * 2.0 ** j, 128).astype(np.float32)
+    w = rng.integers(0, 256, (n, k // 2), dtype=np.uint8)
+    if recipe == fp4.NVFP4:
+        sc = rng.integers(0x08, 0x7E, (n, k // 16), dtype=np.uint8)
+        s2 = 5.9945243e-5
+    else:
+        sc = rng.integers(100, 150, (n, k // 32), dtype=np.uint8)
+        s2 = 0.0
+    codes = torch.empty((g, k), dtype=torch.uint8, device=DEV)
+    scales = torch.empty((g, k // 128), device=DEV)
+    out = fp4.fp4_expert_gemm(_gpu(x), _gpu(w), _gpu(sc), s2, recipe, codes_out=codes,
+                              scales_out=scales)
+    c_ref, s_ref, ref, absp = expert_reference(x, w, sc, s2, recipe)
+    assert np.array_equal(to_np(codes), c_ref) and np.array_equal(to_np(scales), s_ref)
+    exps = np.log2(s_ref)
+    assert np.all(exps == np.round(exps))
+    assert [int(exps[r].max() - exps[r].min()) for r in range(g)] == list(spreads)
+    check_gemm(to_np(out), ref, absp, gemm_bound(fp4.PATH_STREAM, recipe, k), "spread")
+    # each row alone (its own pass, its own route) agrees with the oracle too
+    for r in range(g):
+        one = fp4.fp4_expert_gemm(_gpu(x[r:r + 1]), _gpu(w), _gpu(sc), s2, recipe)
+        check_gemm(to_np(one), ref[r:r + 1], absp[r:r + 1],
+                   gemm_bound(fp4.PATH_STREAM, recipe, k), "spread row %d" % r)
+
+
+@pytest.mark.parametrize("recipe", [fp4.NVFP4, fp4.MXFP4])
 def test_expert_gemm_exact_special_case(recipe, golden_dir):
     """P-EXACT: lossless quantisation, unit weight scales -> bit-equal to a float64 matmul."""
     from test_oracle_pins import _dense_weights, _exact_inputs, golden_e2m1
