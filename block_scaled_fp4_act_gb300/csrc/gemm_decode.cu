@@ -205,7 +205,9 @@ __device__ __forceinline__ uint32_t load_scales(const uint8_t *srow, int ch0, in
     return r;
 }
 
-template <int GS, bool F16>
+// FULL: k is a multiple of 256, so every batch has four chunks and the scale rows are
+// 16-byte aligned; no per-chunk checks.
+template <int GS, bool F16, bool FULL, int PR>
 __device__ __forceinline__ void decode_pass(const GroupedProblem &p, const uint16_t *act,
                                             const float *rowscale, const int *rowok, int64_t c0,
                                             int rows, const uint8_t *wexp, const uint8_t *sexp,
@@ -215,47 +217,64 @@ __device__ __forceinline__ void decode_pass(const GroupedProblem &p, const uint1
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     const int colA = blockIdx.x * kDecCols + warp * kDecRowsPerWarp + g, colB = colA + 8;
-    const bool okA = colA < n, okB = colB < n, bro_ok = g < rows;
-    const uint8_t *wA = wexp + (size_t)colA * (k / 2) + c * 8;
-    const uint8_t *wB = wexp + (size_t)colB * (k / 2) + c * 8;
-    const uint8_t *sA = sexp + (size_t)colA * (k / GS);
-    const uint8_t *sB = sexp + (size_t)colB * (k / GS);
-    const uint16_t *bro = act + (size_t)g * ld + 16 * c;  // activation row n = g
-    const bool vec = (k & 255) == 0;  // scale rows 16-byte aligned
+    // Rows past n read row n-1 and B columns past the pass read the last row the buffer
+    // holds: the loads need no predicate, and those outputs are never stored (an output
+    // depends only on its own A row and B column).
+    const int rA = min(colA, n - 1), rB = min(colB, n - 1);
+    const uint8_t *wA = wexp + (size_t)rA * (k / 2) + c * 8;
+    const uint8_t *wB = wexp + (size_t)rB * (k / 2) + c * 8;
+    const uint8_t *sA = sexp + (size_t)rA * (k / GS);
+    const uint8_t *sB = sexp + (size_t)rB * (k / GS);
+    const uint16_t *bro = act + (size_t)min(g, PR - 1) * ld + 16 * c;  // activation row n = g
     float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     const int nch = k / 64;
     for (int ch0 = 0; ch0 < nch; ch0 += kDecU) {
         uint2 wa[kDecU], wb[kDecU];
 #pragma unroll
         for (int u = 0; u < kDecU; ++u) {
-            const bool in = ch0 + u < nch;
-            wa[u] = (in && okA) ? __ldcs(reinterpret_cast<const uint2 *>(wA + (ch0 + u) * 32))
-                                : make_uint2(0u, 0u);
-            wb[u] = (in && okB) ? __ldcs(reinterpret_cast<const uint2 *>(wB + (ch0 + u) * 32))
-                                : make_uint2(0u, 0u);
+            const bool in = FULL || ch0 + u < nch;
+            wa[u] = in ? __ldcs(reinterpret_cast<const uint2 *>(wA + (ch0 + u) * 32))
+                       : make_uint2(0u, 0u);
+            wb[u] = in ? __ldcs(reinterpret_cast<const uint2 *>(wB + (ch0 + u) * 32))
+                       : make_uint2(0u, 0u);
         }
-        const uint32_t sa = okA ? load_scales<GS>(sA, ch0, nch, c, vec) : 0u;
-        const uint32_t sb = okB ? load_scales<GS>(sB, ch0, nch, c, vec) : 0u;
+        const uint32_t sa = load_scales<GS>(sA, ch0, nch, c, FULL);
+        const uint32_t sb = load_scales<GS>(sB, ch0, nch, c, FULL);
+        // NVFP4 f16 route: the four chunks' scales as f16, two per word
+        uint32_t sA01 = 0, sA23 = 0, sB01 = 0, sB23 = 0;
+        if (F16) {
+            sA01 = e4m3x2_to_f16x2(sa & 0xFFFFu);
+            sA23 = e4m3x2_to_f16x2(sa >> 16);
+            sB01 = e4m3x2_to_f16x2(sb & 0xFFFFu);
+            sB23 = e4m3x2_to_f16x2(sb >> 16);
+        }
 #pragma unroll
         for (int u = 0; u < kDecU; ++u) {
             const int ch = ch0 + u;
-            if (ch >= nch)
+            if (!FULL && ch >= nch)
                 break;
-            const uint32_t ba = (sa >> (8 * u)) & 0xFFu, bb = (sb >> (8 * u)) & 0xFFu;
             uint32_t hA[8], hB[8];
             e2m1x8_to_f16x8(wa[u].x, *reinterpret_cast<uint32_t(*)[4]>(&hA[0]));
             e2m1x8_to_f16x8(wa[u].y, *reinterpret_cast<uint32_t(*)[4]>(&hA[4]));
             e2m1x8_to_f16x8(wb[u].x, *reinterpret_cast<uint32_t(*)[4]>(&hB[0]));
             e2m1x8_to_f16x8(wb[u].y, *reinterpret_cast<uint32_t(*)[4]>(&hB[4]));
             if (F16) {
-                const uint32_t scA = e4m3x2_to_f16x2(ba | (ba << 8));
-                const uint32_t scB = e4m3x2_to_f16x2(bb | (bb << 8));
+                const uint32_t wA2 = (u < 2) ? sA01 : sA23, wB2 = (u < 2) ? sB01 : sB23;
+                const __half2 hA2 = *reinterpret_cast<const __half2 *>(&wA2);
+                const __half2 hB2 = *reinterpret_cast<const __half2 *>(&wB2);
+                const __half2 scA = (u & 1) ? __high2half2(hA2) : __low2half2(hA2);
+                const __half2 scB = (u & 1) ? __high2half2(hB2) : __low2half2(hB2);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    hA[j] = f16x2_mul(hA[j], scA);
-                    hB[j] = f16x2_mul(hB[j], scB);
+                    __half2 a2 = *reinterpret_cast<__half2 *>(&hA[j]);
+                    __half2 b2 = *reinterpret_cast<__half2 *>(&hB[j]);
+                    a2 = __hmul2(a2, scA);
+                    b2 = __hmul2(b2, scB);
+                    hA[j] = *reinterpret_cast<uint32_t *>(&a2);
+                    hB[j] = *reinterpret_cast<uint32_t *>(&b2);
                 }
             } else {
+                const uint32_t ba = (sa >> (8 * u)) & 0xFFu, bb = (sb >> (8 * u)) & 0xFFu;
                 const float fA = (GS == 16) ? e4m3_to_f32(ba) : e8m0_to_f32(ba);
                 const float fB = (GS == 16) ? e4m3_to_f32(bb) : e8m0_to_f32(bb);
 #pragma unroll
@@ -267,9 +286,7 @@ __device__ __forceinline__ void decode_pass(const GroupedProblem &p, const uint1
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 const uint32_t a[4] = {hA[2 * s], hB[2 * s], hA[2 * s + 1], hB[2 * s + 1]};
-                uint2 bv = make_uint2(0u, 0u);
-                if (bro_ok)
-                    bv = *reinterpret_cast<const uint2 *>(bro + ch * 64 + 4 * s);
+                const uint2 bv = *reinterpret_cast<const uint2 *>(bro + ch * 64 + 4 * s);
                 if (F16)
                     mma_f16_16816(d, a, bv.x, bv.y);
                 else
@@ -291,7 +308,7 @@ __device__ __forceinline__ void decode_pass(const GroupedProblem &p, const uint1
 
 // PR: most routed rows one pass holds (the MMA's N is 8; 4 halves the shared memory).
 template <int GS, int PR>
-__global__ void __launch_bounds__(kDecThreads) decode_mma_kernel(const GroupedProblem p)
+__global__ void __launch_bounds__(kDecThreads, 4) decode_mma_kernel(const GroupedProblem p)
 {
     extern __shared__ __align__(16) uint8_t smem_dec[];
     const int k = p.k, n = p.n, kq = k >> 7;
@@ -323,10 +340,18 @@ __global__ void __launch_bounds__(kDecThreads) decode_mma_kernel(const GroupedPr
     for (int64_t c0 = r0; c0 < r1; c0 += PR) {
         const int rows = (int)((r1 - c0) < PR ? (r1 - c0) : PR);
         decode_prologue(p, c0, rows, act, ascale, rowscale, rowok, route_f16, write_codes);
-        if (GS == 16 && *route_f16)
-            decode_pass<GS, true>(p, act, rowscale, rowok, c0, rows, wexp, sexp, s2);
-        else
-            decode_pass<GS, false>(p, act, rowscale, rowok, c0, rows, wexp, sexp, s2);
+        const bool full = (k & 255) == 0;
+        if (GS == 16 && *route_f16) {
+            if (full)
+                decode_pass<GS, true, true, PR>(p, act, rowscale, rowok, c0, rows, wexp, sexp, s2);
+            else
+                decode_pass<GS, true, false, PR>(p, act, rowscale, rowok, c0, rows, wexp, sexp, s2);
+        } else {
+            if (full)
+                decode_pass<GS, false, true, PR>(p, act, rowscale, rowok, c0, rows, wexp, sexp, s2);
+            else
+                decode_pass<GS, false, false, PR>(p, act, rowscale, rowok, c0, rows, wexp, sexp, s2);
+        }
         __syncthreads();  // act and the route flag are rewritten by the next pass
     }
 }
@@ -336,9 +361,11 @@ static size_t decode_smem_bytes(int pr, int64_t k)
     return (size_t)pr * (k + kDecRowPad) * 2 + (size_t)pr * (k / 128) * 4 + (size_t)pr * 8 + 16;
 }
 
+constexpr size_t kDecSmemLimit = 227 * 1024;
+
 bool decode_fits(int64_t k)
 {
-    return decode_smem_bytes(8, k) <= 227 * 1024;
+    return decode_smem_bytes(4, k) <= kDecSmemLimit;
 }
 
 template <int GS, int PR>
@@ -357,7 +384,7 @@ static cudaError_t launch_pr(const GroupedProblem &p, cudaStream_t s)
 cudaError_t launch_decode_gemm(const GroupedProblem &p, int rows_per_pass, cudaStream_t s)
 {
     const bool nv = p.recipe == FP4_NVFP4;
-    if (rows_per_pass <= 4)
+    if (rows_per_pass <= 4 || decode_smem_bytes(8, p.k) > kDecSmemLimit)
         return nv ? launch_pr<16, 4>(p, s) : launch_pr<32, 4>(p, s);
     return nv ? launch_pr<16, 8>(p, s) : launch_pr<32, 8>(p, s);
 }

@@ -100,13 +100,13 @@ def test_status_strings_and_error_model(lib):
     assert lib.fp4_status_string(123) == b"FP4_ERR_UNKNOWN"
     for recipe, gs in ((fp4.NVFP4, 16), (fp4.MXFP4, 32)):
         extra = 2 if recipe == fp4.NVFP4 else 0
-        for k in (128, 1536, 4096, 7168, 14208):
-            # up to k = 14208 the streaming path is the warp-MMA kernel: one f32 rounding
+        for k in (128, 1536, 4096, 7168, 28544):
+            # up to k = 28544 the streaming path is the warp-MMA kernel: one f32 rounding
             # per 16-product MMA step, as on the tcgen05 path
             n_ops = fp4.fp4_error_ops(fp4.PATH_STREAM, recipe, k)
             assert n_ops == k // 16 + extra + 1
             assert n_ops == fp4.fp4_error_ops(fp4.PATH_TC, recipe, k)
-        for k in (14336, 65536):
+        for k in (28672, 65536):
             # beyond it, the FMA streaming kernel: the order of the pages' own kernel,
             # (gs-1) + ceil(groups/128) + 7
             n_ops = fp4.fp4_error_ops(fp4.PATH_STREAM, recipe, k)

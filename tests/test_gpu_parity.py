@@ -148,10 +148,11 @@ def test_expert_gemm_configs(cfg):
 
 @pytest.mark.parametrize("recipe", [fp4.NVFP4, fp4.MXFP4])
 @pytest.mark.parametrize("g,n,k", [(1, 1, 128), (3, 200, 256), (5, 64, 1536), (9, 129, 512),
-                                   (2, 70, 7168), (17, 100, 384)])
+                                   (2, 70, 7168), (17, 100, 384), (3, 40, 28672)])
 def test_expert_gemm_shapes(recipe, g, n, k):
-    """Ragged n (not a multiple of the 64-column tile), short k (idle lanes), k that is
-    not a multiple of 1024, rows not a multiple of the rows per pass."""
+    """Ragged n (not a multiple of the tile), short k (idle lanes), k that is not a
+    multiple of 256 or 1024, rows not a multiple of the rows per pass, and a k too long
+    for the warp-MMA kernel's shared memory (the FMA streaming kernel takes it)."""
     rng = np.random.default_rng(g * 1000 + n + k + recipe)
     x = (rng.standard_normal((g, k)) * rng.choice([1e-3, 1, 100], (g, 1))).astype(np.float32)
     w = rng.integers(0, 256, (n, k // 2), dtype=np.uint8)
