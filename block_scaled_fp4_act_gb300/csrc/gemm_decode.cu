@@ -13,13 +13,17 @@
 //                    bf16(code * 2^m)                   otherwise (MXFP4 always)
 //   out = (D * 2^M_row) * scale2
 //
-// k order inside a 64-k chunk. Lane (g, c) = (lane / 4, lane % 4) loads bytes 8c..8c+7
-// of weight rows g and g+8, i.e. physical k 16c..16c+15 (one NVFP4 scale group). The
-// MMA's k index is a relabelling of physical k, applied identically to A and B (the terms
-// of a dot product can be taken in any order): in MMA step s (0..3) of the chunk,
-// fragment k {2c, 2c+1} is physical k 16c + 4s + {0, 1} and fragment k {2c+8, 2c+9} is
-// 16c + 4s + {2, 3}. A lane's A registers are then bytes 2s and 2s+1 of its own loads,
-// and its B registers one 8-byte shared-memory read of activation row g.
+// k order inside a 128-k block. Lane (g, c) = (lane / 4, lane % 4) loads bytes
+// 16c..16c+15 of the block's 64 bytes of weight rows g and g+8 (one 16-byte load each,
+// four lanes covering 64 contiguous bytes of a row), i.e. physical k 32c..32c+31: two
+// NVFP4 scale groups, one MXFP4 group. The MMA's k index is a relabelling of physical k,
+// applied identically to A and B (the terms of a dot product can be taken in any order):
+// in MMA step s (0..7) of the block, fragment k {2c, 2c+1} is physical k 32c + 4s + {0, 1}
+// and fragment k {2c+8, 2c+9} is 32c + 4s + {2, 3}. A lane's A registers are then bytes
+// 2s and 2s+1 of its own loads, and its B registers one 8-byte shared-memory read of
+// activation row g: the four elements at 32c + 4s, i.e. 4-element group q = 8c + s,
+// which the activation buffer stores at group q ^ ((q >> 4) & 1) so that the reads of a
+// half-warp fall in 32 distinct banks.
 //
 // Summation: one f32 accumulation per MMA (k/16 of them), then the row scale (exact) and
 // scale2, the same depth as the tcgen05 path.
@@ -33,8 +37,7 @@ constexpr int kDecThreads = 256;
 constexpr int kDecRowsPerWarp = 16;
 constexpr int kDecCols = (kDecThreads / 32) * kDecRowsPerWarp;  // 128 weight rows per CTA
 constexpr int kDecMaxScaleGap = 15;
-constexpr int kDecRowPad = 4;  // f16 elements after each activation row: conflict-free B reads
-constexpr int kDecU = 4;       // 64-k chunks whose loads are issued together
+constexpr int kDecRowPad = 8;  // f16 elements after each activation row: conflict-free B reads
 
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                               uint32_t b1)
@@ -76,8 +79,8 @@ __device__ __forceinline__ int f32_biased_exponent(float s)
 }
 
 // act_quant of the pass's rows (fn quant_rows of the page) into 16-bit MMA operands in
-// shared memory, row stride k + kDecRowPad. Rows >= `rows` are not written: lanes whose
-// B row is past the pass use zero registers instead.
+// shared memory, row stride k + kDecRowPad. Rows >= `rows` are not written: the MMA
+// columns they feed are never stored.
 __device__ __forceinline__ void decode_prologue(const GroupedProblem &p, int64_t c0, int rows,
                                                 uint16_t *act, float *ascale, float *rowscale,
                                                 int *rowok, int *route_f16, bool write_codes)
@@ -114,7 +117,8 @@ __device__ __forceinline__ void decode_prologue(const GroupedProblem &p, int64_t
         } else if (lane == 0 && g == 0) {
             raise_device_error(p.err, FP4_DEVERR_ROW_ID);
         }
-        *reinterpret_cast<uint2 *>(act + (size_t)r * ld + g * 128 + lane * 4) = h;
+        // 4-element group q of a 128-block is stored at q ^ ((q >> 4) & 1) (see decode_pass)
+        *reinterpret_cast<uint2 *>(act + (size_t)r * ld + g * 128 + 4 * (lane ^ ((lane >> 4) & 1))) = h;
         if (lane == 0) {
             ascale[r * kq + g] = s;
             if (g == 0)
@@ -168,45 +172,48 @@ __device__ __forceinline__ void decode_prologue(const GroupedProblem &p, int64_t
     __syncthreads();
 }
 
-// The scale bytes lane c needs for chunks ch0 .. ch0+kDecU-1 of one weight row, byte u =
-// chunk ch0+u (NVFP4: group 4ch + c; MXFP4: group 2ch + c/2).
-// The packing below takes exactly four chunks: 16 NVFP4 (8 MXFP4) scale bytes, one
-// aligned vector load.
-static_assert(kDecU == 4, "load_scales packs four chunks' scale bytes");
-
-template <int GS>
-__device__ __forceinline__ uint32_t load_scales(const uint8_t *srow, int ch0, int nch, int c,
-                                                bool vec)
+// The scale bytes of weight row `srow` lane c needs for k-batch b (256 k: blocks 2b and
+// 2b+1), packed as byte pairs: NVFP4 groups 16b + 2c, +1 (bits 0-15) and 16b + 8 + 2c, +1
+// (bits 16-31); MXFP4 group 8b + c (bits 0-7) and 8b + 4 + c (bits 8-15). h1: block 2b+1
+// exists. FULL: k % 256 == 0, so the batch's scale bytes are one aligned vector.
+template <int GS, bool FULL>
+__device__ __forceinline__ uint32_t batch_scales(const uint8_t *srow, int b, int c, bool h1)
 {
-    if (vec && ch0 + kDecU <= nch) {
-        if (GS == 16) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(srow + ch0 * 4);
-            const uint32_t sel = (uint32_t)c;
-            uint32_t lo, hi;
-            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(v.x), "r"(v.y), "r"(sel | ((sel + 4) << 4)));
-            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(v.z), "r"(v.w), "r"(sel | ((sel + 4) << 4)));
-            uint32_t r;
-            asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(r) : "r"(lo), "r"(hi));
-            return r;
+    uint32_t lo, hi;
+    if (GS == 16) {
+        uint2 v0, v1 = make_uint2(0u, 0u);
+        if (FULL) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(srow + b * 16);
+            v0 = make_uint2(v.x, v.y);
+            v1 = make_uint2(v.z, v.w);
         } else {
-            const uint2 v = *reinterpret_cast<const uint2 *>(srow + ch0 * 2);
-            const uint32_t b = (uint32_t)(c >> 1);
-            uint32_t r;
-            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r)
-                : "r"(v.x), "r"(v.y), "r"(b | ((b + 2) << 4) | ((b + 4) << 8) | ((b + 6) << 12)));
-            return r;
+            v0 = *reinterpret_cast<const uint2 *>(srow + b * 16);
+            if (h1)
+                v1 = *reinterpret_cast<const uint2 *>(srow + b * 16 + 8);
         }
+        lo = (c >> 1) ? v0.y : v0.x;
+        hi = (c >> 1) ? v1.y : v1.x;
+        const uint32_t o = 2u * (uint32_t)(c & 1);
+        uint32_t r;
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r)
+            : "r"(lo), "r"(hi), "r"(o | ((o + 1) << 4) | ((o + 4) << 8) | ((o + 5) << 12)));
+        return r;
+    } else {
+        if (FULL) {
+            const uint2 v = *reinterpret_cast<const uint2 *>(srow + b * 8);
+            lo = v.x;
+            hi = v.y;
+        } else {
+            lo = *reinterpret_cast<const uint32_t *>(srow + b * 8);
+            hi = h1 ? *reinterpret_cast<const uint32_t *>(srow + b * 8 + 4) : 0u;
+        }
+        uint32_t r;
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(lo), "r"(hi), "r"(c | ((c + 4) << 4)));
+        return r & 0xFFFFu;
     }
-    uint32_t r = 0;
-#pragma unroll
-    for (int u = 0; u < kDecU; ++u)
-        if (ch0 + u < nch)
-            r |= (uint32_t)srow[GS == 16 ? (ch0 + u) * 4 + c : (ch0 + u) * 2 + (c >> 1)] << (8 * u);
-    return r;
 }
 
-// FULL: k is a multiple of 256, so every batch has four chunks and the scale rows are
-// 16-byte aligned; no per-chunk checks.
+// FULL: k is a multiple of 256, so every batch has both 128-k blocks; no per-block checks.
 template <int GS, bool F16, bool FULL, int PR>
 __device__ __forceinline__ void decode_pass(const GroupedProblem &p, const uint16_t *act,
                                             const float *rowscale, const int *rowok, int64_t c0,
@@ -215,82 +222,85 @@ __device__ __forceinline__ void decode_pass(const GroupedProblem &p, const uint1
 {
     const int k = p.k, n = p.n, ld = k + kDecRowPad;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, c = lane & 3;
+    const int g = lane >> 2, c = lane & 3, swz = c >> 1;
     const int colA = blockIdx.x * kDecCols + warp * kDecRowsPerWarp + g, colB = colA + 8;
     // Rows past n read row n-1 and B columns past the pass read the last row the buffer
     // holds: the loads need no predicate, and those outputs are never stored (an output
     // depends only on its own A row and B column).
     const int rA = min(colA, n - 1), rB = min(colB, n - 1);
-    const uint8_t *wA = wexp + (size_t)rA * (k / 2) + c * 8;
-    const uint8_t *wB = wexp + (size_t)rB * (k / 2) + c * 8;
+    const uint8_t *wA = wexp + (size_t)rA * (k / 2) + c * 16;
+    const uint8_t *wB = wexp + (size_t)rB * (k / 2) + c * 16;
     const uint8_t *sA = sexp + (size_t)rA * (k / GS);
     const uint8_t *sB = sexp + (size_t)rB * (k / GS);
-    const uint16_t *bro = act + (size_t)min(g, PR - 1) * ld + 16 * c;  // activation row n = g
+    // activation row n = g; step 2w + t reads group 8c + (2w + (t ^ swz)) of its block
+    const uint16_t *bro = act + (size_t)min(g, PR - 1) * ld + 32 * c;
+    const uint16_t *bro_t[2] = {bro + 4 * swz, bro + 4 * (swz ^ 1)};
     float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    const int nch = k / 64;
-    for (int ch0 = 0; ch0 < nch; ch0 += kDecU) {
-        uint2 wa[kDecU], wb[kDecU];
+    const int nblk = k / 128, nb = (nblk + 1) / 2;
+    for (int b = 0; b < nb; ++b) {
+        const bool h1 = FULL || 2 * b + 1 < nblk;
+        uint4 wa[2], wb[2];
+        wa[0] = __ldcs(reinterpret_cast<const uint4 *>(wA + b * 128));
+        wb[0] = __ldcs(reinterpret_cast<const uint4 *>(wB + b * 128));
+        wa[1] = h1 ? __ldcs(reinterpret_cast<const uint4 *>(wA + b * 128 + 64)) : make_uint4(0, 0, 0, 0);
+        wb[1] = h1 ? __ldcs(reinterpret_cast<const uint4 *>(wB + b * 128 + 64)) : make_uint4(0, 0, 0, 0);
+        const uint32_t sa = batch_scales<GS, FULL>(sA, b, c, h1);
+        const uint32_t sb = batch_scales<GS, FULL>(sB, b, c, h1);
 #pragma unroll
-        for (int u = 0; u < kDecU; ++u) {
-            const bool in = FULL || ch0 + u < nch;
-            wa[u] = in ? __ldcs(reinterpret_cast<const uint2 *>(wA + (ch0 + u) * 32))
-                       : make_uint2(0u, 0u);
-            wb[u] = in ? __ldcs(reinterpret_cast<const uint2 *>(wB + (ch0 + u) * 32))
-                       : make_uint2(0u, 0u);
-        }
-        const uint32_t sa = load_scales<GS>(sA, ch0, nch, c, FULL);
-        const uint32_t sb = load_scales<GS>(sB, ch0, nch, c, FULL);
-        // NVFP4 f16 route: the four chunks' scales as f16, two per word
-        uint32_t sA01 = 0, sA23 = 0, sB01 = 0, sB23 = 0;
-        if (F16) {
-            sA01 = e4m3x2_to_f16x2(sa & 0xFFFFu);
-            sA23 = e4m3x2_to_f16x2(sa >> 16);
-            sB01 = e4m3x2_to_f16x2(sb & 0xFFFFu);
-            sB23 = e4m3x2_to_f16x2(sb >> 16);
-        }
-#pragma unroll
-        for (int u = 0; u < kDecU; ++u) {
-            const int ch = ch0 + u;
-            if (!FULL && ch >= nch)
+        for (int h = 0; h < 2; ++h) {
+            if (!FULL && h == 1 && !h1)
                 break;
-            uint32_t hA[8], hB[8];
-            e2m1x8_to_f16x8(wa[u].x, *reinterpret_cast<uint32_t(*)[4]>(&hA[0]));
-            e2m1x8_to_f16x8(wa[u].y, *reinterpret_cast<uint32_t(*)[4]>(&hA[4]));
-            e2m1x8_to_f16x8(wb[u].x, *reinterpret_cast<uint32_t(*)[4]>(&hB[0]));
-            e2m1x8_to_f16x8(wb[u].y, *reinterpret_cast<uint32_t(*)[4]>(&hB[4]));
+            const int blk = 2 * b + h;
+            const uint32_t va[4] = {wa[h].x, wa[h].y, wa[h].z, wa[h].w};
+            const uint32_t vb[4] = {wb[h].x, wb[h].y, wb[h].z, wb[h].w};
+            __half2 scA_lo, scA_hi, scB_lo, scB_hi;  // f16 route: groups 2c and 2c+1
+            float fA_lo = 0.0f, fA_hi = 0.0f, fB_lo = 0.0f, fB_hi = 0.0f;
             if (F16) {
-                const uint32_t wA2 = (u < 2) ? sA01 : sA23, wB2 = (u < 2) ? sB01 : sB23;
-                const __half2 hA2 = *reinterpret_cast<const __half2 *>(&wA2);
-                const __half2 hB2 = *reinterpret_cast<const __half2 *>(&wB2);
-                const __half2 scA = (u & 1) ? __high2half2(hA2) : __low2half2(hA2);
-                const __half2 scB = (u & 1) ? __high2half2(hB2) : __low2half2(hB2);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    __half2 a2 = *reinterpret_cast<__half2 *>(&hA[j]);
-                    __half2 b2 = *reinterpret_cast<__half2 *>(&hB[j]);
-                    a2 = __hmul2(a2, scA);
-                    b2 = __hmul2(b2, scB);
-                    hA[j] = *reinterpret_cast<uint32_t *>(&a2);
-                    hB[j] = *reinterpret_cast<uint32_t *>(&b2);
-                }
+                const uint32_t pa = e4m3x2_to_f16x2((sa >> (16 * h)) & 0xFFFFu);
+                const uint32_t pb = e4m3x2_to_f16x2((sb >> (16 * h)) & 0xFFFFu);
+                const __half2 ha = *reinterpret_cast<const __half2 *>(&pa);
+                const __half2 hb = *reinterpret_cast<const __half2 *>(&pb);
+                scA_lo = __low2half2(ha);
+                scA_hi = __high2half2(ha);
+                scB_lo = __low2half2(hb);
+                scB_hi = __high2half2(hb);
+            } else if (GS == 16) {
+                fA_lo = e4m3_to_f32((sa >> (16 * h)) & 0xFFu);
+                fA_hi = e4m3_to_f32((sa >> (16 * h + 8)) & 0xFFu);
+                fB_lo = e4m3_to_f32((sb >> (16 * h)) & 0xFFu);
+                fB_hi = e4m3_to_f32((sb >> (16 * h + 8)) & 0xFFu);
             } else {
-                const uint32_t ba = (sa >> (8 * u)) & 0xFFu, bb = (sb >> (8 * u)) & 0xFFu;
-                const float fA = (GS == 16) ? e4m3_to_f32(ba) : e8m0_to_f32(ba);
-                const float fB = (GS == 16) ? e4m3_to_f32(bb) : e8m0_to_f32(bb);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    hA[j] = f16x2_scaled_bf16(hA[j], fA);
-                    hB[j] = f16x2_scaled_bf16(hB[j], fB);
-                }
+                fA_lo = fA_hi = e8m0_to_f32((sa >> (8 * h)) & 0xFFu);
+                fB_lo = fB_hi = e8m0_to_f32((sb >> (8 * h)) & 0xFFu);
             }
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint32_t a[4] = {hA[2 * s], hB[2 * s], hA[2 * s + 1], hB[2 * s + 1]};
-                const uint2 bv = *reinterpret_cast<const uint2 *>(bro + ch * 64 + 4 * s);
-                if (F16)
-                    mma_f16_16816(d, a, bv.x, bv.y);
-                else
-                    mma_bf16_16816(d, a, bv.x, bv.y);
+            for (int w = 0; w < 4; ++w) {
+                uint32_t hA[4], hB[4];
+                e2m1x8_to_f16x8(va[w], hA);
+                e2m1x8_to_f16x8(vb[w], hB);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (F16) {
+                        __half2 a2 = *reinterpret_cast<__half2 *>(&hA[j]);
+                        __half2 b2 = *reinterpret_cast<__half2 *>(&hB[j]);
+                        a2 = __hmul2(a2, w < 2 ? scA_lo : scA_hi);
+                        b2 = __hmul2(b2, w < 2 ? scB_lo : scB_hi);
+                        hA[j] = *reinterpret_cast<uint32_t *>(&a2);
+                        hB[j] = *reinterpret_cast<uint32_t *>(&b2);
+                    } else {
+                        hA[j] = f16x2_scaled_bf16(hA[j], w < 2 ? fA_lo : fA_hi);
+                        hB[j] = f16x2_scaled_bf16(hB[j], w < 2 ? fB_lo : fB_hi);
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const uint32_t a[4] = {hA[2 * t], hB[2 * t], hA[2 * t + 1], hB[2 * t + 1]};
+                    const uint2 bv = *reinterpret_cast<const uint2 *>(bro_t[t] + blk * 128 + 8 * w);
+                    if (F16)
+                        mma_f16_16816(d, a, bv.x, bv.y);
+                    else
+                        mma_bf16_16816(d, a, bv.x, bv.y);
+                }
             }
         }
     }
