@@ -73,23 +73,14 @@ static int choose_path(int64_t P, int E, int64_t n, int64_t k, int recipe, bool 
     return FP4_PATH_STREAM;
 }
 
-// Most rows one streaming pass takes: passes are specialised for 1..4 rows, so an
-// expert's rows cost only their own arithmetic, and up to 4 rows share one weight read.
-static int stream_rows_per_pass(int64_t P, int E)
-{
-    (void)P;
-    (void)E;
-    return 4;
-}
-
-// The path that needs no workspace: the warp-MMA decode kernel wherever 8 activation rows
-// of length k fit in shared memory (8 rows per pass once experts average more than 4),
-// the FMA streaming kernel beyond that.
+// The path that needs no workspace: the warp-MMA decode kernel wherever 4 activation rows
+// of length k fit in its shared memory (k <= 28544; 8 rows per pass where they fit and
+// experts average more than 4), the FMA streaming kernel (1-2 rows per pass) beyond.
 static cudaError_t launch_streaming(const GroupedProblem &p, cudaStream_t s)
 {
     if (decode_fits(p.k))
         return launch_decode_gemm(p, p.P > 4 * (int64_t)p.E ? 8 : 4, s);
-    return launch_stream_gemm(p, stream_rows_per_pass(p.P, p.E), s);
+    return launch_stream_gemm(p, 2, s);
 }
 
 // Shared shape checks; returns FP4_OK or the status to report.

@@ -57,13 +57,6 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b)
-{
-    uint32_t r;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
 // f16x2 of two E2M1 values times an f32 scale -> bf16x2, exactly (<= 6 significant bits).
 __device__ __forceinline__ uint32_t f16x2_scaled_bf16(uint32_t h, float s)
 {

@@ -1,8 +1,8 @@
 // gemm_stream.cu -- weight-streaming grouped expert GEMM on CUDA cores, act_quant fused.
 //
-// For decode-sized row counts the projection is bound by HBM reads of the nibble
-// weights (0.5 B per weight plus 1/16 or 1/32 B of scale); each weight is used by only
-// a few activation rows, so the tensor cores would idle. This kernel streams every
+// The no-workspace path for k too long for the warp-MMA decode kernel's shared memory
+// (four activation rows of k > 28544). Like that kernel it is bound by HBM reads of the
+// nibble weights (0.5 B per weight plus 1/16 or 1/32 B of scale). It streams every
 // touched expert's weights once with 128-bit loads and keeps the arithmetic on CUDA
 // cores in the order the pages define (fn mirror_gemm / fn f64_ref of memra-engine
 // 0.98.0, src/bin/dsv4_native_gemm_gate.rs):
@@ -16,10 +16,10 @@
 // 8 weight rows; lane l reads k in chunks [32 l + 1024 i, +32): 16 B of nibbles per
 // weight row per chunk, so a warp reads 512 contiguous bytes of each row per step.
 // Activation rows of the expert are quantised by the CTA in a prologue (fused
-// act_quant), up to 4 rows a pass, into shared memory as exact f16 code values plus the
-// per-128 f32 scales; the weights of the CTA are re-read (from L2) once per pass. Each
-// pass runs code specialised for its row count (1..4): at decode most experts hold one
-// or two routed rows, and a fixed pass size would spend arithmetic on empty rows.
+// act_quant), up to 2 rows a pass (what shared memory holds at these k), into shared
+// memory as exact f16 code values plus the per-128 f32 scales; the weights of the CTA are
+// re-read (from L2) once per pass. Each pass runs code specialised for its row count, so
+// an expert with one routed row does one row's arithmetic.
 #include "common.cuh"
 
 #include <algorithm>
@@ -100,9 +100,7 @@ __device__ __forceinline__ void load_chunk(const uint8_t *wexp, const uint8_t *s
 }
 
 // One pass over the CTA's weight rows for RB quantised activation rows in shared memory.
-// PF: load chunk i + 1 of the weights while chunk i is being multiplied (two register
-// buffers; only where the RB-row accumulators leave room for them).
-template <int RB, int GS, bool PF>
+template <int RB, int GS>
 __device__ __forceinline__ void stream_pass(const GroupedProblem &p, const __half *act,
                                             const float *ascale, const int *rowok, int64_t c0,
                                             int rows, const uint8_t *wexp, const uint8_t *sexp,
@@ -119,24 +117,10 @@ __device__ __forceinline__ void stream_pass(const GroupedProblem &p, const __hal
         for (int r = 0; r < RB; ++r)
             acc[i][r] = 0.0f;
 
-    uint4 nwv[kRowsPerWarp];
-    uint32_t nsb[kRowsPerWarp];
-    if (PF && lane * 32 < k)
-        load_chunk<GS>(wexp, sexp, wrow, srow, col_base, n, lane * 32, nwv, nsb);
     for (int kb = lane * 32; kb < k; kb += 1024) {
         uint4 wv[kRowsPerWarp];
         uint32_t sb[kRowsPerWarp];
-        if (PF) {
-#pragma unroll
-            for (int i = 0; i < kRowsPerWarp; ++i) {
-                wv[i] = nwv[i];
-                sb[i] = nsb[i];
-            }
-            if (kb + 1024 < k)
-                load_chunk<GS>(wexp, sexp, wrow, srow, col_base, n, kb + 1024, nwv, nsb);
-        } else {
-            load_chunk<GS>(wexp, sexp, wrow, srow, col_base, n, kb, wv, sb);
-        }
+        load_chunk<GS>(wexp, sexp, wrow, srow, col_base, n, kb, wv, sb);
         float asv[RB];
 #pragma unroll
         for (int r = 0; r < RB; ++r)
@@ -206,7 +190,7 @@ __device__ __forceinline__ void stream_rows(const GroupedProblem &p, __half *act
     __syncthreads();
     quantize_chunk<RB>(p, c0, RB, act, ascale, rowok, write_codes);
     __syncthreads();
-    stream_pass<RB, GS, false>(p, act, ascale, rowok, c0, RB, wexp, sexp, col_base, s2);
+    stream_pass<RB, GS>(p, act, ascale, rowok, c0, RB, wexp, sexp, col_base, s2);
 }
 
 // RBMAX: most activation rows the shared-memory buffer holds (by k). Each pass takes
@@ -247,15 +231,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_gemm_kernel(const Gr
 
     for (int64_t c0 = r0; c0 < r1;) {
         const int left = (int)((r1 - c0) < RBMAX ? (r1 - c0) : RBMAX);
-        if (RBMAX >= 4 && left >= 4) {
-            stream_rows<(RBMAX >= 4 ? 4 : 1), GS>(p, act, ascale, rowok, c0, wexp, sexp, col_base,
-                                                   s2, write_codes);
-            c0 += 4;
-        } else if (RBMAX >= 3 && left == 3) {
-            stream_rows<(RBMAX >= 3 ? 3 : 1), GS>(p, act, ascale, rowok, c0, wexp, sexp, col_base,
-                                                   s2, write_codes);
-            c0 += 3;
-        } else if (RBMAX >= 2 && left == 2) {
+        if (RBMAX >= 2 && left == 2) {
             stream_rows<(RBMAX >= 2 ? 2 : 1), GS>(p, act, ascale, rowok, c0, wexp, sexp, col_base,
                                                    s2, write_codes);
             c0 += 2;
@@ -290,7 +266,7 @@ static cudaError_t launch_rb(const GroupedProblem &p, cudaStream_t s)
 int stream_max_rows_per_pass(int k)
 {
     const size_t limit = 227 * 1024;
-    for (int rb : {4, 2, 1})
+    for (int rb : {2, 1})
         if (stream_smem_bytes(rb, k) <= limit)
             return rb;
     return 0;
@@ -301,7 +277,6 @@ cudaError_t launch_stream_gemm(const GroupedProblem &p, int rows_per_pass, cudaS
     const int rb = std::min(rows_per_pass, stream_max_rows_per_pass(p.k));
     const bool nv = p.recipe == FP4_NVFP4;
     switch (rb) {
-    case 4: return nv ? launch_rb<4, 16>(p, s) : launch_rb<4, 32>(p, s);
     case 2: return nv ? launch_rb<2, 16>(p, s) : launch_rb<2, 32>(p, s);
     case 1: return nv ? launch_rb<1, 16>(p, s) : launch_rb<1, 32>(p, s);
     default: return cudaErrorInvalidValue;

@@ -44,8 +44,8 @@ cudaError_t launch_swiglu_quant(const float *gate, const float *up, int64_t ld, 
                                 int64_t rows, int64_t inter, float *h_out, uint8_t *codes,
                                 float *scales, cudaStream_t s);
 cudaError_t launch_stream_gemm(const GroupedProblem &p, int rows_per_pass, cudaStream_t s);
-// Decode kernel (warp-level MMA); rows_per_pass 4 or 8. decode_fits(k): its shared memory
-// holds 8 activation rows of length k.
+// Decode kernel (warp-level MMA); rows_per_pass 4 or 8 (8 only where they fit).
+// decode_fits(k): its shared memory holds 4 activation rows of length k (k <= 28544).
 cudaError_t launch_decode_gemm(const GroupedProblem &p, int rows_per_pass, cudaStream_t s);
 bool decode_fits(int64_t k);
 
