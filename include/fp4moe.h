@@ -55,7 +55,8 @@ enum {
 /* Kernel paths (fp4_gemm_path / fp4_force_path). */
 enum {
     FP4_PATH_AUTO = 0,   /* library choice by shape (fp4_gemm_path) */
-    FP4_PATH_STREAM = 1, /* CUDA-core weight-streaming kernel with fused act-quant prologue */
+    FP4_PATH_STREAM = 1, /* no-workspace weight streaming with a fused act-quant prologue:
+                            warp-level MMA (mma.sync) for k <= 28544, CUDA-core FMA above */
     FP4_PATH_TC = 2      /* tcgen05 tensor-core kernel over a quantized-activation workspace */
 };
 
@@ -180,7 +181,9 @@ int fp4_gemm_path(int64_t total_rows, int num_experts, int64_t n, int64_t k, int
 /*
  * The n_ops of the per-output error model |out - f64 reference| <= n_ops * 2^-24 *
  * sum|scaled products| (dsv4_native_gemm_gate.rs, header comment and the f64 check)
- * for `path` at this recipe and k. Derived from the kernel's summation structure.
+ * for `path` at this recipe and k. Derived from the kernel's summation structure:
+ * FP4_PATH_TC k/16 + 1 (+2 NVFP4); FP4_PATH_STREAM the same for k <= 28544 (the MMA
+ * kernel), (gs-1) + 2*ceil(k/1024) (NVFP4; MXFP4 ceil(k/1024)) + 5 above (the FMA kernel).
  */
 double fp4_error_ops(int path, int recipe, int64_t k);
 
