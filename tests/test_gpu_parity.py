@@ -309,6 +309,34 @@ def test_grouped_decode_c3_full_size(scale2):
     del rng
 
 
+@pytest.mark.parametrize("variant", ["mxfp4", "nvfp4_wide_spread"])
+def test_grouped_decode_shapes_full_size_variants(variant):
+    """The decode workload's shapes (64 experts, 8 tokens top-8, gate/up [3072, 4096] and
+    down [4096, 1536]) with an MXFP4 bank, and with NVFP4 activations whose 128-blocks
+    alternate between x 2^8 and x 2^-10 (block scales about 2^18 apart, past the f16
+    route's 2^15): both take the bf16 operands of the no-workspace kernel. Every routed
+    row, every column."""
+    wl = synth.decode_c3(device=DEV)
+    for proj in wl.projections:
+        bank, x = proj.bank, proj.x
+        if variant == "mxfp4":
+            bank = synth.make_bank(fp4.MXFP4, bank.E, bank.n, bank.k, 1203, DEV)
+        else:
+            blocks = torch.arange(x.shape[1] // 128, device=DEV)
+            f = torch.where(blocks % 2 == 0, 2.0 ** 8, 2.0 ** -10).repeat_interleave(128)
+            x = (x * f).contiguous()
+        proj = synth.Projection(proj.name, x, proj.routing, bank, row_ids_used=proj.row_ids_used)
+        if variant != "mxfp4":
+            _, scales = oracle.act_quant(to_np(x[:4]))
+            e = np.log2(scales)
+            assert np.all(e.max(axis=1) - e.min(axis=1) > 15)
+        out, path = run_projection(proj)
+        assert path == fp4.PATH_STREAM
+        grouped_sampled_check(proj, out, path, np.arange(proj.routing.P),
+                              "c3 %s %s" % (variant, proj.name))
+    assert fp4.fp4_get_device_error() == 0
+
+
 @pytest.mark.parametrize("name", ["c4", "c5"])
 def test_grouped_prefill_full_size_sampled(name):
     wl = synth.workload(name, device=DEV)
