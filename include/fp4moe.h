@@ -174,7 +174,9 @@ int fp4_gemm_mirror(const uint8_t *codes, const float *scales, const uint8_t *w,
 int fp4_swiglu_quant(const float *gate, const float *up, int64_t ld, float limit, int64_t rows,
                      int64_t inter, float *h_out, uint8_t *codes, float *scales, void *stream);
 
-/* Which path a grouped call of this shape takes (never FP4_PATH_AUTO). */
+/* Which path a grouped call of this shape takes (never FP4_PATH_AUTO): the tensor-core
+ * path when a workspace is given, the shape is one it supports and the routed rows
+ * average at least 8 per expert; the no-workspace path otherwise. */
 int fp4_gemm_path(int64_t total_rows, int num_experts, int64_t n, int64_t k, int recipe,
                   int have_workspace);
 
