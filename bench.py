@@ -56,6 +56,9 @@ def parse_args():
     ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count")
     ap.add_argument("--path", choices=["auto", "stream", "tc"], default="auto",
                     help="force a kernel path (default: the library's choice by shape)")
+    ap.add_argument("--path-sweep", action="store_true",
+                    help="instead of the benchmark: time both grouped paths by routed rows per "
+                         "expert (the measurement behind the library's path threshold)")
     return ap.parse_args()
 
 
@@ -654,8 +657,59 @@ def measure_swiglu(fp4, device, peaks, peak_src, rows=32768, inter=1024, limit=7
             "gpu_launches": iters}
 
 
+def path_sweep(rows_per_expert=(2, 4, 8, 16, 24, 32, 48, 64), E=64, n=3072, k=4096, iters=20):
+    """Both grouped paths (no-workspace and tensor-core) on 64 NVFP4 experts [3072, 4096]
+    with exactly r routed rows per expert, L2 flushed before each call; median microseconds.
+    One JSON line per r."""
+    import torch
+    import block_scaled_fp4_act_gb300 as fp4
+    from block_scaled_fp4_act_gb300 import synth
+    dev = "cuda"
+    bank = synth.make_bank(fp4.NVFP4, E, n, k, 77, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for rpe in rows_per_expert:
+        T = rpe * E // 8
+        # each token picks 8 distinct experts; round-robin blocks give exactly rpe per expert
+        choices = torch.stack([torch.arange(8) + 8 * (t % (E // 8)) for t in range(T)])
+        r = synth.routing_from_choices(choices, E)
+        gen = torch.Generator(device="cpu").manual_seed(rpe)
+        x = torch.randn(T, k, generator=gen).to(dev)
+        rid, off = r.row_ids.to(dev), r.offsets.to(dev)
+        ws = fp4.workspace_for(T, r.P, n, k, fp4.NVFP4, device=dev)
+        us = {}
+        for name, path in (("no_workspace", fp4.PATH_STREAM), ("tensor_core", fp4.PATH_TC)):
+            fp4.fp4_force_path(path)
+            try:
+                def call():
+                    fp4.fp4_grouped_expert_gemm(x, rid, off, bank.w, bank.sc, bank.scale2,
+                                                fp4.NVFP4, workspace=ws)
+                for _ in range(3):
+                    call()
+                ts = []
+                for _ in range(iters):
+                    flush.fill_(1)
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    call()
+                    e1.record()
+                    torch.cuda.synchronize()
+                    ts.append(e0.elapsed_time(e1) * 1000.0)
+            finally:
+                fp4.fp4_force_path(fp4.PATH_AUTO)
+            ts.sort()
+            us[name] = round(ts[len(ts) // 2], 1)
+        auto = fp4.fp4_gemm_path(r.P, E, n, k, fp4.NVFP4, True)
+        print(json.dumps({"rows_per_expert": rpe, "routed_rows": r.P, "us": us,
+                          "auto_path": "tensor_core" if auto == fp4.PATH_TC else "no_workspace"}),
+              flush=True)
+
+
 def main():
     args = parse_args()
+    if args.path_sweep:
+        path_sweep()
+        return
     if args.impl == "reference":
         # the oracle arm runs on rank 0 only; other ranks exit without work
         world = int(os.environ.get("WORLD_SIZE", "1"))
