@@ -61,10 +61,11 @@ static bool recipe_ok(int r)
 }
 
 // Rows per expert (on average) at or above which the tensor-core path, workspace pass
-// included, is faster than the warp-MMA decode kernel. Measured on GB300 (64 NVFP4 experts,
-// [3072, 4096], L2 flushed): decode 138 / 234 / 437 us at 4 / 8 / 16 rows per expert,
-// tensor cores 225 / 225 / 227 us. The decode kernel re-converts the weights once per
-// pass of up to 8 rows; the tensor-core kernel once per 192-row tile.
+// included, is faster than the warp-MMA decode kernel. Measured on GB300 (bench.py
+// --path-sweep: 64 NVFP4 experts, [3072, 4096], L2 flushed): decode 140 / 230 / 433 us at
+// 4 / 8 / 16 rows per expert, tensor cores 225 / 225 / 227 us. The decode kernel
+// re-converts the weights once per pass of up to 8 rows; the tensor-core kernel once per
+// 192-row tile.
 constexpr int64_t kTcMinRowsPerExpert = 8;
 
 static int choose_path(int64_t P, int E, int64_t n, int64_t k, int recipe, bool have_ws)
