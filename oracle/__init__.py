@@ -12,6 +12,10 @@ Functions and the page passages they follow (memra-engine docs.rs source pages):
   e4m3_decode         0.71.0 src/bin/kernel_check.rs, F8-E4M3 MMVQ section's decoder
   mirror_gemm         same page, fn mirror_gemm: the page's own kernel order in f32
                       (128 strided partials per output + a fixed halving tree)
+  route_topk          0.125.0 src/bin/qwen4exp_gpu_gate.rs, the device-router arm (softmax
+                      top-k; body not printed: the reading is stated in oracle.c)
+  route_csr           0.71.0 kernel_check.rs, grouped MoE GEMM section (CSR offsets)
+  moe_combine         same section (per-routed-row factor on the output), summed per token
   swiglu              0.98.0 dsv4_native_gemm_gate.rs, swiglu_limit saturation cell and
                       the f64 check of main: h = min(g,L) * sigmoid(min(g,L)) * clamp(u,-L,L)
   within_bound        the error model stated in the header comment of
@@ -63,6 +67,12 @@ def _load():
         lib.orc_grouped_ref_sampled.argtypes = [P, i64, i64, P, P, i32, i64, P, P, P, i32, i64,
                                                 P, P, i64, P, P, P, P]
         lib.orc_grouped_ref_sampled.restype = i32
+        lib.orc_route_topk.argtypes = [P, i64, i32, i32, i32, P, P]
+        lib.orc_route_topk.restype = None
+        lib.orc_route_csr.argtypes = [P, i64, i32, i32, P, P, P]
+        lib.orc_route_csr.restype = i32
+        lib.orc_moe_combine.argtypes = [P, P, P, i64, i32, i64, P, P]
+        lib.orc_moe_combine.restype = None
         _lib = lib
     return _lib
 
@@ -228,6 +238,50 @@ def grouped_ref_sampled(x, row_ids, offsets, w, sc, scale2, recipe, sample_p, sa
     return out, absp
 
 
+# --------------------------------------------------------------------------- routing front-end
+
+def route_topk(logits, topk, renormalize=False):
+    """logits f32 [T, E] -> (ids int32 [T, topk], weights f64 [T, topk]): the topk largest
+    logits per token (ties: lower expert id first), best first; softmax weights over all
+    experts, or over the selected ones with renormalize."""
+    logits = _c(logits, np.float32)
+    T, E = logits.shape
+    ids = np.empty((T, topk), dtype=np.int32)
+    w = np.empty((T, topk), dtype=np.float64)
+    _load().orc_route_topk(_ptr(logits), T, E, topk, 1 if renormalize else 0, _ptr(ids), _ptr(w))
+    return ids, w
+
+
+def route_csr(ids, num_experts):
+    """ids int32 [T, topk] -> (offsets int32 [E+1], row_ids int32 [T*topk], pair_rows int32
+    [T, topk]): routed rows grouped by expert, token order within an expert."""
+    ids = _c(ids, np.int32)
+    T, topk = ids.shape
+    offsets = np.empty(num_experts + 1, dtype=np.int32)
+    row_ids = np.empty(T * topk, dtype=np.int32)
+    pair_rows = np.empty((T, topk), dtype=np.int32)
+    rc = _load().orc_route_csr(_ptr(ids), T, topk, num_experts, _ptr(offsets), _ptr(row_ids),
+                               _ptr(pair_rows))
+    if rc != 0:
+        raise ValueError("oracle: expert id outside [0, num_experts)")
+    return offsets, row_ids, pair_rows
+
+
+def moe_combine(out, pair_rows, weights):
+    """out f32 [P, n], pair_rows int32 [T, topk], weights f32 [T, topk] -> (y f64 [T, n],
+    absy f64 [T, n]): y[t] = sum_j weights[t, j] * out[pair_rows[t, j]]."""
+    out = _c(out, np.float32)
+    pair_rows = _c(pair_rows, np.int32)
+    weights = _c(weights, np.float32)
+    T, topk = pair_rows.shape
+    n = out.shape[1]
+    y = np.empty((T, n), dtype=np.float64)
+    absy = np.empty((T, n), dtype=np.float64)
+    _load().orc_moe_combine(_ptr(out), _ptr(pair_rows), _ptr(weights), T, topk, n, _ptr(y),
+                            _ptr(absy))
+    return y, absy
+
+
 # --------------------------------------------------------------------------- acceptance
 
 U32 = 2.0 ** -24
@@ -264,4 +318,5 @@ def lib_path():
 
 __all__ = ["NVFP4", "MXFP4", "e4m3_decode", "e2m1_decode", "e8m0_decode", "e4m3_encode",
            "pow2_ceil", "e4m3_threshold", "act_quant", "gemm_ref", "grouped_ref_sampled",
-           "within_bound", "max_rel", "lib_path", "U32"]
+           "route_topk", "route_csr", "moe_combine", "within_bound", "max_rel", "lib_path",
+           "U32"]

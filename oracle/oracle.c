@@ -16,10 +16,14 @@
  *        exponent 0 -> subnormal, exponent 15 with mantissa 7 -> NaN).
  *   [S]  same page as [Q]: struct ExpertRaw (nibble pairs [n,k/2], low nibble = even k;
  *        e4m3 scale per 16 (NVFP4) or e8m0 scale per 32 (MXFP4); f32 scale2 for NVFP4).
- *   [M]  same page as [Q], fn mirror_gemm: the order of the page's own GPU kernel, in f32:
- *        128 partials per output, partial t takes groups t, t+128, ..., each group's
- *        sum of gs products accumulated in order, times f32(ws * as), added to the
- *        partial; then a fixed halving tree (offsets 64, 32, ..., 1).
+ *   [M]  same page as [Q], fn mirror_gemm: the summation order of the page's own GPU
+ *        kernel, in f32, restated as a specification where it is implemented below.
+ *   [C]  memra-engine 0.71.0, src/bin/kernel_check.rs, grouped MoE GEMM section: routed
+ *        rows grouped by expert behind CSR offsets, offsets[e+1] = offsets[e] + rows of e,
+ *        and a per-routed-row factor applied to that row's output.
+ *   [T]  memra-engine 0.125.0, src/bin/qwen4exp_gpu_gate.rs, the device-router arm: a
+ *        softmax top-k router (selected ids and their order exact, weights within a few
+ *        ulps). Its body is not printed; the reading taken is stated at orc_route_topk.
  *   [G]  same page as [Q], the swiglu_limit saturation cell and the f64 check of main:
  *        h = g * (1 / (1 + exp(-g))) * u with u = clamp(up, -L, L) and g = min(gate, L)
  *        (up clamped on both sides, gate on one side, both before the sigmoid).
@@ -43,6 +47,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "oracle.h"
@@ -302,7 +307,33 @@ void orc_swiglu(const float *gate, const float *up, int64_t ld, int64_t rows, in
 
 /* ------------------------------------------------------------------ mirror order [M] */
 
-#define ORC_MIRROR_THREADS 128
+/*
+ * The summation order of the page's own kernel, restated as a specification:
+ *   group term  G_j = (the gs exact products e4m3(code) * E2M1(nibble) of weight group j,
+ *                     added one at a time in k order, in f32) * f32(ws_j * s_a), with s_a
+ *                     the scale of the activation block that holds the group;
+ *   partial     P_t = the f32 running sum of G_t, G_{t+128}, G_{t+256}, ..., in that order
+ *                     (starting from 0);
+ *   result          = P_0 after the levels w = 64, 32, ..., 1 of a pairwise tree, each
+ *                     replacing P_t by P_t + P_{t+w} for every t < w.
+ * Below: all group terms of an output first, then the strided fold, then the tree.
+ */
+#define ORC_MIRROR_WIDTH 128
+
+static float mirror_group_term(const uint8_t *codes_row, const float *scales_row,
+                               const uint8_t *nibbles, uint8_t scale_byte, float scale2,
+                               int recipe, int gs, int64_t j)
+{
+    float dot = 0.0f;
+    for (int64_t kk = j * gs; kk < (j + 1) * gs; ++kk) {
+        const unsigned nib = (unsigned)(nibbles[kk / 2] >> (4 * (kk % 2))) & 0x0Fu;
+        const float a = (float)g_e4m3[codes_row[kk]];
+        const float wv = (float)g_e2m1[nib];
+        dot = dot + a * wv; /* the product is exact in f32; one rounding per add */
+    }
+    const float ws = weight_scale(recipe, scale_byte, scale2);
+    return dot * (ws * scales_row[(j * gs) / 128]);
+}
 
 void orc_mirror_gemm(const uint8_t *codes, const float *scales, const uint8_t *w,
                      const uint8_t *sc, float scale2, int recipe, int64_t g, int64_t n, int64_t k,
@@ -310,37 +341,124 @@ void orc_mirror_gemm(const uint8_t *codes, const float *scales, const uint8_t *w
 {
     init_tables();
     const int gs = group_size(recipe);
-    const int64_t ngroups = k / gs, kq = k / 128;
-    float part[ORC_MIRROR_THREADS];
+    const int64_t groups = k / gs;
+    float *terms = (float *)malloc((size_t)groups * sizeof(float));
+    float part[ORC_MIRROR_WIDTH];
+    if (!terms)
+        return;
     for (int64_t r = 0; r < g; ++r) {
-        const uint8_t *arow = codes + r * k;
-        const float *asrow = scales + r * kq;
         for (int64_t c = 0; c < n; ++c) {
-            const uint8_t *wrow = w + c * (k / 2);
-            const uint8_t *srow = sc + c * ngroups;
-            for (int t = 0; t < ORC_MIRROR_THREADS; ++t) {
-                float acc = 0.0f;
-                for (int64_t j = t; j < ngroups; j += ORC_MIRROR_THREADS) {
-                    const int64_t k0 = j * gs;
-                    float sub = 0.0f;
-                    for (int i = 0; i < gs; ++i) {
-                        const int64_t kk = k0 + i;
-                        const uint8_t byte = wrow[kk >> 1];
-                        const uint8_t nib = (kk & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0x0F);
-                        const float prod = (float)g_e4m3[arow[kk]] * (float)g_e2m1[nib];
-                        sub = sub + prod;
-                    }
-                    const float ws = weight_scale(recipe, srow[j], scale2);
-                    const float scl = ws * asrow[k0 / 128];
-                    const float term = sub * scl;
-                    acc = acc + term;
-                }
-                part[t] = acc;
+            for (int64_t j = 0; j < groups; ++j)
+                terms[j] = mirror_group_term(codes + r * k, scales + r * (k / 128),
+                                             w + c * (k / 2), sc[c * groups + j], scale2, recipe,
+                                             gs, j);
+            for (int t = 0; t < ORC_MIRROR_WIDTH; ++t) {
+                part[t] = 0.0f;
+                for (int64_t j = t; j < groups; j += ORC_MIRROR_WIDTH)
+                    part[t] = part[t] + terms[j];
             }
-            for (int off = ORC_MIRROR_THREADS >> 1; off > 0; off >>= 1)
-                for (int t = 0; t < off; ++t)
-                    part[t] = part[t] + part[t + off];
+            for (int width = ORC_MIRROR_WIDTH / 2; width >= 1; width /= 2)
+                for (int t = 0; t < width; ++t)
+                    part[t] = part[t] + part[t + width];
             out[r * n + c] = part[0];
         }
     }
+    free(terms);
+}
+
+/* ------------------------------------------------------------------ routing front-end [T] [C] */
+
+/*
+ * Router [T] (reading): each token picks the topk experts with the largest logits (a
+ * softmax is monotone, so these are also the largest probabilities); equal logits rank the
+ * lower expert id first; ids are emitted best first. Weights are softmax probabilities in
+ * f64: p_e = exp(l_e - max) / sum_e' exp(l_e' - max) over all E experts, or, with
+ * renormalize, the selected ones divided by their sum.
+ */
+void orc_route_topk(const float *logits, int64_t T, int E, int topk, int renormalize,
+                    int32_t *ids, double *weights)
+{
+    for (int64_t t = 0; t < T; ++t) {
+        const float *l = logits + t * E;
+        int32_t *id = ids + t * topk;
+        for (int j = 0; j < topk; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                int taken = 0;
+                for (int i = 0; i < j; ++i)
+                    taken |= (id[i] == e);
+                if (!taken && (best < 0 || l[e] > l[best]))
+                    best = e; /* strictly greater: the lower id keeps a tie */
+            }
+            id[j] = best;
+        }
+        double mx = -INFINITY;
+        for (int e = 0; e < E; ++e)
+            if ((double)l[e] > mx)
+                mx = (double)l[e];
+        double denom = 0.0;
+        if (renormalize) {
+            for (int j = 0; j < topk; ++j)
+                denom += exp((double)l[id[j]] - mx);
+        } else {
+            for (int e = 0; e < E; ++e)
+                denom += exp((double)l[e] - mx);
+        }
+        for (int j = 0; j < topk; ++j)
+            weights[t * topk + j] = exp((double)l[id[j]] - mx) / denom;
+    }
+}
+
+/*
+ * CSR construction [C]: routed rows grouped by expert, in token order within an expert (a
+ * counting sort of the (token, slot) pairs by expert id, stable in token order).
+ * ids [T, topk] -> offsets [E+1], row_ids [T*topk] (the token of each routed row) and
+ * pair_rows [T, topk] (the routed row of each pair). Returns 0, or -1 if an id is outside
+ * [0, E).
+ */
+int orc_route_csr(const int32_t *ids, int64_t T, int topk, int E, int32_t *offsets,
+                  int32_t *row_ids, int32_t *pair_rows)
+{
+    for (int e = 0; e <= E; ++e)
+        offsets[e] = 0;
+    for (int64_t i = 0; i < T * topk; ++i) {
+        if (ids[i] < 0 || ids[i] >= E)
+            return -1;
+        offsets[ids[i] + 1] += 1;
+    }
+    for (int e = 0; e < E; ++e)
+        offsets[e + 1] += offsets[e];
+    int32_t *fill = (int32_t *)calloc((size_t)E, sizeof(int32_t));
+    if (!fill)
+        return -1;
+    for (int64_t t = 0; t < T; ++t)
+        for (int j = 0; j < topk; ++j) {
+            const int e = ids[t * topk + j];
+            const int32_t p = offsets[e] + fill[e]++;
+            row_ids[p] = (int32_t)t;
+            pair_rows[t * topk + j] = p;
+        }
+    free(fill);
+    return 0;
+}
+
+/*
+ * Weighted combine [C]: y[t][c] = sum over the token's pairs j of weight[t][j] *
+ * out[pair_rows[t][j]][c], in f64, plus sum |weight * out| per output for the error model.
+ */
+void orc_moe_combine(const float *out, const int32_t *pair_rows, const float *weights,
+                     int64_t T, int topk, int64_t n, double *y, double *absy)
+{
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t c = 0; c < n; ++c) {
+            double acc = 0.0, aabs = 0.0;
+            for (int j = 0; j < topk; ++j) {
+                const double term = (double)weights[t * topk + j] *
+                                    (double)out[(int64_t)pair_rows[t * topk + j] * n + c];
+                acc += term;
+                aabs += fabs(term);
+            }
+            y[t * n + c] = acc;
+            absy[t * n + c] = aabs;
+        }
 }

@@ -44,6 +44,15 @@ void orc_mirror_gemm(const uint8_t *codes, const float *scales, const uint8_t *w
 void orc_swiglu(const float *gate, const float *up, int64_t ld, int64_t rows, int64_t inter,
                 float limit, double *h);
 
+/* Routing front-end: softmax top-k router (reading in oracle.c), CSR construction,
+ * weighted combine of the routed rows' outputs back to tokens. */
+void orc_route_topk(const float *logits, int64_t T, int E, int topk, int renormalize,
+                    int32_t *ids, double *weights);
+int orc_route_csr(const int32_t *ids, int64_t T, int topk, int E, int32_t *offsets,
+                  int32_t *row_ids, int32_t *pair_rows);
+void orc_moe_combine(const float *out, const int32_t *pair_rows, const float *weights,
+                     int64_t T, int topk, int64_t n, double *y, double *absy);
+
 #ifdef __cplusplus
 }
 #endif

@@ -541,3 +541,100 @@ def test_mirror_halving_tree_order():
     assert seq == np.float32(32.0)          # the order matters for this input
     ref, _ = oracle.gemm_ref(codes, scales, w, sc, 1.0, oracle.NVFP4)
     assert ref[0, 0] == 32.0 + 2.0 ** -18   # and the tree result is the exact sum
+
+
+# ------------------------------------------------------------------ routing front-end
+
+def _parse_routing(golden_dir):
+    topk, csr = [], []
+    with open(os.path.join(golden_dir, "routing_examples.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line.startswith("topk:"):
+                parts = [p.strip() for p in line[5:].split(";")]
+                topk.append((np.array(parts[0].split(), dtype=np.float32), int(parts[1]),
+                             [int(v) for v in parts[2].split()], float(parts[3])))
+            elif line.startswith("csr:"):
+                parts = [p.strip() for p in line[4:].split(";")]
+                ids = np.array([[int(v) for v in g.split()] for g in parts[1].split("|")],
+                               dtype=np.int32)
+                csr.append((int(parts[0]), ids, [int(v) for v in parts[2].split()],
+                            [int(v) for v in parts[3].split()],
+                            np.array([int(v) for v in parts[4].split()]).reshape(ids.shape)))
+    return topk, csr
+
+
+def test_route_topk_worked_examples(golden_dir):
+    topk, _ = _parse_routing(golden_dir)
+    assert len(topk) >= 4
+    for logits, k, want_ids, want_w0 in topk:
+        ids, w = oracle.route_topk(logits[None, :], k)
+        assert ids[0].tolist() == want_ids
+        assert abs(w[0, 0] - want_w0) <= 5e-9   # the fixture prints 9 decimals
+
+
+def test_route_topk_matches_sort_and_softmax():
+    """Selection = a stable sort of the experts by descending logit (numpy lexsort),
+    weights = the softmax (closed form in numpy, f64), renormalised or not; logits drawn
+    from a few values so that ties straddle the top-k boundary often."""
+    rng = np.random.default_rng(71)
+    for E, k in [(8, 2), (64, 8), (512, 10)]:
+        logits = rng.choice(np.linspace(-3, 3, 13), size=(40, E)).astype(np.float32)
+        logits[0] = 1.5                                   # all equal
+        logits[1, :] = -200.0
+        logits[1, 3] = 200.0                              # others underflow
+        for renorm in (False, True):
+            ids, w = oracle.route_topk(logits, k, renormalize=renorm)
+            for t in range(logits.shape[0]):
+                order = np.lexsort((np.arange(E), -logits[t].astype(np.float64)))
+                assert ids[t].tolist() == order[:k].tolist()
+                z = np.exp(logits[t].astype(np.float64) - logits[t].max())
+                p = z / z.sum()
+                want = p[order[:k]] / (p[order[:k]].sum() if renorm else 1.0)
+                np.testing.assert_allclose(w[t], want, rtol=1e-12, atol=0)
+    ids, _ = oracle.route_topk(np.full((1, 16), 0.5, np.float32), 4)
+    assert ids[0].tolist() == [0, 1, 2, 3]
+
+
+def test_route_csr_worked_examples(golden_dir):
+    _, csr = _parse_routing(golden_dir)
+    assert len(csr) >= 3
+    for E, ids, off, rid, prows in csr:
+        o, r, p = oracle.route_csr(ids, E)
+        assert o.tolist() == off and r.tolist() == rid
+        assert np.array_equal(p, prows)
+
+
+def test_route_csr_matches_stable_sort():
+    """Routed rows = the (token, slot) pairs stably sorted by expert (numpy argsort, kind
+    stable, over the token-major pair list); offsets = the cumulative counts."""
+    rng = np.random.default_rng(72)
+    for T, E, k in [(1, 4, 1), (37, 16, 3), (300, 64, 8)]:
+        ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+        off, rid, prow = oracle.route_csr(ids, E)
+        flat = ids.reshape(-1)
+        order = np.argsort(flat, kind="stable")
+        assert rid.tolist() == (order // k).tolist()
+        pos = np.empty_like(order)
+        pos[order] = np.arange(order.size)
+        assert prow.reshape(-1).tolist() == pos.tolist()
+        assert off.tolist() == [0] + np.cumsum(np.bincount(flat, minlength=E)).tolist()
+    with pytest.raises(ValueError):
+        oracle.route_csr(np.array([[0, 4]], np.int32), 4)
+
+
+def test_moe_combine_closed_forms():
+    rng = np.random.default_rng(73)
+    T, k, n = 5, 3, 64
+    out = rng.standard_normal((T * k, n)).astype(np.float32)
+    prow = rng.permutation(T * k).reshape(T, k).astype(np.int32)
+    onehot = np.zeros((T, k), np.float32)
+    onehot[:, 1] = 1.0
+    y, absy = oracle.moe_combine(out, prow, onehot)
+    assert np.array_equal(y, out[prow[:, 1]].astype(np.float64))     # selection, exact
+    w = rng.random((T, k)).astype(np.float32)
+    y, absy = oracle.moe_combine(out, prow, w)
+    want = np.einsum("tj,tjc->tc", w.astype(np.float64), out[prow].astype(np.float64))
+    np.testing.assert_allclose(y, want, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(absy, np.einsum("tj,tjc->tc", np.abs(w.astype(np.float64)),
+                                               np.abs(out[prow].astype(np.float64))), rtol=1e-13)
