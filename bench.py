@@ -50,6 +50,8 @@ def parse_args():
                     help="skip the mixed-recipe line (128 NVFP4 + 128 MXFP4 experts)")
     ap.add_argument("--no-swiglu", action="store_true",
                     help="skip the SwiGLU + requantisation line (the step after gate/up)")
+    ap.add_argument("--no-routing", action="store_true",
+                    help="skip the routing front-end line (router, CSR, combine)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--experts", type=int, default=0, help="override the workload's expert count")
@@ -230,6 +232,14 @@ def proj_bytes(proj):
     return weights + act + out, weights
 
 
+def quant_bytes(proj):
+    """Algorithmic bytes of the quantise pass: each token's activation row read once (f32),
+    the 16-bit workspace row of every routed row written once, plus the row scales."""
+    T, k = proj.x.shape
+    P = proj.routing.P
+    return T * k * 4 + P * k * 2 + P * 4
+
+
 def launches_per_call(fp4, proj, have_ws):
     """Kernels of ours one grouped call launches: the streaming kernel alone, or the
     tensor-core path's quantise pass(es) + GEMM (NVFP4: f16 pass, conditional bf16 pass)."""
@@ -243,6 +253,10 @@ def launches_per_call(fp4, proj, have_ws):
 # ------------------------------------------------------------------ our arm
 
 def make_calls(fp4, wl, device):
+    """One entry per grouped projection. On the tensor-core path the call is run as its
+    two halves (fp4_grouped_quantize, then fp4_grouped_gemm_quantized on the same stream:
+    exactly the launches fp4_grouped_expert_gemm makes), so that the quantise pass and the
+    GEMM kernel are timed apart; the streaming path is one launch."""
     import torch
     calls = []
     for proj in wl.projections:
@@ -256,18 +270,30 @@ def make_calls(fp4, wl, device):
             fp4.fp4_grouped_expert_gemm(proj.x if x is None else x, rid, proj.routing.offsets,
                                         proj.bank.w, proj.bank.sc, proj.bank.scale2,
                                         proj.bank.recipe, out=out, workspace=ws)
-        calls.append({"proj": proj, "call": call, "out": out, "ws": ws, "path": path,
-                      "launches": nl})
+        if path == fp4.PATH_TC:
+            def quantize(proj=proj, ws=ws, rid=rid):
+                fp4.fp4_grouped_quantize(proj.x, rid, proj.routing.P, proj.bank.recipe, ws)
+
+            def gemm(proj=proj, ws=ws, out=out):
+                fp4.fp4_grouped_gemm_quantized(ws, proj.routing.offsets, proj.bank.w, proj.bank.sc,
+                                               proj.bank.scale2, proj.bank.recipe, out)
+            phases = [("quantize", quantize), ("gemm", gemm)]
+        else:
+            phases = [("gemm", call)]
+        calls.append({"proj": proj, "call": call, "phases": phases, "out": out, "ws": ws,
+                      "path": path, "launches": nl})
     return calls
 
 
 def time_steps(calls, steps, flush=None):
-    """Run `steps` steps; per call, CUDA events on the launching (current) stream.
-    Returns (elapsed ms of the whole region, per-call list of durations in ms)."""
+    """Run `steps` steps; CUDA events on the launching (current) stream around every phase
+    of every call. Returns (elapsed ms of the whole region, per-call list of per-step call
+    durations in ms, per-call dict phase -> per-step durations in ms)."""
     import torch
     stream = torch.cuda.current_stream()
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in calls] for _ in range(steps)]
+    nph = [len(c["phases"]) for c in calls]
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for n in nph]
+           for _ in range(steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -276,14 +302,34 @@ def time_steps(calls, steps, flush=None):
         if flush is not None:
             flush.zero_()
         for i, c in enumerate(calls):
-            evs[s][i][0].record(stream)
-            c["call"]()
-            evs[s][i][1].record(stream)
+            e = evs[s][i]
+            e[0].record(stream)
+            for j, (_, fn) in enumerate(c["phases"]):
+                fn()
+                e[j + 1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
-    per_call = [[evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(steps)]
+    per_call = [[evs[s][i][0].elapsed_time(evs[s][i][-1]) for s in range(steps)]
                 for i in range(len(calls))]
-    return t0.elapsed_time(t1), per_call
+    per_phase = [{name: [evs[s][i][j].elapsed_time(evs[s][i][j + 1]) for s in range(steps)]
+                  for j, (name, _) in enumerate(c["phases"])} for i, c in enumerate(calls)]
+    return t0.elapsed_time(t1), per_call, per_phase
+
+
+def pct(v, q):
+    """q-quantile of a list (linear interpolation)."""
+    import statistics
+    v = sorted(v)
+    if len(v) == 1:
+        return v[0]
+    return statistics.quantiles(v, n=100, method="inclusive")[int(q * 100) - 1] if 0 < q < 1 else (
+        v[0] if q <= 0 else v[-1])
+
+
+def stats_ms(v):
+    import statistics
+    return {"mean": round(sum(v) / len(v), 4), "median": round(statistics.median(v), 4),
+            "p10": round(pct(v, 0.10), 4), "p90": round(pct(v, 0.90), 4)}
 
 
 def run_e2e(fp4, calls, steps):
@@ -369,45 +415,110 @@ def run_e2e(fp4, calls, steps):
     return t0.elapsed_time(t1) / steps, h2d, d2h, ok
 
 
-def cpu_oracle_sample(wl, budget_s, rows_cap=None, seed=0):
-    """Time the CPU oracle (as it stands, single-threaded C) on a bounded sample of the
-    workload's routed rows, all n columns each. Returns (flops, seconds, description)."""
+def host_cpu():
+    """Core count and CPU model of this host."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith(("model name", "cpu part")):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return os.cpu_count() or 1, model or "unknown"
+
+
+def cpu_sample_tasks(wl, frac=1.0 / 64, seed=0, rows_per_proj=None):
+    """A seeded sample of the workload's routed rows for the CPU oracle: per projection,
+    max(1, round(frac * rows)) random rows of every expert that has rows (or, with
+    rows_per_proj, that many random routed rows). Each task is one routed row with its
+    expert's weights as host arrays; all n columns of the row are computed."""
     import numpy as np
-    import oracle
     rng = np.random.default_rng(seed)
-    flops = 0.0
-    secs = 0.0
-    rows_done = 0
-    per_proj = budget_s / len(wl.projections)
+    tasks = []
     for proj in wl.projections:
         b = proj.bank
         off = proj.routing.offsets.cpu().numpy().astype(np.int64)
         rid = proj.routing.row_ids.cpu().numpy()
-        P = proj.routing.P
-        t_start = time.perf_counter()
-        done_here = 0
-        while True:
-            p = int(rng.integers(0, P))
-            e = int(np.searchsorted(off, p, side="right") - 1)
-            t = int(rid[p]) if proj.row_ids_used else p
-            x = proj.x[t:t + 1].cpu().numpy()
-            w = b.w[e].cpu().numpy()
-            sc = b.sc[e].cpu().numpy()
-            s2 = float(b.scale2[e].item())
-            t1 = time.perf_counter()
-            codes, scales = oracle.act_quant(x)
-            oracle.gemm_ref(codes, scales, w, sc, s2, b.recipe)
-            secs += time.perf_counter() - t1
-            flops += 2.0 * b.n * b.k
-            done_here += 1
-            rows_done += 1
-            if rows_cap is not None and done_here >= rows_cap:
-                break
-            if time.perf_counter() - t_start >= per_proj and done_here >= 2:
-                break
-    desc = "%d random routed rows x all n columns (act_quant + f64 reference), %s" % (
-        rows_done, "+".join(p.name for p in wl.projections))
-    return flops, secs, desc
+        if rows_per_proj is None:
+            picks = []
+            for e in range(b.E):
+                cnt = int(off[e + 1] - off[e])
+                if cnt > 0:
+                    m = max(1, int(round(frac * cnt)))
+                    picks.extend((off[e] + rng.choice(cnt, size=m, replace=False)).tolist())
+        else:
+            picks = rng.integers(0, proj.routing.P, size=rows_per_proj).tolist()
+        experts = np.searchsorted(off, np.asarray(picks, dtype=np.int64), side="right") - 1
+        cache = {}
+        for p, e in zip(picks, experts.tolist()):
+            if e not in cache:
+                cache[e] = (b.w[e].cpu().numpy(), b.sc[e].cpu().numpy(), float(b.scale2[e].item()))
+            w, sc, s2 = cache[e]
+            t = int(rid[p]) if proj.row_ids_used else int(p)
+            tasks.append((proj.x[t:t + 1].cpu().numpy(), w, sc, s2, b.recipe, 2.0 * b.n * b.k))
+    return tasks
+
+
+def run_cpu_tasks(tasks, threads):
+    """Time the oracle (as it stands: act_quant + the f64 reference of one routed row, all
+    n columns) over the tasks on `threads` host threads. The oracle is C called through
+    ctypes, which releases the GIL, so the threads run on separate cores. Returns seconds."""
+    import numpy as np
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    oracle.act_quant(np.zeros((1, 128), dtype=np.float32))  # builds the oracle's tables once
+
+    def one(t):
+        x, w, sc, s2, recipe, _ = t
+        codes, scales = oracle.act_quant(x)
+        oracle.gemm_ref(codes, scales, w, sc, s2, recipe)
+
+    t0 = time.perf_counter()
+    if threads <= 1:
+        for t in tasks:
+            one(t)
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(one, tasks))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wl, flops_step, single_budget_s=12.0):
+    """The oracle on the host cores over a seeded 1/64 row sample of the workload: all
+    cores, and single-threaded on a bounded prefix of the same sample; per-FLOP
+    extrapolation to one full step."""
+    cores, model = host_cpu()
+    tasks = cpu_sample_tasks(wl)
+    fl_all = sum(t[-1] for t in tasks)
+    secs_all = run_cpu_tasks(tasks, cores)
+    rate_all = fl_all / secs_all
+    # single thread: the same sample in order until about single_budget_s of work
+    per_row_s = secs_all * cores / len(tasks)
+    n1 = max(2, min(len(tasks), int(single_budget_s / max(per_row_s, 1e-6))))
+    secs_1 = run_cpu_tasks(tasks[:n1], 1)
+    rate_1 = sum(t[-1] for t in tasks[:n1]) / secs_1
+    names = "+".join(p.name for p in wl.projections)
+    return {"value": rate_all / 1e12, "unit": "TFLOP/s", "cores": cores, "cpu_model": model,
+            "kind": "oracle",
+            "sample": "%d routed rows (1/64 of each expert's rows, at least one per expert with "
+                      "rows) x all n columns, act_quant + f64 reference, %s, on %d threads" % (
+                          len(tasks), names, cores),
+            "seconds": round(secs_all, 2),
+            "single_thread": {"value": rate_1 / 1e12, "unit": "TFLOP/s", "rows": n1,
+                              "seconds": round(secs_1, 2)},
+            "extrapolated_s_per_step": round(flops_step / rate_all, 1),
+            "extrapolated_s_per_step_single_thread": round(flops_step / rate_1, 1)}
 
 
 def run_ours(args, world, rank, local):
@@ -438,40 +549,63 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     steps = args.steps
     if steps <= 0:
-        el, _ = time_steps(calls, 3)
+        el, _, _ = time_steps(calls, 3)
         steps = max(10, min(2000, int(2000.0 / max(el / 3, 1e-3))))
     steps = int(max_over_ranks(steps, world))
 
     barrier(world)
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
-    elapsed, per_call = time_steps(calls, steps)
+    elapsed, per_call, per_phase = time_steps(calls, steps)
     clk = clocks.stop()
     barrier(world)
     elapsed = max_over_ranks(elapsed, world)
     ms_step = elapsed / steps
     value = world * flops_step / (ms_step * 1e-3) / 1e12
+    step_ms = [sum(per_call[i][s] for i in range(len(calls))) for s in range(steps)]
 
-    # roofline of the dominant kernel: the grouped GEMM call (all launches of it)
+    # roofline of the dominant kernel: on the tensor-core path the GEMM kernel alone (its
+    # launches timed apart from the quantise pass), else the streaming kernel
     paths = sorted({c["path"] for c in calls})
     call_ms = [sum(d) / len(d) for d in per_call]
     kflops = sum(proj_flops(c["proj"]) for c in calls)
-    kms = sum(call_ms)
     tc = all(c["path"] == fp4.PATH_TC for c in calls)
     if tc:
-        # both recipes run the bf16 kind::f16 MMA (operands bf16, exact): bf16 dense peak
+        gemm_ms = sum(sum(ph["gemm"]) / len(ph["gemm"]) for ph in per_phase)
+        quant_ms = sum(sum(ph["quantize"]) / len(ph["quantize"]) for ph in per_phase)
+        # both recipes run the kind::f16 MMA (16-bit operands, exact): bf16 dense peak
         peak = peaks["bf16_tflops"]
-        achieved = kflops / (kms * 1e-3) / 1e12
+        achieved = kflops / (gemm_ms * 1e-3) / 1e12
+        call_level = kflops / (sum(call_ms) * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1),
-                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "kernel": "tc_grouped_gemm",
+                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                    "kernel": "tc_gemm_kernel",
+                    "kernel_ms_per_step": round(gemm_ms, 4),
                     "traffic": ncu_traffic("tc_grouped_gemm/%s" % args.workload),
-                    "traffic_basis": "DRAM bytes per step (all grouped calls)",
+                    "traffic_basis": "DRAM bytes per step of the tc_gemm_kernel launches (one "
+                                     "per projection), without the quantise pass",
                     "peak_source": peak_src + " bf16 dense (burst)",
                     # the FP8 dense rate (2x bf16, nominal ratio) for comparison with an
                     # FP8-MMA design; this path's exact products need 16-bit operands
-                    "fp8_peak": round(2 * peak, 1), "frac_of_fp8": round(achieved / (2 * peak), 4)}
+                    "fp8_peak": round(2 * peak, 1), "frac_of_fp8": round(achieved / (2 * peak), 4),
+                    "call_level": {"achieved": round(call_level, 2),
+                                   "frac": round(call_level / peak, 4),
+                                   "ms_per_step": round(sum(call_ms), 4),
+                                   "what": "quantise pass + GEMM per grouped call"}}
+        qbytes = sum(quant_bytes(c["proj"]) for c in calls)
+        qgbs = qbytes / (quant_ms * 1e-3) / 1e9
+        result_quant = {"kernel": "quant_ws_kernel", "ms_per_step": round(quant_ms, 4),
+                        "bytes_per_step": qbytes,
+                        "roofline": {"bound": "hbm", "achieved": round(qgbs, 1),
+                                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                     "frac": round(qgbs / peaks["hbm_gbs"], 4),
+                                     "traffic": ncu_traffic("tc_quantize/%s" % args.workload),
+                                     "peak_source": peak_src + " HBM copy bandwidth"},
+                        "bytes_basis": "activation rows read once per token (f32), the 16-bit "
+                                       "workspace written once per routed row"}
     else:
         # the streaming path is bound by HBM reads of the weights
+        kms = sum(call_ms)
         kbytes = sum(proj_bytes(c["proj"])[0] for c in calls)
         achieved = kbytes / (kms * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]
@@ -480,8 +614,11 @@ def run_ours(args, world, rank, local):
                     "traffic": ncu_traffic("%s/%s" % (STREAM_KERNEL, args.workload)),
                     "traffic_basis": "DRAM bytes per step (all grouped calls)",
                     "peak_source": peak_src + " HBM copy bandwidth"}
+        result_quant = None
     roofline["launches"] = steps * sum(c["launches"] for c in calls)
     roofline["per_call_ms"] = [round(m, 4) for m in call_ms]
+    roofline["per_phase_ms"] = [{k: round(sum(v) / len(v), 4) for k, v in ph.items()}
+                                for ph in per_phase]
 
     result = {"metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
               "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -497,8 +634,11 @@ def run_ours(args, world, rank, local):
                          "l2": "inputs larger than L2 (weights %.2f GB per step)" %
                                (sum(proj_bytes(c["proj"])[1] for c in calls) / 1e9),
                          "parallelism": "replicas x%d" % world},
+              "step_ms": stats_ms(step_ms),
               "roofline": roofline, "clocks": clk,
               "gpu_launches": steps * sum(c["launches"] for c in calls)}
+    if result_quant is not None:
+        result["quantize"] = result_quant
 
     # decode workload alongside: weight GB/s against HBM, L2 flushed between steps
     if args.workload == "c4" and not args.no_decode:
@@ -509,7 +649,7 @@ def run_ours(args, world, rank, local):
             for c in dcalls:
                 c["call"]()
         dsteps = 200
-        _, dper = time_steps(dcalls, dsteps, flush=flush)
+        _, dper, _ = time_steps(dcalls, dsteps, flush=flush)
         dms = [sum(d) / len(d) for d in dper]
         dbytes = sum(proj_bytes(c["proj"])[0] for c in dcalls)
         dweights = sum(proj_bytes(c["proj"])[1] for c in dcalls)
@@ -536,6 +676,10 @@ def run_ours(args, world, rank, local):
     if args.workload == "c4" and not args.no_swiglu:
         result["swiglu_quant"] = measure_swiglu(fp4, device, peaks, peak_src)
 
+    # the routing front-end (before and after the projections)
+    if args.workload == "c4" and not args.no_routing:
+        result["routing"] = measure_routing(fp4, device, peaks, peak_src)
+
     # end to end through the public API with host buffers
     if not args.no_e2e:
         e2e_steps = min(steps, 10)
@@ -549,15 +693,12 @@ def run_ours(args, world, rank, local):
                                      "streams, double-buffered device inputs and outputs"}
 
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
-        fl, secs, desc = cpu_oracle_sample(wl, 12.0)
-        result["cpu_baseline"] = {"value": fl / secs / 1e12, "unit": "TFLOP/s", "cores": 1,
-                                  "kind": "oracle", "sample": desc,
-                                  "seconds": round(secs, 2)}
+        result["cpu_baseline"] = cpu_baseline(wl, flops_step)
     return result
 
 
 def run_reference(args, world, rank):
-    """The oracle (as it stands) on the host cores: each step is a bounded sample of the
+    """The oracle (as it stands) on all host cores: each step is a bounded sample of the
     same workload (16 random routed rows per projection, all n columns)."""
     import torch
     from block_scaled_fp4_act_gb300 import synth
@@ -565,25 +706,33 @@ def run_reference(args, world, rank):
     oracle.lib_path()
     device = "cuda" if torch.cuda.is_available() else "cpu"
     wl = synth.workload(args.workload, device=device)
+    cores, model = host_cpu()
     rows = 16
     for i in range(args.warmup):
-        cpu_oracle_sample(wl, 1e9, rows_cap=rows, seed=1000 + i)
-    fl_tot, s_tot = 0.0, 0.0
+        run_cpu_tasks(cpu_sample_tasks(wl, seed=1000 + i, rows_per_proj=rows), cores)
+    fl_tot, s_tot, ntasks = 0.0, 0.0, 0
     steps = args.steps if args.steps > 0 else 10
+    step_s = []
     for i in range(steps):
-        fl, secs, desc = cpu_oracle_sample(wl, 1e9, rows_cap=rows, seed=i)
-        fl_tot += fl
+        tasks = cpu_sample_tasks(wl, seed=i, rows_per_proj=rows)
+        secs = run_cpu_tasks(tasks, cores)
+        fl_tot += sum(t[-1] for t in tasks)
         s_tot += secs
+        ntasks += len(tasks)
+        step_s.append(secs * 1e3)
     value = fl_tot / s_tot / 1e12
     ms = s_tot / steps * 1e3
+    desc = "%d random routed rows per projection per step x all n columns (act_quant + f64 " \
+           "reference), %s, on %d threads" % (rows, "+".join(p.name for p in wl.projections), cores)
     return {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "step_ms": stats_ms(step_s),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded)", "impl": "reference",
             "config": {"workload": WORKLOAD_NAMES[args.workload],
                        "sample": "%d random routed rows per projection per step" % rows},
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-                             "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores,
+                             "cpu_model": model, "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
@@ -599,19 +748,26 @@ def measure_mixed(fp4, synth, device, peaks, peak_src, steps=20):
     for _ in range(3):
         for c in calls:
             c["call"]()
-    _, per = time_steps(calls, steps)
+    _, per, phases = time_steps(calls, steps)
     ms = [sum(d) / len(d) for d in per]
     bf16 = peaks["bf16_tflops"]
     out = {"workload": WORKLOAD_NAMES["c5"], "steps": steps, "recipes": {}}
     tot_f = 0.0
-    for c, m in zip(calls, ms):
+    for c, m, ph in zip(calls, ms, phases):
         f = proj_flops(c["proj"])
         tot_f += f
         tf = f / (m * 1e-3) / 1e12
-        out["recipes"][c["proj"].name] = {
-            "ms_per_call": round(m, 4), "tflops": round(tf, 1),
-            "frac_bf16": round(tf / bf16, 4), "frac_fp8": round(tf / (2 * bf16), 4),
-            "path": c["path"]}
+        rec = {"ms_per_call": round(m, 4), "tflops": round(tf, 1),
+               "frac_bf16": round(tf / bf16, 4), "frac_fp8": round(tf / (2 * bf16), 4),
+               "path": c["path"]}
+        if "quantize" in ph:
+            gm = sum(ph["gemm"]) / len(ph["gemm"])
+            kt = f / (gm * 1e-3) / 1e12
+            rec["gemm_kernel"] = {"ms": round(gm, 4), "tflops": round(kt, 1),
+                                  "frac_bf16": round(kt / bf16, 4),
+                                  "frac_fp8": round(kt / (2 * bf16), 4)}
+            rec["quantize_ms"] = round(sum(ph["quantize"]) / len(ph["quantize"]), 4)
+        out["recipes"][c["proj"].name] = rec
     tf_all = tot_f / (sum(ms) * 1e-3) / 1e12
     out["combined"] = {"ms_per_step": round(sum(ms), 4), "tflops": round(tf_all, 1),
                        "frac_bf16": round(tf_all / bf16, 4), "frac_fp8": round(tf_all / (2 * bf16), 4),
@@ -656,6 +812,50 @@ def measure_swiglu(fp4, device, peaks, peak_src, rows=32768, inter=1024, limit=7
                          "bytes_per_call": nbytes, "kernel": "swiglu_quant",
                          "peak_source": peak_src},
             "gpu_launches": iters}
+
+
+def measure_routing(fp4, device, peaks, peak_src, T=4096, E=256, topk=8, n=7168, iters=50):
+    """The routing front-end at the prefill shapes: the router over [T, E] logits, the CSR
+    construction of T x topk routed rows, and the weighted combine of the down projection's
+    output [T*topk, n] back to [T, n] (HBM-bound: every routed row read once, y written
+    once). Not part of the projection step."""
+    import torch
+    gen = torch.Generator(device=device).manual_seed(33)
+    logits = torch.randn(T, E, generator=gen, device=device)
+    ids, w = fp4.fp4_route_topk(logits, topk, renormalize=True)
+    ws = torch.empty(max(16, int(fp4.lib().fp4_route_csr_workspace_size(T, E))), dtype=torch.uint8,
+                     device=device)
+    off, rid, prow = fp4.fp4_route_csr(ids, E, workspace=ws)
+    out = torch.randn(T * topk, n, generator=gen, device=device)
+    y = torch.empty(T, n, device=device)
+    calls = {"route_topk": lambda: fp4.fp4_route_topk(logits, topk, renormalize=True, ids=ids,
+                                                      weights=w),
+             "route_csr": lambda: fp4.fp4_route_csr(ids, E, workspace=ws, offsets=off,
+                                                    row_ids=rid, pair_rows=prow),
+             "moe_combine": lambda: fp4.fp4_moe_combine(out, prow, w, y=y)}
+    res = {"workload": "router over [%d, %d] logits top-%d, CSR of %d routed rows, combine of "
+                       "[%d, %d] f32 into [%d, %d]" % (T, E, topk, T * topk, T * topk, n, T, n)}
+    stream = torch.cuda.current_stream()
+    for name, fn in calls.items():
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(iters):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res[name + "_us"] = round(e0.elapsed_time(e1) * 1e3 / iters, 2)
+    nbytes = T * topk * n * 4 + T * n * 4 + T * topk * 8
+    gbs = nbytes / (res["moe_combine_us"] * 1e-6) / 1e9
+    res["combine_roofline"] = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                               "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                               "bytes_per_call": nbytes, "kernel": "moe_combine_kernel",
+                               "peak_source": peak_src}
+    res["gpu_launches"] = iters * (1 + 4 + 1)
+    del out, y
+    return res
 
 
 def path_sweep(rows_per_expert=(2, 4, 8, 16, 24, 32, 48, 64), E=64, n=3072, k=4096, iters=20):

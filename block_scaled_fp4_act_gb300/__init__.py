@@ -25,6 +25,7 @@ FP4_ERR_WORKSPACE = -6
 FP4_DEVERR_OFFSETS = 1
 FP4_DEVERR_ROW_ID = 2
 FP4_DEVERR_TIMEOUT = 4
+FP4_DEVERR_EXPERT_ID = 8
 
 PATH_AUTO = 0
 PATH_STREAM = 1
@@ -65,6 +66,19 @@ def lib():
         L.fp4_grouped_expert_gemm_noalloc.argtypes = [P, i64, P, P, i32, i64, P, P, P, i32, P,
                                                        i64, i64, P]
         L.fp4_grouped_expert_gemm_noalloc.restype = i32
+        L.fp4_grouped_quantize.argtypes = [P, i64, P, i64, i64, i32, P, sz, P]
+        L.fp4_grouped_quantize.restype = i32
+        L.fp4_grouped_gemm_quantized.argtypes = [P, sz, P, i32, i64, P, P, P, i32, P, i64, i64,
+                                                 P]
+        L.fp4_grouped_gemm_quantized.restype = i32
+        L.fp4_route_topk.argtypes = [P, i64, i32, i32, i32, P, P, P]
+        L.fp4_route_topk.restype = i32
+        L.fp4_route_csr_workspace_size.argtypes = [i64, i32]
+        L.fp4_route_csr_workspace_size.restype = sz
+        L.fp4_route_csr.argtypes = [P, i64, i32, i32, P, P, P, P, sz, P]
+        L.fp4_route_csr.restype = i32
+        L.fp4_moe_combine.argtypes = [P, i64, P, P, i64, i32, i64, P, P]
+        L.fp4_moe_combine.restype = i32
         L.fp4_gemm_mirror.argtypes = [P, P, P, P, f32, i32, P, i64, i64, i64, P]
         L.fp4_gemm_mirror.restype = i32
         L.fp4_swiglu_quant.argtypes = [P, P, i64, f32, i64, i64, P, P, P, P]
@@ -196,11 +210,51 @@ def fp4_grouped_expert_gemm(x, row_ids, offsets, w, wscale, scale2, recipe, out=
     return out
 
 
-def fp4_grouped_expert_gemm_noalloc(x, row_ids, offsets, w, wscale, scale2, recipe, out=None,
+def fp4_grouped_quantize(x, row_ids, total_rows, recipe, workspace, stream=None):
+    """Stage 1 of the tensor-core path: every routed row of x (x[row_ids[p]], or x[p]
+    without row ids) quantised into `workspace` (a uint8 CUDA tensor of at least
+    fp4_grouped_workspace_size(...) bytes) for fp4_grouped_gemm_quantized."""
+    import torch
+    T, k = x.shape
+    _need(x, torch.float32, None, "x")
+    if row_ids is not None:
+        _need(row_ids, torch.int32, (total_rows,), "row_ids")
+    _need(workspace, torch.uint8, None, "workspace")
+    _check(lib().fp4_grouped_quantize(_ptr(x), T, _ptr(row_ids), int(total_rows), k, int(recipe),
+                                      _ptr(workspace), workspace.numel(), _stream(stream)),
+           "fp4_grouped_quantize")
+    return workspace
+
+
+def fp4_grouped_gemm_quantized(workspace, offsets, w, wscale, scale2, recipe, out,
+                               stream=None):
+    """Stage 2 on the tensor cores from a workspace fp4_grouped_quantize filled for the same
+    routed rows, k and recipe: offsets [E+1] int32, w [E,n,k/2], wscale [E,n,k/gs],
+    scale2 [E] (NVFP4) -> out [P,n] f32 (caller-owned)."""
+    import torch
+    E, n = w.shape[0], w.shape[1]
+    k = w.shape[2] * 2
+    P = out.shape[0]
+    _need(workspace, torch.uint8, None, "workspace")
+    _need(offsets, torch.int32, (E + 1,), "offsets")
+    _need(w, torch.uint8, (E, n, k // 2), "w")
+    _need(wscale, torch.uint8, (E, n, k // group_size(recipe)), "wscale")
+    if scale2 is not None:
+        _need(scale2, torch.float32, (E,), "scale2")
+    _need(out, torch.float32, (P, n), "out")
+    _check(lib().fp4_grouped_gemm_quantized(_ptr(workspace), workspace.numel(), _ptr(offsets), E,
+                                            P, _ptr(w), _ptr(wscale), _ptr(scale2), int(recipe),
+                                            _ptr(out), n, k, _stream(stream)),
+           "fp4_grouped_gemm_quantized")
+    return out
+
+
+def fp4_grouped_expert_gemm_noalloc(x, row_ids, offsets, w, wscale, scale2, recipe, out,
                                     stream=None):
     """As fp4_grouped_expert_gemm, for callers that cannot allocate device memory: runs the
-    tensor-core path with the library's fixed 32 MiB scratch (total_rows*k*2+1024 bytes at
-    most) instead of a workspace. Calls that overlap on the GPU race on that scratch."""
+    tensor-core path with the library's fixed 32 MiB scratch instead of a workspace (the call
+    needs fp4_grouped_workspace_size(...) bytes of it). `out` is required: this binding
+    allocates nothing either. Calls that overlap on the GPU race on that scratch."""
     import torch
     T, k = x.shape
     E, n = w.shape[0], w.shape[1]
@@ -216,7 +270,7 @@ def fp4_grouped_expert_gemm_noalloc(x, row_ids, offsets, w, wscale, scale2, reci
     if scale2 is not None:
         _need(scale2, torch.float32, (E,), "scale2")
     if out is None:
-        out = torch.empty((P, n), dtype=torch.float32, device=x.device)
+        raise ValueError("fp4_grouped_expert_gemm_noalloc needs a caller-owned `out`")
     _need(out, torch.float32, (P, n), "out")
     _check(lib().fp4_grouped_expert_gemm_noalloc(_ptr(x), T, _ptr(row_ids), _ptr(offsets), E, P,
                                                  _ptr(w), _ptr(wscale), _ptr(scale2), int(recipe),
@@ -274,6 +328,67 @@ def fp4_swiglu_quant(gate, up, limit, want_h=False, codes=None, scales=None, h_o
                                   _ptr(h_out), _ptr(codes), _ptr(scales), _stream(stream)),
            "fp4_swiglu_quant")
     return codes, scales, h_out
+
+
+def fp4_route_topk(logits, topk, renormalize=False, ids=None, weights=None, stream=None):
+    """Router: logits [T, E] f32 -> (ids [T, topk] int32, weights [T, topk] f32): the topk
+    largest logits per token (ties: lower expert id), best first; softmax weights over all
+    experts, or over the selected ones with renormalize."""
+    import torch
+    T, E = logits.shape
+    _need(logits, torch.float32, None, "logits")
+    if ids is None:
+        ids = torch.empty((T, topk), dtype=torch.int32, device=logits.device)
+    if weights is None:
+        weights = torch.empty((T, topk), dtype=torch.float32, device=logits.device)
+    _need(ids, torch.int32, (T, topk), "ids")
+    _need(weights, torch.float32, (T, topk), "weights")
+    _check(lib().fp4_route_topk(_ptr(logits), T, E, int(topk), 1 if renormalize else 0, _ptr(ids),
+                                _ptr(weights), _stream(stream)), "fp4_route_topk")
+    return ids, weights
+
+
+def fp4_route_csr(ids, num_experts, workspace=None, offsets=None, row_ids=None, pair_rows=None,
+                  stream=None):
+    """CSR routing from expert ids [T, topk] int32: (offsets [E+1], row_ids [T*topk],
+    pair_rows [T, topk]), routed rows grouped by expert in token order."""
+    import torch
+    T, topk = ids.shape
+    _need(ids, torch.int32, None, "ids")
+    dev = ids.device
+    if workspace is None:
+        nbytes = int(lib().fp4_route_csr_workspace_size(T, int(num_experts)))
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    if offsets is None:
+        offsets = torch.empty(num_experts + 1, dtype=torch.int32, device=dev)
+    if row_ids is None:
+        row_ids = torch.empty(T * topk, dtype=torch.int32, device=dev)
+    if pair_rows is None:
+        pair_rows = torch.empty((T, topk), dtype=torch.int32, device=dev)
+    _need(offsets, torch.int32, (num_experts + 1,), "offsets")
+    _need(row_ids, torch.int32, (T * topk,), "row_ids")
+    _need(pair_rows, torch.int32, (T, topk), "pair_rows")
+    _need(workspace, torch.uint8, None, "workspace")
+    _check(lib().fp4_route_csr(_ptr(ids), T, topk, int(num_experts), _ptr(offsets), _ptr(row_ids),
+                               _ptr(pair_rows), _ptr(workspace), workspace.numel(),
+                               _stream(stream)), "fp4_route_csr")
+    return offsets, row_ids, pair_rows
+
+
+def fp4_moe_combine(out, pair_rows, weights, y=None, stream=None):
+    """y [T, n] = per token, sum over its slots j of weights[t, j] * out[pair_rows[t, j]]."""
+    import torch
+    P, n = out.shape
+    T, topk = pair_rows.shape
+    _need(out, torch.float32, None, "out")
+    _need(pair_rows, torch.int32, None, "pair_rows")
+    _need(weights, torch.float32, (T, topk), "weights")
+    if y is None:
+        y = torch.empty((T, n), dtype=torch.float32, device=out.device)
+    _need(y, torch.float32, (T, n), "y")
+    _check(lib().fp4_moe_combine(_ptr(out), P, _ptr(pair_rows), _ptr(weights), T, int(topk), n,
+                                 _ptr(y), _stream(stream)), "fp4_moe_combine")
+    return y
 
 
 def fp4_gemm_path(total_rows, num_experts, n, k, recipe, have_workspace=True):

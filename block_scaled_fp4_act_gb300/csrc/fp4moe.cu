@@ -1,7 +1,6 @@
 // fp4moe.cu -- the exported C ABI (include/fp4moe.h): argument checks, path choice,
 // kernel launches and the per-device error word. No allocation, no synchronisation in
 // the compute calls.
-#include <atomic>
 #include <stdio.h>
 #include <string.h>
 
@@ -29,10 +28,12 @@ unsigned *device_error_word()
 int stream_max_rows_per_pass(int k);
 size_t tc_workspace_bytes(int64_t total_rows, int64_t k, int recipe);
 bool tc_supported(int64_t n, int64_t k, int recipe, int E);
-cudaError_t launch_tc_gemm(const GroupedProblem &p, void *workspace, cudaStream_t s);
+cudaError_t launch_tc_quantize(const GroupedProblem &p, void *workspace, cudaStream_t s);
+cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaStream_t s);
 double tc_error_ops(int recipe, int64_t k);
 
-static std::atomic<int> g_forced_path{FP4_PATH_AUTO};
+// Path forced by fp4_force_path for calls made on the same host thread.
+static thread_local int g_forced_path = FP4_PATH_AUTO;
 static thread_local char g_last_error[256] = "";
 
 static int record(cudaError_t e)
@@ -70,7 +71,7 @@ constexpr int64_t kTcMinRowsPerExpert = 8;
 
 static int choose_path(int64_t P, int E, int64_t n, int64_t k, int recipe, bool have_ws)
 {
-    const int forced = g_forced_path.load();
+    const int forced = g_forced_path;
     if (forced != FP4_PATH_AUTO)
         return forced;
     if (have_ws && tc_supported(n, k, recipe, E) && P >= kTcMinRowsPerExpert * (int64_t)E)
@@ -116,6 +117,14 @@ static int run_grouped(GroupedProblem p, void *workspace, size_t ws_bytes, cudaS
             return FP4_ERR_SHAPE;
         if (!have_ws)
             return FP4_ERR_WORKSPACE;
+        if (p.codes_out) {  // the codes are not a by-product of the quantise pass: one act_quant
+            const int st = record(launch_act_quant(p.x, p.codes_out, p.scales_out, p.P, p.k, s));
+            if (st != FP4_OK)
+                return st;
+        }
+        const int st = record(launch_tc_quantize(p, workspace, s));
+        if (st != FP4_OK)
+            return st;
         return record(launch_tc_gemm(p, workspace, s));
     }
     return record(launch_streaming(p, s));
@@ -213,13 +222,6 @@ int fp4_expert_gemm(const float *x, const uint8_t *w, const uint8_t *wscale, flo
     p.k = (int)k;
     p.codes_out = codes_out;
     p.scales_out = scales_out;
-    if (codes_out) {
-        // The quantised activations are a by-product of the streaming path's prologue.
-        p.err = device_error_word();
-        if (!p.err)
-            return record(cudaErrorInvalidDevice);
-        return record(launch_streaming(p, (cudaStream_t)stream));
-    }
     return run_grouped(p, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
@@ -273,6 +275,156 @@ int fp4_grouped_expert_gemm(const float *x, int64_t num_tokens, const int32_t *r
     return run_grouped(p, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
+// Shared checks of the two halves of the tensor-core path.
+static int check_tc_call(int recipe, int64_t total_rows, int64_t n, int64_t k, const void *ws,
+                         size_t ws_bytes)
+{
+    if (!recipe_ok(recipe))
+        return FP4_ERR_ARG;
+    const int st = check_shape(total_rows, n, k);
+    if (st != FP4_OK)
+        return st;
+    if (!tc_supported(n, k, recipe, 1))
+        return FP4_ERR_SHAPE;
+    if (total_rows > 0 && (!ws || ws_bytes < tc_workspace_bytes(total_rows, k, recipe)))
+        return FP4_ERR_WORKSPACE;
+    return FP4_OK;
+}
+
+int fp4_grouped_quantize(const float *x, int64_t num_tokens, const int32_t *row_ids,
+                         int64_t total_rows, int64_t k, int recipe, void *workspace,
+                         size_t workspace_bytes, void *stream)
+{
+    if (num_tokens < 0)
+        return FP4_ERR_ARG;
+    int st = check_tc_call(recipe, total_rows, 128, k, workspace, workspace_bytes);
+    if (st != FP4_OK)
+        return st;
+    if (total_rows == 0)
+        return FP4_OK;
+    if (!x)
+        return FP4_ERR_ARG;
+    if (!row_ids && num_tokens < total_rows)
+        return FP4_ERR_SHAPE;
+    if (!aligned16(x))
+        return FP4_ERR_ALIGN;
+    GroupedProblem p{};
+    p.x = x;
+    p.T = num_tokens;
+    p.row_ids = row_ids;
+    p.E = 1;
+    p.P = total_rows;
+    p.recipe = recipe;
+    p.n = 128;
+    p.k = (int)k;
+    p.err = device_error_word();
+    if (!p.err)
+        return record(cudaErrorInvalidDevice);
+    return record(launch_tc_quantize(p, workspace, (cudaStream_t)stream));
+}
+
+int fp4_grouped_gemm_quantized(const void *workspace, size_t workspace_bytes,
+                               const int32_t *offsets, int num_experts, int64_t total_rows,
+                               const uint8_t *w, const uint8_t *wscale, const float *scale2,
+                               int recipe, float *out, int64_t n, int64_t k, void *stream)
+{
+    if (num_experts < 1 || num_experts > 65535)
+        return FP4_ERR_ARG;
+    int st = check_tc_call(recipe, total_rows, n, k, workspace, workspace_bytes);
+    if (st != FP4_OK)
+        return st;
+    if (!tc_supported(n, k, recipe, num_experts))
+        return FP4_ERR_SHAPE;
+    if (total_rows == 0)
+        return FP4_OK;
+    if (!offsets || !w || !wscale || !out || (recipe == FP4_NVFP4 && !scale2))
+        return FP4_ERR_ARG;
+    if (!aligned16(w) || !aligned16(wscale) || !aligned16(out))
+        return FP4_ERR_ALIGN;
+    GroupedProblem p{};
+    p.offsets = offsets;
+    p.E = num_experts;
+    p.P = total_rows;
+    p.w = w;
+    p.sc = wscale;
+    p.scale2 = recipe == FP4_NVFP4 ? scale2 : nullptr;
+    p.scale2_host = 1.0f;
+    p.recipe = recipe;
+    p.out = out;
+    p.n = (int)n;
+    p.k = (int)k;
+    p.err = device_error_word();
+    if (!p.err)
+        return record(cudaErrorInvalidDevice);
+    return record(launch_tc_gemm(p, workspace, (cudaStream_t)stream));
+}
+
+int fp4_route_topk(const float *logits, int64_t num_tokens, int num_experts, int topk,
+                   int renormalize, int32_t *ids, float *weights, void *stream)
+{
+    if (num_tokens < 0 || num_experts < 1 || topk < 1)
+        return FP4_ERR_ARG;
+    if (num_experts > 1024 || topk > 32 || topk > num_experts)
+        return FP4_ERR_SHAPE;
+    if (num_tokens == 0)
+        return FP4_OK;
+    if (!logits || !ids || !weights)
+        return FP4_ERR_ARG;
+    if (!aligned16(logits) || !aligned16(ids) || !aligned16(weights))
+        return FP4_ERR_ALIGN;
+    return record(launch_route_topk(logits, num_tokens, num_experts, topk, renormalize, ids,
+                                    weights, (cudaStream_t)stream));
+}
+
+size_t fp4_route_csr_workspace_size(int64_t num_tokens, int num_experts)
+{
+    if (num_tokens < 0 || num_experts < 1)
+        return 0;
+    return route_csr_workspace_bytes(num_tokens, num_experts);
+}
+
+int fp4_route_csr(const int32_t *ids, int64_t num_tokens, int topk, int num_experts,
+                  int32_t *offsets, int32_t *row_ids, int32_t *pair_rows, void *workspace,
+                  size_t workspace_bytes, void *stream)
+{
+    if (num_tokens < 0 || topk < 1 || num_experts < 1 || num_experts > 65535)
+        return FP4_ERR_ARG;
+    if (num_tokens * (int64_t)topk > ((int64_t)1 << 31) - 1)
+        return FP4_ERR_SHAPE;
+    if (!offsets || !workspace || (num_tokens > 0 && (!ids || !row_ids)))
+        return FP4_ERR_ARG;
+    if (workspace_bytes < route_csr_workspace_bytes(num_tokens, num_experts))
+        return FP4_ERR_WORKSPACE;
+    if (!aligned16(workspace))
+        return FP4_ERR_ALIGN;
+    unsigned *err = device_error_word();
+    if (!err)
+        return record(cudaErrorInvalidDevice);
+    return record(launch_route_csr(ids, num_tokens, topk, num_experts, offsets, row_ids,
+                                   pair_rows, workspace, err, (cudaStream_t)stream));
+}
+
+int fp4_moe_combine(const float *out, int64_t total_rows, const int32_t *pair_rows,
+                    const float *weights, int64_t num_tokens, int topk, int64_t n, float *y,
+                    void *stream)
+{
+    if (total_rows < 0 || num_tokens < 0 || topk < 1 || n < 0)
+        return FP4_ERR_ARG;
+    if (n == 0 || n % 4 != 0 || topk > 1024)
+        return FP4_ERR_SHAPE;
+    if (num_tokens == 0)
+        return FP4_OK;
+    if (!out || !pair_rows || !weights || !y)
+        return FP4_ERR_ARG;
+    if (!aligned16(out) || !aligned16(y))
+        return FP4_ERR_ALIGN;
+    unsigned *err = device_error_word();
+    if (!err)
+        return record(cudaErrorInvalidDevice);
+    return record(launch_moe_combine(out, pair_rows, weights, num_tokens, topk, n, total_rows, y,
+                                     err, (cudaStream_t)stream));
+}
+
 int fp4_gemm_path(int64_t total_rows, int num_experts, int64_t n, int64_t k, int recipe,
                   int have_workspace)
 {
@@ -288,7 +440,7 @@ double fp4_error_ops(int path, int recipe, int64_t k)
 
 void fp4_force_path(int path)
 {
-    g_forced_path.store(path == FP4_PATH_STREAM || path == FP4_PATH_TC ? path : FP4_PATH_AUTO);
+    g_forced_path = path == FP4_PATH_STREAM || path == FP4_PATH_TC ? path : FP4_PATH_AUTO;
 }
 
 int fp4_get_device_error(void *stream, unsigned *bits)

@@ -798,127 +798,152 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ quantise pass
 
-// Routed row p of the workspace = bf16(e4m3 code * scale) of activation row x[row_ids[p]]
-// (fn quant_rows of dsv4_native_gemm_gate.rs; bf16 holds code * 2^m exactly). With
-// only_if set, the kernel runs only when *only_if is nonzero (the f16 quantise pass found a
-// row whose block scales span more than f16 can hold exactly) and then replaces the whole
-// f16 workspace by bf16.
-__global__ void __launch_bounds__(256) quant_ws_kernel(const float *__restrict__ x, int64_t T,
-                                                       const int32_t *__restrict__ row_ids,
-                                                       int64_t P, int k,
-                                                       uint2 *__restrict__ ws, unsigned *err,
-                                                       const unsigned *only_if)
-{
-    if (only_if && *((volatile const unsigned *)only_if) == 0u)
-        return;
-    const int lane = threadIdx.x & 31;
-    const int kq = k >> 7;
-    const int64_t groups = P * kq;
-    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t gi = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); gi < groups;
-         gi += warps) {
-        const int64_t pr = gi / kq;
-        const int g = (int)(gi - pr * kq);
-        const int64_t t = row_ids ? (int64_t)__ldg(row_ids + pr) : pr;
-        uint2 o = make_uint2(0u, 0u);
-        if (t >= 0 && t < T) {
-            const float4 v = __ldg(reinterpret_cast<const float4 *>(x + t * k + g * 128) + lane);
-            float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-            amax = warp_max(amax);
-            const float s = group_scale(amax);
-            const float inv = pow2_reciprocal(s);
-            const uint32_t q = e4m3x4(scaled_clamped(v.x, inv), scaled_clamped(v.y, inv),
-                                      scaled_clamped(v.z, inv), scaled_clamped(v.w, inv));
-            const float2 lo = f16x2_to_f32x2(e4m3x2_to_f16x2(q & 0xFFFFu));
-            const float2 hi = f16x2_to_f32x2(e4m3x2_to_f16x2(q >> 16));
-            o.x = pack_bf16x2(lo.x * s, lo.y * s);
-            o.y = pack_bf16x2(hi.x * s, hi.y * s);
-        } else if (lane == 0 && g == 0) {
-            raise_device_error(err, FP4_DEVERR_ROW_ID);
-        }
-        ws[(pr * k + g * 128) / 4 + lane] = o;
-    }
-}
-
 // Largest exponent gap between a row's block scales that f16 still holds exactly: codes
 // are multiples of 2^-9, so code * 2^-15 is a multiple of 2^-24, f16's finest spacing.
 constexpr int kF16MaxScaleGap = 15;
+// 128-groups a warp of the quantise pass holds in registers (rows up to k = 8 * 8 * 128).
+constexpr int kQuantRegGroups = 8;
 
-// f16 quantise pass (NVFP4): one CTA (8 warps) per routed row. Pass 1 finds the row's
-// block scales 2^m_b (warps split the 128-groups) and, through shared memory, their
-// largest exponent M_p; pass 2 (re-reading the row from L1) writes f16(code * 2^(m_b - M_p))
-// (exact when every m_b >= M_p - 15) and rowscale[p] = 2^M_p, which the GEMM epilogue
-// applies per routed row. A row with a wider gap sets *route_flag; the bf16 pass then
-// rewrites the whole workspace.
-__global__ void __launch_bounds__(256) quant_ws_f16_kernel(const float *__restrict__ x, int64_t T,
-                                                           const int32_t *__restrict__ row_ids,
-                                                           int64_t P, int k,
-                                                           uint2 *__restrict__ ws,
-                                                           float *__restrict__ rowscale,
-                                                           unsigned *route_flag, unsigned *err)
+// act_quant of one 128-group held as a float4 per lane (fn quant_rows of
+// dsv4_native_gemm_gate.rs): returns the group scale 2^m (shuffle max, floor 1e-4, times
+// f32(1/448), pow2_ceil) and this lane's four e4m3 codes, packed.
+__device__ __forceinline__ float quant_group4(const float4 v, uint32_t &q)
 {
-    extern __shared__ uint32_t sexp[];  // [k/128] biased exponent of each block scale
+    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    amax = warp_max(amax);
+    const float s = group_scale(amax);
+    const float inv = pow2_reciprocal(s);
+    q = e4m3x4(scaled_clamped(v.x, inv), scaled_clamped(v.y, inv), scaled_clamped(v.z, inv),
+               scaled_clamped(v.w, inv));
+    return s;
+}
+
+// The 16-bit MMA operands of four packed codes: f16(code * mul) with mul = 2^(m - M) in
+// [2^-15, 1] (f16 route), or bf16(code * 2^m) (bf16 route). Both exact.
+__device__ __forceinline__ uint2 ws_word(uint32_t q, float mul, bool f16)
+{
+    const float2 lo = f16x2_to_f32x2(e4m3x2_to_f16x2(q & 0xFFFFu));
+    const float2 hi = f16x2_to_f32x2(e4m3x2_to_f16x2(q >> 16));
+    uint2 o;
+    if (f16) {
+        o.x = pack_f16x2(lo.x * mul, lo.y * mul);
+        o.y = pack_f16x2(hi.x * mul, hi.y * mul);
+    } else {
+        o.x = pack_bf16x2(lo.x * mul, lo.y * mul);
+        o.y = pack_bf16x2(hi.x * mul, hi.y * mul);
+    }
+    return o;
+}
+
+// Quantise pass: routed row p of the workspace = the 16-bit MMA operand of act_quant of
+// activation row x[row_ids[p]] (x[p] without row ids), in one of two forms:
+//   f16 route (NVFP4): f16(code * 2^(m_b - M_p)) and rowscale[p] = 2^M_p, M_p the row's
+//       largest block exponent; exact while every block lies within 2^15 of M_p. A row
+//       with a wider spread sets *route_flag and is not written: the bf16 pass then
+//       rewrites every row (the GEMM takes one operand type per call).
+//   bf16 route (MXFP4, and the f16 route's fallback): bf16(code * 2^m_b), always exact.
+// A CTA of 8 warps takes 8 / wr rows at a time; the wr warps of a row split its 128-groups
+// (warp i of the row takes groups i, i + wr, ...). With REG (at most kQuantRegGroups
+// groups per warp) the row stays in registers between the scale reduction and the
+// writes, so it is read once; otherwise (k above 8192) the f16 route reads it twice.
+// Rows whose id is outside [0, T) are written as zeros and raise FP4_DEVERR_ROW_ID.
+// With only_if set, the kernel runs only when *only_if is nonzero.
+template <bool REG>
+__global__ void __launch_bounds__(256, 3) quant_ws_kernel(const float *__restrict__ x, int64_t T,
+                                                       const int32_t *__restrict__ row_ids,
+                                                       int64_t P, int k, int wr, int f16_route,
+                                                       uint2 *__restrict__ ws,
+                                                       float *__restrict__ rowscale,
+                                                       unsigned *route_flag,
+                                                       const unsigned *only_if, unsigned *err)
+{
+    if (only_if && *((volatile const unsigned *)only_if) == 0u)
+        return;
     __shared__ uint32_t red[2][8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kq = k >> 7;
-    for (int64_t pr = blockIdx.x; pr < P; pr += gridDim.x) {
-        const int64_t t = row_ids ? (int64_t)__ldg(row_ids + pr) : pr;
-        if (t < 0 || t >= T) {  // uniform over the CTA
-            if (threadIdx.x == 0) {
-                raise_device_error(err, FP4_DEVERR_ROW_ID);
-                rowscale[pr] = 1.0f;
-            }
-            for (int g = warp; g < kq; g += 8)
-                ws[(pr * k + g * 128) / 4 + lane] = make_uint2(0u, 0u);
-            continue;
-        }
-        const float4 *xr = reinterpret_cast<const float4 *>(x + t * k);
+    const int rpc = 8 / wr;
+    const int slot = warp / wr, wi = warp - slot * wr;
+    const bool f16 = f16_route != 0;
+    for (int64_t base = (int64_t)blockIdx.x * rpc; base < P; base += (int64_t)gridDim.x * rpc) {
+        const int64_t pr = base + slot;
+        const bool have = pr < P;
+        const int64_t t = have ? (row_ids ? (int64_t)__ldg(row_ids + pr) : pr) : -1;
+        const bool valid = t >= 0 && t < T;
+        if (have && !valid && wi == 0 && lane == 0)
+            raise_device_error(err, FP4_DEVERR_ROW_ID);
+        const float4 *xr = reinterpret_cast<const float4 *>(x + (valid ? t : 0) * (int64_t)k);
+        uint2 *wrow = ws + pr * (int64_t)(k / 4);
+        const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
         uint32_t emax = 0u, emin = 255u;
-        for (int g = warp; g < kq; g += 8) {
-            const float4 v = __ldg(xr + g * 32 + lane);
-            float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-            amax = warp_max(amax);
-            const uint32_t e = __float_as_uint(group_scale(amax)) >> 23;
-            if (lane == 0)
-                sexp[g] = e;
-            emax = max(emax, e);
-            emin = min(emin, e);
-        }
-        if (lane == 0) {
-            red[0][warp] = emax;
-            red[1][warp] = emin;
-        }
-        __syncthreads();
+        uint32_t c[kQuantRegGroups];
+        float s[kQuantRegGroups];
+        if (REG) {
+            float4 v[kQuantRegGroups];
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            emax = max(emax, red[0][w]);
-            emin = min(emin, red[1][w]);
-        }
-        const bool wide = emin + kF16MaxScaleGap < emax;
-        if (wide) {
-            if (threadIdx.x == 0)
-                atomicOr(route_flag, 1u);  // the bf16 pass rewrites every row
-        } else {
-            if (threadIdx.x == 0)
-                rowscale[pr] = __uint_as_float(emax << 23);
-            for (int g = warp; g < kq; g += 8) {
-                const float4 v = __ldg(xr + g * 32 + lane);
-                const uint32_t e = sexp[g];
-                const float sc = __uint_as_float(e << 23);
-                const float inv = pow2_reciprocal(sc);
-                const uint32_t q = e4m3x4(scaled_clamped(v.x, inv), scaled_clamped(v.y, inv),
-                                          scaled_clamped(v.z, inv), scaled_clamped(v.w, inv));
-                // 2^(m_b - M_p) in [2^-15, 1], exact in f32
-                const float rel = __uint_as_float((e + 127u - emax) << 23);
-                const float2 lo = f16x2_to_f32x2(e4m3x2_to_f16x2(q & 0xFFFFu));
-                const float2 hi = f16x2_to_f32x2(e4m3x2_to_f16x2(q >> 16));
-                uint2 o;
-                o.x = pack_f16x2(lo.x * rel, lo.y * rel);
-                o.y = pack_f16x2(hi.x * rel, hi.y * rel);
-                ws[(pr * k + g * 128) / 4 + lane] = o;
+            for (int i = 0; i < kQuantRegGroups; ++i) {
+                const int g = wi + i * wr;
+                v[i] = (valid && g < kq) ? __ldg(xr + g * 32 + lane) : zero;
+            }
+#pragma unroll
+            for (int i = 0; i < kQuantRegGroups; ++i) {
+                if (wi + i * wr < kq) {  // uniform over the warp
+                    s[i] = quant_group4(v[i], c[i]);
+                    const uint32_t e = __float_as_uint(s[i]) >> 23;
+                    emax = max(emax, e);
+                    emin = min(emin, e);
+                }
+            }
+        } else if (f16) {
+            for (int g = wi; g < kq; g += wr) {
+                uint32_t cc;
+                const uint32_t e =
+                    __float_as_uint(quant_group4(valid ? __ldg(xr + g * 32 + lane) : zero, cc)) >> 23;
+                emax = max(emax, e);
+                emin = min(emin, e);
             }
         }
-        __syncthreads();  // sexp and red are reused by the next row
+        if (f16) {  // the row's largest and smallest block exponent, over its wr warps
+            if (lane == 0) {
+                red[0][warp] = emax;
+                red[1][warp] = emin;
+            }
+            __syncthreads();
+            for (int j = 0; j < wr; ++j) {
+                emax = max(emax, red[0][slot * wr + j]);
+                emin = min(emin, red[1][slot * wr + j]);
+            }
+        }
+        const bool wide = f16 && emin + kF16MaxScaleGap < emax;
+        if (have && wide && wi == 0 && lane == 0)
+            atomicOr(route_flag, 1u);
+        if (have && !wide) {
+            if (f16 && wi == 0 && lane == 0)
+                rowscale[pr] = __uint_as_float(emax << 23);
+            if (REG) {
+#pragma unroll
+                for (int i = 0; i < kQuantRegGroups; ++i) {
+                    const int g = wi + i * wr;
+                    if (g < kq) {
+                        // 2^(m - M) in [2^-15, 1] (f16 route), or the group scale (bf16)
+                        const float mul =
+                            f16 ? __uint_as_float(((__float_as_uint(s[i]) >> 23) + 127u - emax) << 23)
+                                : s[i];
+                        wrow[g * 32 + lane] = ws_word(c[i], mul, f16);
+                    }
+                }
+            } else {
+                for (int g = wi; g < kq; g += wr) {
+                    uint32_t cc;
+                    const float sg = quant_group4(valid ? __ldg(xr + g * 32 + lane) : zero, cc);
+                    const float mul =
+                        f16 ? __uint_as_float(((__float_as_uint(sg) >> 23) + 127u - emax) << 23) : sg;
+                    wrow[g * 32 + lane] = ws_word(cc, mul, f16);
+                }
+            }
+        }
+        if (f16)
+            __syncthreads();  // red[] is rewritten by the next rows
     }
 }
 
@@ -964,62 +989,95 @@ bool tc_supported(int64_t n, int64_t k, int recipe, int E)
     return n >= 1;
 }
 
-cudaError_t launch_tc_gemm(const GroupedProblem &p, void *workspace, cudaStream_t s)
+// Multiprocessor count of the current device, looked up once per device.
+static int device_sms()
+{
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 152;
+    if (cached[dev] == 0) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+            sms = 152;
+        cached[dev] = sms;
+    }
+    return cached[dev];
+}
+
+// Where the parts of a workspace live (1024-aligned start, as the TMA tiles need).
+struct WsLayout {
+    uint8_t *act;         // [P, k] 16-bit MMA operands
+    float *rowscale;      // [P] f32 (f16 route)
+    unsigned *route_flag; // nonzero: the bf16 route holds
+};
+
+static WsLayout ws_layout(const void *workspace, int64_t P, int64_t k)
+{
+    WsLayout l;
+    l.act = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(workspace) + 1023) &
+                                        ~(uintptr_t)1023);
+    l.rowscale = reinterpret_cast<float *>(l.act + ws_act_bytes(P, k));
+    l.route_flag = reinterpret_cast<unsigned *>(l.rowscale + P);
+    return l;
+}
+
+// Quantise pass of the tensor-core path: every routed row into the workspace. NVFP4 first
+// tries f16 with a per-row power-of-two scale (the cheaper weight conversion in the GEMM);
+// if any row's block scales span more than f16 holds exactly, the bf16 pass rewrites all
+// rows. MXFP4 weights times 2^(e-127) need bf16's range, so MXFP4 always takes bf16.
+cudaError_t launch_tc_quantize(const GroupedProblem &p, void *workspace, cudaStream_t s)
+{
+    using namespace tc;
+    const WsLayout l = ws_layout(workspace, p.P, p.k);
+    const int sms = device_sms();
+    const bool nvfp4 = p.recipe == FP4_NVFP4;
+    const int kq = p.k / 128;
+    // warps per row: enough that each holds at most kQuantRegGroups groups, a power of two <= 8
+    int wr = 1;
+    while (wr < 8 && (kq + wr - 1) / wr > kQuantRegGroups)
+        wr <<= 1;
+    const bool reg = (kq + wr - 1) / wr <= kQuantRegGroups;
+    const int64_t rpc = 8 / wr;
+    const int64_t want = (p.P + rpc - 1) / rpc;
+    const int blocks = (int)(want < (int64_t)sms * 3 ? want : (int64_t)sms * 3);  // 3 CTAs per SM
+    uint2 *ws = reinterpret_cast<uint2 *>(l.act);
+    auto kern = reg ? quant_ws_kernel<true> : quant_ws_kernel<false>;
+    if (nvfp4) {
+        cudaError_t e = cudaMemsetAsync(l.route_flag, 0, sizeof(unsigned), s);
+        if (e != cudaSuccess)
+            return e;
+        kern<<<blocks, 256, 0, s>>>(p.x, p.T, p.row_ids, p.P, p.k, wr, 1, ws, l.rowscale,
+                                    l.route_flag, nullptr, p.err);
+        // the bf16 fallback: exits at once unless a row was too wide for f16
+        const int fb = 2 * sms < blocks ? 2 * sms : blocks;
+        kern<<<fb, 256, 0, s>>>(p.x, p.T, p.row_ids, p.P, p.k, wr, 0, ws, l.rowscale, nullptr,
+                                l.route_flag, p.err);
+    } else {
+        kern<<<blocks, 256, 0, s>>>(p.x, p.T, p.row_ids, p.P, p.k, wr, 0, ws, l.rowscale, nullptr,
+                                    nullptr, p.err);
+    }
+    return cudaGetLastError();
+}
+
+// The persistent tensor-core GEMM over a workspace that launch_tc_quantize filled for the
+// same routed rows, k and recipe.
+cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaStream_t s)
 {
     using namespace tc;
     if (!tc_supported(p.n, p.k, p.recipe, p.E))
         return cudaErrorInvalidValue;
-    uint8_t *ws = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(workspace) + 1023) & ~(uintptr_t)1023);
-    int dev = 0, sms = 152;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-
-    float *rowscale = reinterpret_cast<float *>(ws + ws_act_bytes(p.P, p.k));
-    unsigned *route_flag = reinterpret_cast<unsigned *>(rowscale + p.P);
+    const WsLayout l = ws_layout(workspace, p.P, p.k);
+    const int sms = device_sms();
     const bool nvfp4 = p.recipe == FP4_NVFP4;
-
-    // 1. quantise the routed rows into the workspace [P, k]: NVFP4 first tries f16 with a
-    //    per-row power-of-two scale (cheaper weight conversion in the GEMM); if any row's
-    //    block scales span more than f16 holds exactly, the bf16 pass rewrites all rows.
-    //    MXFP4 weights times 2^(e-127) need bf16's range, so MXFP4 always takes bf16.
-    {
-        const int64_t groups = p.P * (p.k / 128);
-        const int64_t want = (groups + 7) / 8;
-        const int blocks = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
-        if (nvfp4) {
-            cudaError_t e = cudaMemsetAsync(route_flag, 0, sizeof(unsigned), s);
-            if (e != cudaSuccess)
-                return e;
-            const int rblocks = (int)(p.P < (int64_t)sms * 8 ? p.P : (int64_t)sms * 8);
-            const size_t qsmem = (size_t)(p.k / 128) * sizeof(uint32_t);
-            if (qsmem > 48 * 1024) {
-                e = cudaFuncSetAttribute(quant_ws_f16_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)qsmem);
-                if (e != cudaSuccess)
-                    return e;
-            }
-            quant_ws_f16_kernel<<<rblocks, 256, qsmem, s>>>(p.x, p.T, p.row_ids, p.P, p.k,
-                                                       reinterpret_cast<uint2 *>(ws), rowscale,
-                                                       route_flag, p.err);
-        }
-        quant_ws_kernel<<<blocks, 256, 0, s>>>(p.x, p.T, p.row_ids, p.P, p.k,
-                                              reinterpret_cast<uint2 *>(ws), p.err,
-                                              nvfp4 ? route_flag : nullptr);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess)
-            return e;
-    }
-    // 2. tensor maps and the persistent GEMM
-    const int gs = p.recipe == FP4_NVFP4 ? 16 : 32;
+    const int gs = nvfp4 ? 16 : 32;
     alignas(64) BMaps tmB;
     alignas(64) CUtensorMap tmW, tmS;
     for (int i = 0; i < 4; ++i)
-        if (!make_map_kblocks(&tmB.m[i], ws, (uint64_t)p.k, (uint64_t)p.P, (uint32_t)bmap_rows(i),
-                              (uint32_t)bmap_kblocks(i)))
+        if (!make_map_kblocks(&tmB.m[i], l.act, (uint64_t)p.k, (uint64_t)p.P,
+                              (uint32_t)bmap_rows(i), (uint32_t)bmap_kblocks(i)))
             return cudaErrorInvalidValue;
-    if (
-        !make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w, (uint64_t)p.k / 2,
+    if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w, (uint64_t)p.k / 2,
                   (uint64_t)p.E * p.n, BK / 2, BM, CU_TENSOR_MAP_SWIZZLE_32B) ||
         !make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sc, (uint64_t)p.k / gs,
                   (uint64_t)p.E * p.n, 16, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -1034,14 +1092,21 @@ cudaError_t launch_tc_gemm(const GroupedProblem &p, void *workspace, cudaStream_
     kp.mt = (p.n + BM - 1) / BM;
     kp.scale2 = p.scale2;
     kp.scale2_host = p.scale2_host;
-    kp.route_flag = nvfp4 ? route_flag : nullptr;
-    kp.rowscale = rowscale;
+    kp.route_flag = nvfp4 ? l.route_flag : nullptr;
+    kp.rowscale = l.rowscale;
     kp.out = p.out;
     kp.err = p.err;
-    cudaError_t e =
-        cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess)
-        return e;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess)
+            return e;
+        if (dev >= 0 && dev < 64)
+            attr_set[dev] = true;
+    }
     const int64_t max_tiles = ((p.P + BN - 1) / BN + p.E) * (int64_t)kp.mt;
     const int grid = (int)(max_tiles < sms ? max_tiles : sms);
     tc_gemm_kernel<<<grid, kThreads, SMEM_BYTES, s>>>(tmB, tmW, tmS, kp);
@@ -1132,8 +1197,9 @@ extern "C" int fp4_grouped_expert_gemm_noalloc(const float *x, int64_t num_token
     if (need > kNoAllocScratchBytes) {
         char msg[256];
         snprintf(msg, sizeof(msg),
-                 "fp4_grouped_expert_gemm_noalloc: total_rows*k*2+1024 = %zu bytes exceeds the "
-                 "fixed %zu-byte scratch",
+                 "fp4_grouped_expert_gemm_noalloc: the call needs %zu bytes of scratch "
+                 "(1024 + roundup(total_rows*k*2, 1024) + 4*total_rows + 16), the fixed "
+                 "scratch holds %zu",
                  need, kNoAllocScratchBytes);
         set_last_error(msg);
         return FP4_ERR_WORKSPACE;
@@ -1166,7 +1232,9 @@ extern "C" int fp4_grouped_expert_gemm_noalloc(const float *x, int64_t num_token
     p.err = device_error_word();
     if (!p.err)
         return FP4_ERR_LAUNCH;
-    const cudaError_t e = launch_tc_gemm(p, scratch, (cudaStream_t)stream);
+    cudaError_t e = launch_tc_quantize(p, scratch, (cudaStream_t)stream);
+    if (e == cudaSuccess)
+        e = launch_tc_gemm(p, scratch, (cudaStream_t)stream);
     if (e != cudaSuccess) {
         char msg[256];
         snprintf(msg, sizeof(msg), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));

@@ -49,6 +49,17 @@ cudaError_t launch_stream_gemm(const GroupedProblem &p, int rows_per_pass, cudaS
 cudaError_t launch_decode_gemm(const GroupedProblem &p, int rows_per_pass, cudaStream_t s);
 bool decode_fits(int64_t k);
 
+// Routing front-end (routing.cu).
+cudaError_t launch_route_topk(const float *logits, int64_t T, int E, int topk, int renormalize,
+                              int32_t *ids, float *weights, cudaStream_t s);
+size_t route_csr_workspace_bytes(int64_t T, int E);
+cudaError_t launch_route_csr(const int32_t *ids, int64_t T, int topk, int E, int32_t *offsets,
+                             int32_t *row_ids, int32_t *pair_rows, void *workspace,
+                             unsigned *err, cudaStream_t s);
+cudaError_t launch_moe_combine(const float *out, const int32_t *pair_rows, const float *weights,
+                               int64_t T, int topk, int64_t n, int64_t P, float *y, unsigned *err,
+                               cudaStream_t s);
+
 // Error-model constants of each path (n_ops of |err| <= n_ops 2^-24 sum|p|).
 double stream_error_ops(int recipe, int64_t k);
 double decode_error_ops(int recipe, int64_t k);

@@ -49,7 +49,8 @@ typedef enum { FP4_NVFP4 = 0, FP4_MXFP4 = 1 } fp4_recipe; /* matches the pages' 
 enum {
     FP4_DEVERR_OFFSETS = 1, /* offsets not non-decreasing from 0 to total_rows */
     FP4_DEVERR_ROW_ID = 2,  /* a row id outside [0, num_tokens) */
-    FP4_DEVERR_TIMEOUT = 4  /* a pipeline wait gave up after its iteration limit */
+    FP4_DEVERR_TIMEOUT = 4,  /* a pipeline wait gave up after its iteration limit */
+    FP4_DEVERR_EXPERT_ID = 8 /* an expert id outside [0, num_experts) or repeated in a token */
 };
 
 /* Kernel paths (fp4_gemm_path / fp4_force_path). */
@@ -83,6 +84,8 @@ int act_quant_fp8(const float *x, uint8_t *codes, float *scales, int64_t rows, i
  *   scales_out nullable [g, k/128] f32
  *   workspace  nullable; with at least fp4_grouped_workspace_size(g, g, n, k, recipe)
  *              bytes the tensor-core path may be used, otherwise the streaming path.
+ * Asking for codes_out costs nothing on the streaming path (its prologue quantises
+ * anyway) and one extra act_quant pass over x on the tensor-core path.
  */
 int fp4_expert_gemm(const float *x, const uint8_t *w, const uint8_t *wscale, float scale2,
                     int recipe, float *out, int64_t g, int64_t n, int64_t k, uint8_t *codes_out,
@@ -116,6 +119,42 @@ int fp4_grouped_expert_gemm(const float *x, int64_t num_tokens, const int32_t *r
                             size_t workspace_bytes, void *stream);
 
 /*
+ * The tensor-core path of fp4_grouped_expert_gemm in its two halves, for callers that
+ * time them apart or run several projections over one quantised input (the gate and up
+ * banks of one x, say). fp4_grouped_expert_gemm with a workspace on that path is exactly
+ * fp4_grouped_quantize followed by fp4_grouped_gemm_quantized on the same stream.
+ *
+ * fp4_grouped_quantize -- stage 1 for every routed row (fn quant_rows of
+ * dsv4_native_gemm_gate.rs on x[row_ids[p]], x[p] without row ids), written into the
+ * workspace as the 16-bit operands of the tensor-core GEMM: f16(code * 2^(m - M_p)) with
+ * a per-row power-of-two scale 2^M_p (NVFP4, while every 128-block of the row lies within
+ * 2^15 of its largest) or bf16(code * 2^m) (MXFP4, and NVFP4 calls with a wider row). Both
+ * are exact. The workspace layout is private to the library.
+ *   x, num_tokens, row_ids, total_rows, k, recipe: as fp4_grouped_expert_gemm
+ *   workspace at least fp4_grouped_workspace_size(num_tokens, total_rows, n, k, recipe) bytes
+ * Row ids outside [0, num_tokens) set FP4_DEVERR_ROW_ID; such rows quantise as zeros.
+ * Shapes the tensor-core path does not take (k not a multiple of 16*gs) return
+ * FP4_ERR_SHAPE.
+ */
+int fp4_grouped_quantize(const float *x, int64_t num_tokens, const int32_t *row_ids,
+                         int64_t total_rows, int64_t k, int recipe, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
+/*
+ * fp4_grouped_gemm_quantized -- stage 2 on the tensor cores (fn f64_ref of
+ * dsv4_native_gemm_gate.rs, f32 accumulation) from a workspace that fp4_grouped_quantize
+ * filled earlier on the same stream for the same total_rows, k and recipe; the workspace
+ * is only read, so one quantised input serves any number of these calls.
+ *   offsets, num_experts, w, wscale, scale2, out, n: as fp4_grouped_expert_gemm
+ * Always the tensor-core path (whatever the rows per expert); error model
+ * fp4_error_ops(FP4_PATH_TC, recipe, k).
+ */
+int fp4_grouped_gemm_quantized(const void *workspace, size_t workspace_bytes,
+                               const int32_t *offsets, int num_experts, int64_t total_rows,
+                               const uint8_t *w, const uint8_t *wscale, const float *scale2,
+                               int recipe, float *out, int64_t n, int64_t k, void *stream);
+
+/*
  * fp4_grouped_expert_gemm_noalloc -- the same computation as fp4_grouped_expert_gemm,
  * on the tensor-core path, for callers that cannot allocate device memory (a host
  * framework that owns all device memory and forbids libraries to allocate, a serving
@@ -124,12 +163,20 @@ int fp4_grouped_expert_gemm(const float *x, int64_t num_tokens, const int32_t *r
  * fixed 32 MiB device array inside this library, which every GPU that loads the library
  * holds until the process exits. The pages have no counterpart of this call.
  *   Arguments: as fp4_grouped_expert_gemm without workspace/workspace_bytes.
- *   Limit: total_rows * k * 2 + 1024 <= 32 MiB (e.g. 2048 routed rows at k = 7168);
- *          larger calls return FP4_ERR_WORKSPACE (message in fp4_last_error), shapes the
+ *   Limit: the call needs fp4_grouped_workspace_size(num_tokens, total_rows, n, k, recipe)
+ *          = 1024 + roundup(total_rows * k * 2, 1024) + 4 * total_rows + 16 bytes of
+ *          scratch, at most 32 MiB (e.g. 2048 routed rows at k = 7168); larger calls return
+ *          FP4_ERR_WORKSPACE (the message in fp4_last_error gives both numbers), shapes the
  *          tensor-core path does not take (k not a multiple of 16*gs, more than 1024
- *          experts) return FP4_ERR_SHAPE. Nothing is allocated, freed or synchronised.
+ *          experts) return FP4_ERR_SHAPE. The call itself allocates, frees and synchronises
+ *          nothing.
  *   First call on a device: looks up the scratch array's device address for that
- *          device (cudaGetSymbolAddress), so make it before any stream capture.
+ *          device (cudaGetSymbolAddress), so make it before any stream capture. The
+ *          driver reserves the array when this library's device code is first loaded on
+ *          a device (at the first call that needs it under lazy module loading, or when
+ *          the library is loaded with eager loading), and that reservation may
+ *          synchronise: make one warm-up call per device before any phase in which
+ *          nothing may allocate or synchronise.
  *   Sharing: every call uses the same array and leaves its contents behind; nothing in
  *          it needs to start at zero. Calls whose kernels overlap on the GPU (other
  *          streams, other threads) race on it: serialise them.
@@ -174,6 +221,60 @@ int fp4_gemm_mirror(const uint8_t *codes, const float *scales, const uint8_t *w,
 int fp4_swiglu_quant(const float *gate, const float *up, int64_t ld, float limit, int64_t rows,
                      int64_t inter, float *h_out, uint8_t *codes, float *scales, void *stream);
 
+/*
+ * The routing front-end: the steps before and after the grouped projections.
+ *
+ * fp4_route_topk -- the router (memra-engine 0.125.0, src/bin/qwen4exp_gpu_gate.rs,
+ * device-router arm: a softmax top-k whose selected ids and their order are exact and
+ * whose weights are within a few ulps; the pages do not print its body). Reading taken:
+ * each token selects the topk experts with the largest logits, equal logits ranking the
+ * lower expert id first, emitted best first; weights are softmax probabilities
+ * exp(l - max) / sum over all experts, or with renormalize != 0 over the selected ones.
+ *   logits  [num_tokens, num_experts] f32 (finite), 1 <= num_experts <= 1024
+ *   ids     [num_tokens, topk] int32 out, weights [num_tokens, topk] f32 out
+ *   1 <= topk <= min(32, num_experts)
+ */
+int fp4_route_topk(const float *logits, int64_t num_tokens, int num_experts, int topk,
+                   int renormalize, int32_t *ids, float *weights, void *stream);
+
+/* Workspace bytes fp4_route_csr needs (a bitmap and popcount prefix of num_experts x
+ * ceil(num_tokens/32) words, and the experts' row counts). */
+size_t fp4_route_csr_workspace_size(int64_t num_tokens, int num_experts);
+
+/*
+ * fp4_route_csr -- the CSR layout the grouped calls take (memra-engine 0.71.0,
+ * src/bin/kernel_check.rs, grouped MoE GEMM section: offsets[e+1] = offsets[e] + rows of
+ * expert e), built on the device from each token's expert ids. Routed rows are grouped by
+ * expert and, within an expert, in token order; the result does not depend on thread
+ * timing.
+ *   ids        [num_tokens, topk] int32 (distinct within a token, in [0, num_experts))
+ *   offsets    [num_experts + 1] int32 out (offsets[num_experts] = num_tokens * topk)
+ *   row_ids    [num_tokens * topk] int32 out: the token of each routed row
+ *   pair_rows  nullable [num_tokens, topk] int32 out: the routed row of each (token, slot)
+ *   workspace  at least fp4_route_csr_workspace_size(num_tokens, num_experts) bytes
+ * An id outside [0, num_experts) or repeated within a token sets FP4_DEVERR_EXPERT_ID;
+ * the outputs are then unspecified.
+ */
+int fp4_route_csr(const int32_t *ids, int64_t num_tokens, int topk, int num_experts,
+                  int32_t *offsets, int32_t *row_ids, int32_t *pair_rows, void *workspace,
+                  size_t workspace_bytes, void *stream);
+
+/*
+ * fp4_moe_combine -- the weighted combine of the routed rows' outputs back to tokens
+ * (memra-engine 0.71.0, src/bin/kernel_check.rs, grouped MoE GEMM section: a per-routed-
+ * row factor on the output, summed here over a token's routed rows):
+ *   y[t][c] = sum over slots j = 0 .. topk-1, in order, of weights[t][j] * out[pair_rows[t][j]][c]
+ * with one f32 fma per slot (error model: n_ops = topk against the f64 sum of |terms|).
+ *   out        [total_rows, n] f32 (a grouped call's output)
+ *   pair_rows  [num_tokens, topk] int32 (from fp4_route_csr); rows outside
+ *              [0, total_rows) set FP4_DEVERR_ROW_ID and are skipped
+ *   weights    [num_tokens, topk] f32
+ *   y          [num_tokens, n] f32 out; n must be a multiple of 4
+ */
+int fp4_moe_combine(const float *out, int64_t total_rows, const int32_t *pair_rows,
+                    const float *weights, int64_t num_tokens, int topk, int64_t n, float *y,
+                    void *stream);
+
 /* Which path a grouped call of this shape takes (never FP4_PATH_AUTO): the tensor-core
  * path when a workspace is given, the shape is one it supports and the routed rows
  * average at least 8 per expert; the no-workspace path otherwise. */
@@ -189,7 +290,8 @@ int fp4_gemm_path(int64_t total_rows, int num_experts, int64_t n, int64_t k, int
  */
 double fp4_error_ops(int path, int recipe, int64_t k);
 
-/* Test hook: force a path for later calls (FP4_PATH_AUTO restores the choice by shape). */
+/* Test hook: force a path for later calls made on the calling host thread (other threads
+ * keep the choice by shape); FP4_PATH_AUTO restores the choice by shape. */
 void fp4_force_path(int path);
 
 /*

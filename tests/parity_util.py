@@ -1,5 +1,8 @@
 """Helpers for the parity tests: run the CUDA path through the C ABI, run the oracle on
 the same inputs, and compare under the stated error model."""
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -17,6 +20,28 @@ def gemm_bound(path, recipe, k):
     # no more than one rounding per 16 products plus a fixed epilogue depth.
     assert 0 < n_ops <= 64 + k / 16, n_ops
     return n_ops
+
+
+def page_n_ops(recipe, k):
+    """n_ops of the pages' own kernel for this recipe and k: (gs-1) + ceil(groups/128) + 7
+    (dsv4_native_gemm_gate.rs, the f64 check in main)."""
+    gs = 16 if recipe == fp4.NVFP4 else 32
+    return (gs - 1) + -(-(k // gs) // 128) + 7
+
+
+def record_error(what, path, recipe, k, n_ops, worst, rel, count):
+    """With FP4_ERR_REPORT set to a file name, append the worst |err| / (2^-24 sum|p|) seen
+    by a parity check (its error in units of the error model's step), beside the stated
+    n_ops of the path and the pages' own n_ops for the shape."""
+    dest = os.environ.get("FP4_ERR_REPORT")
+    if not dest:
+        return
+    rec = {"what": what, "path": int(path) if path is not None else None, "recipe": int(recipe),
+           "k": int(k), "outputs": int(count), "n_ops": float(n_ops),
+           "page_n_ops": page_n_ops(recipe, k), "worst_units": float(worst) * float(n_ops),
+           "max_rel": float(rel)}
+    with open(dest, "a") as f:
+        f.write(json.dumps(rec) + "\n")
 
 
 def check_gemm(gpu_out, ref, absp, n_ops, what=""):
@@ -77,6 +102,7 @@ def grouped_sampled_check(proj, out_gpu, path, rows, what):
     rel = oracle.max_rel(np.concatenate([g.reshape(-1) for g in rel_gpu]),
                          np.concatenate([r.reshape(-1) for r in rel_refs]))
     assert rel <= 1e-3, (what, rel)
+    record_error(what, path, bank.recipe, k, n_ops, worst_all, rel, len(rows) * n)
     return worst_all, rel
 
 

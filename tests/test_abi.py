@@ -74,6 +74,53 @@ def test_host_side_argument_checks(lib):
     assert G(a16, 8, None, a16, 2, 8, odd, a16, a16, 1, a16, 4, 128, None, 0, None) == \
         fp4.FP4_ERR_ALIGN
     assert G(a16, 8, None, a16, 2, 0, a16, a16, a16, 1, a16, 4, 128, None, 0, None) == fp4.FP4_OK
+    # fp4_grouped_quantize(x, T, row_ids, P, k, recipe, workspace, ws_bytes, stream)
+    Q = lib.fp4_grouped_quantize
+    big = 1 << 40
+    assert Q(a16, 8, None, 8, 512, 5, a16, big, None) == fp4.FP4_ERR_ARG          # recipe
+    assert Q(a16, 8, None, 8, 384, 0, a16, big, None) == fp4.FP4_ERR_SHAPE        # k % 256
+    assert Q(a16, 8, None, 8, 768, 1, a16, big, None) == fp4.FP4_ERR_SHAPE        # k % 512
+    assert Q(a16, 8, None, 8, 512, 0, None, 0, None) == fp4.FP4_ERR_WORKSPACE
+    assert Q(a16, 8, None, 8, 512, 0, a16, 100, None) == fp4.FP4_ERR_WORKSPACE    # too small
+    assert Q(None, 8, None, 8, 512, 0, a16, big, None) == fp4.FP4_ERR_ARG
+    assert Q(a16, 4, None, 8, 512, 0, a16, big, None) == fp4.FP4_ERR_SHAPE        # T < P
+    assert Q(odd, 8, None, 8, 512, 0, a16, big, None) == fp4.FP4_ERR_ALIGN
+    assert Q(None, 0, None, 0, 512, 0, None, 0, None) == fp4.FP4_OK               # empty
+    # fp4_grouped_gemm_quantized(ws, ws_bytes, offsets, E, P, w, wscale, scale2, recipe,
+    #                            out, n, k, stream)
+    R = lib.fp4_grouped_gemm_quantized
+    assert R(a16, big, a16, 0, 8, a16, a16, a16, 0, a16, 256, 512, None) == fp4.FP4_ERR_ARG
+    assert R(None, 0, a16, 2, 8, a16, a16, a16, 0, a16, 256, 512, None) == fp4.FP4_ERR_WORKSPACE
+    assert R(a16, big, a16, 2, 8, a16, a16, None, 0, a16, 256, 512, None) == fp4.FP4_ERR_ARG
+    assert R(a16, big, None, 2, 8, a16, a16, a16, 0, a16, 256, 512, None) == fp4.FP4_ERR_ARG
+    assert R(a16, big, a16, 2, 8, odd, a16, a16, 0, a16, 256, 512, None) == fp4.FP4_ERR_ALIGN
+    assert R(a16, big, a16, 2, 8, a16, a16, None, 1, a16, 256, 768, None) == fp4.FP4_ERR_SHAPE
+    assert R(a16, big, a16, 2, 8, a16, a16, a16, 0, a16, 0, 512, None) == fp4.FP4_ERR_SHAPE
+    assert R(a16, big, a16, 2, 0, a16, a16, a16, 0, a16, 256, 512, None) == fp4.FP4_OK
+    # fp4_route_topk(logits, T, E, topk, renorm, ids, weights, stream)
+    K = lib.fp4_route_topk
+    assert K(a16, 4, 0, 1, 0, a16, a16, None) == fp4.FP4_ERR_ARG
+    assert K(a16, 4, 2048, 8, 0, a16, a16, None) == fp4.FP4_ERR_SHAPE          # E > 1024
+    assert K(a16, 4, 8, 9, 0, a16, a16, None) == fp4.FP4_ERR_SHAPE             # topk > E
+    assert K(a16, 4, 64, 33, 0, a16, a16, None) == fp4.FP4_ERR_SHAPE           # topk > 32
+    assert K(None, 4, 64, 8, 0, a16, a16, None) == fp4.FP4_ERR_ARG
+    assert K(odd, 4, 64, 8, 0, a16, a16, None) == fp4.FP4_ERR_ALIGN
+    assert K(None, 0, 64, 8, 0, None, None, None) == fp4.FP4_OK
+    # fp4_route_csr(ids, T, topk, E, offsets, row_ids, pair_rows, ws, ws_bytes, stream)
+    C = lib.fp4_route_csr
+    need = lib.fp4_route_csr_workspace_size(100, 16)
+    assert need == 4 * (2 * 16 * 4 + 16)
+    assert C(a16, 100, 2, 0, a16, a16, a16, a16, need, None) == fp4.FP4_ERR_ARG
+    assert C(a16, 100, 2, 16, None, a16, a16, a16, need, None) == fp4.FP4_ERR_ARG
+    assert C(a16, 100, 2, 16, a16, a16, a16, a16, need - 1, None) == fp4.FP4_ERR_WORKSPACE
+    assert C(a16, 100, 2, 16, a16, a16, a16, odd, need, None) == fp4.FP4_ERR_ALIGN
+    # fp4_moe_combine(out, P, pair_rows, weights, T, topk, n, y, stream)
+    B = lib.fp4_moe_combine
+    assert B(a16, 8, a16, a16, 4, 2, 6, a16, None) == fp4.FP4_ERR_SHAPE           # n % 4
+    assert B(a16, 8, a16, a16, 4, 0, 8, a16, None) == fp4.FP4_ERR_ARG
+    assert B(None, 8, a16, a16, 4, 2, 8, a16, None) == fp4.FP4_ERR_ARG
+    assert B(a16, 8, a16, a16, 4, 2, 8, odd, None) == fp4.FP4_ERR_ALIGN
+    assert B(None, 0, None, None, 0, 2, 8, None, None) == fp4.FP4_OK
     # fp4_gemm_mirror(codes, scales, w, wscale, scale2, recipe, out, g, n, k, stream)
     M = lib.fp4_gemm_mirror
     assert M(a16, a16, a16, a16, 1.0, 5, a16, 2, 4, 128, None) == fp4.FP4_ERR_ARG      # recipe

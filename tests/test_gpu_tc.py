@@ -183,3 +183,45 @@ def test_tc_full_size_prefill_repeatable_and_matches_stream():
                 assert diff == 0, "%s run %d: %d outputs differ from run 0" % (proj.name, rep, diff)
             del out
         del ref, first
+
+
+@pytest.mark.parametrize("recipe", [fp4.NVFP4, fp4.MXFP4])
+def test_two_phase_calls_match_one_call_and_share_the_quantised_input(recipe):
+    """fp4_grouped_quantize + fp4_grouped_gemm_quantized are the launches of one grouped
+    call on this path: same bits. One quantised input then serves a second bank (the gate
+    and up projections of one x), checked against the oracle on every output."""
+    proj = _projection(recipe, [40, 0, 100, 9, 1], n=256, k=1024, T=120, seed=3)
+    one, _ = run_projection(proj)
+    bank, r = proj.bank, proj.routing
+    T, k = proj.x.shape
+    ws = fp4.workspace_for(T, r.P, bank.n, k, recipe)
+    fp4.fp4_grouped_quantize(proj.x, r.row_ids, r.P, recipe, ws)
+    two = torch.empty_like(one)
+    fp4.fp4_grouped_gemm_quantized(ws, r.offsets, bank.w, bank.sc, bank.scale2, recipe, two)
+    assert torch.equal(one, two)
+    other = synth.make_bank(recipe, bank.E, bank.n, k, 977, DEV, scale2_value=1.0 / 64.0)
+    three = torch.empty_like(one)
+    fp4.fp4_grouped_gemm_quantized(ws, r.offsets, other.w, other.sc, other.scale2, recipe, three)
+    proj2 = synth.Projection("second bank", proj.x, r, other)
+    grouped_sampled_check(proj2, three, fp4.PATH_TC, np.arange(r.P), "second bank")
+    assert fp4.fp4_get_device_error() == 0
+
+
+@pytest.mark.parametrize("recipe", [fp4.NVFP4, fp4.MXFP4])
+def test_tc_quantise_pass_long_rows(recipe):
+    """k past what the quantise pass holds in registers (8 warps x 8 groups of 128): the
+    row is read twice. NVFP4 rows within the f16 route, then one row that forces the bf16
+    pass."""
+    for gaps, tag in [([0, 5, 9, 3, 12], "f16"), ([0, 5, 25, 3, 12], "bf16")]:
+        rng = np.random.default_rng(17)
+        k = 9216
+        x = rng.standard_normal((len(gaps), k))
+        for r, gmax in enumerate(gaps):
+            u = rng.uniform(0, gmax, k // 128)
+            u[0], u[-1] = 0.0, gmax
+            x[r] *= np.repeat(np.exp2(-u), 128)
+        proj = _projection_from(recipe, x.astype(np.float32), 200, k, 21)
+        out, path = run_projection(proj)
+        assert path == fp4.PATH_TC
+        grouped_sampled_check(proj, out, path, np.arange(proj.routing.P), "long rows " + tag)
+        assert fp4.fp4_get_device_error() == 0
