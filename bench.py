@@ -233,8 +233,10 @@ def proj_bytes(proj):
 
 
 def quant_bytes(proj):
-    """Algorithmic bytes of the quantise pass: each token's activation row read once (f32),
-    the 16-bit workspace row of every routed row written once, plus the row scales."""
+    """Algorithmic bytes of the quantise phase: each token's activation row read once (f32),
+    the 16-bit workspace row of every routed row written once, plus the row scales. (When
+    tokens repeat, the path also writes and re-reads a per-token copy: 2 B per token
+    element each way, counted as traffic, not as algorithmic bytes.)"""
     T, k = proj.x.shape
     P = proj.routing.P
     return T * k * 4 + P * k * 2 + P * 4
@@ -242,12 +244,15 @@ def quant_bytes(proj):
 
 def launches_per_call(fp4, proj, have_ws):
     """Kernels of ours one grouped call launches: the streaming kernel alone, or the
-    tensor-core path's quantise pass(es) + GEMM (NVFP4: f16 pass, conditional bf16 pass)."""
+    tensor-core path's quantise pass(es) (NVFP4: f16 pass, conditional bf16 pass), the
+    per-token expand when tokens repeat, and the GEMM."""
     path = fp4.fp4_gemm_path(proj.routing.P, proj.bank.E, proj.bank.n, proj.bank.k,
                              proj.bank.recipe, have_ws)
     if path != fp4.PATH_TC:
         return path, 1
-    return path, (3 if proj.bank.recipe == fp4.NVFP4 else 2)
+    T = proj.x.shape[0]
+    repeats = proj.row_ids_used and T < proj.routing.P  # quantise per token, then expand
+    return path, (3 if proj.bank.recipe == fp4.NVFP4 else 2) + (1 if repeats else 0)
 
 
 # ------------------------------------------------------------------ our arm
@@ -274,9 +279,10 @@ def make_calls(fp4, wl, device):
             def quantize(proj=proj, ws=ws, rid=rid):
                 fp4.fp4_grouped_quantize(proj.x, rid, proj.routing.P, proj.bank.recipe, ws)
 
-            def gemm(proj=proj, ws=ws, out=out):
-                fp4.fp4_grouped_gemm_quantized(ws, proj.routing.offsets, proj.bank.w, proj.bank.sc,
-                                               proj.bank.scale2, proj.bank.recipe, out)
+            def gemm(proj=proj, ws=ws, out=out, rid=rid):
+                fp4.fp4_grouped_gemm_quantized(ws, proj.x.shape[0], rid, proj.routing.offsets,
+                                               proj.bank.w, proj.bank.sc, proj.bank.scale2,
+                                               proj.bank.recipe, out)
             phases = [("quantize", quantize), ("gemm", gemm)]
         else:
             phases = [("gemm", call)]
@@ -602,7 +608,7 @@ def run_ours(args, world, rank, local):
                                      "traffic": ncu_traffic("tc_quantize/%s" % args.workload),
                                      "peak_source": peak_src + " HBM copy bandwidth"},
                         "bytes_basis": "activation rows read once per token (f32), the 16-bit "
-                                       "workspace written once per routed row"}
+                                       "workspace row of every routed row written once"}
     else:
         # the streaming path is bound by HBM reads of the weights
         kms = sum(call_ms)

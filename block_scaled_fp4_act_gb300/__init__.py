@@ -68,8 +68,8 @@ def lib():
         L.fp4_grouped_expert_gemm_noalloc.restype = i32
         L.fp4_grouped_quantize.argtypes = [P, i64, P, i64, i64, i32, P, sz, P]
         L.fp4_grouped_quantize.restype = i32
-        L.fp4_grouped_gemm_quantized.argtypes = [P, sz, P, i32, i64, P, P, P, i32, P, i64, i64,
-                                                 P]
+        L.fp4_grouped_gemm_quantized.argtypes = [P, sz, i64, P, P, i32, i64, P, P, P, i32, P,
+                                                 i64, i64, P]
         L.fp4_grouped_gemm_quantized.restype = i32
         L.fp4_route_topk.argtypes = [P, i64, i32, i32, i32, P, P, P]
         L.fp4_route_topk.restype = i32
@@ -226,15 +226,17 @@ def fp4_grouped_quantize(x, row_ids, total_rows, recipe, workspace, stream=None)
     return workspace
 
 
-def fp4_grouped_gemm_quantized(workspace, offsets, w, wscale, scale2, recipe, out,
-                               stream=None):
+def fp4_grouped_gemm_quantized(workspace, num_tokens, row_ids, offsets, w, wscale, scale2,
+                               recipe, out, stream=None):
     """Stage 2 on the tensor cores from a workspace fp4_grouped_quantize filled for the same
-    routed rows, k and recipe: offsets [E+1] int32, w [E,n,k/2], wscale [E,n,k/gs],
-    scale2 [E] (NVFP4) -> out [P,n] f32 (caller-owned)."""
+    tokens, row ids, routed rows, k and recipe: offsets [E+1] int32, w [E,n,k/2],
+    wscale [E,n,k/gs], scale2 [E] (NVFP4) -> out [P,n] f32 (caller-owned)."""
     import torch
     E, n = w.shape[0], w.shape[1]
     k = w.shape[2] * 2
     P = out.shape[0]
+    if row_ids is not None:
+        _need(row_ids, torch.int32, (P,), "row_ids")
     _need(workspace, torch.uint8, None, "workspace")
     _need(offsets, torch.int32, (E + 1,), "offsets")
     _need(w, torch.uint8, (E, n, k // 2), "w")
@@ -242,9 +244,10 @@ def fp4_grouped_gemm_quantized(workspace, offsets, w, wscale, scale2, recipe, ou
     if scale2 is not None:
         _need(scale2, torch.float32, (E,), "scale2")
     _need(out, torch.float32, (P, n), "out")
-    _check(lib().fp4_grouped_gemm_quantized(_ptr(workspace), workspace.numel(), _ptr(offsets), E,
-                                            P, _ptr(w), _ptr(wscale), _ptr(scale2), int(recipe),
-                                            _ptr(out), n, k, _stream(stream)),
+    _check(lib().fp4_grouped_gemm_quantized(_ptr(workspace), workspace.numel(), int(num_tokens),
+                                            _ptr(row_ids), _ptr(offsets), E, P, _ptr(w),
+                                            _ptr(wscale), _ptr(scale2), int(recipe), _ptr(out), n,
+                                            k, _stream(stream)),
            "fp4_grouped_gemm_quantized")
     return out
 

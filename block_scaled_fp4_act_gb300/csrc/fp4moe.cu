@@ -26,7 +26,7 @@ unsigned *device_error_word()
 }
 
 int stream_max_rows_per_pass(int k);
-size_t tc_workspace_bytes(int64_t total_rows, int64_t k, int recipe);
+size_t tc_workspace_bytes(int64_t num_tokens, int64_t total_rows, int64_t k, int recipe);
 bool tc_supported(int64_t n, int64_t k, int recipe, int E);
 cudaError_t launch_tc_quantize(const GroupedProblem &p, void *workspace, cudaStream_t s);
 cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaStream_t s);
@@ -110,7 +110,7 @@ static int run_grouped(GroupedProblem p, void *workspace, size_t ws_bytes, cudaS
         return record(cudaGetLastError() != cudaSuccess ? cudaGetLastError()
                                                           : cudaErrorInvalidDevice);
     const bool have_ws =
-        workspace != nullptr && ws_bytes >= tc_workspace_bytes(p.P, p.k, p.recipe);
+        workspace != nullptr && ws_bytes >= tc_workspace_bytes(p.T, p.P, p.k, p.recipe);
     const int path = choose_path(p.P, p.E, p.n, p.k, p.recipe, have_ws);
     if (path == FP4_PATH_TC) {
         if (!tc_supported(p.n, p.k, p.recipe, p.E))
@@ -228,12 +228,11 @@ int fp4_expert_gemm(const float *x, const uint8_t *w, const uint8_t *wscale, flo
 size_t fp4_grouped_workspace_size(int64_t num_tokens, int64_t total_rows, int64_t n, int64_t k,
                                   int recipe)
 {
-    (void)num_tokens;
-    if (!recipe_ok(recipe) || check_shape(total_rows, n, k) != FP4_OK)
+    if (num_tokens < 0 || !recipe_ok(recipe) || check_shape(total_rows, n, k) != FP4_OK)
         return 0;
     if (!tc_supported(n, k, recipe, 1))
         return 0;  // the shape always takes the streaming path, which needs no workspace
-    return tc_workspace_bytes(total_rows, k, recipe);
+    return tc_workspace_bytes(num_tokens, total_rows, k, recipe);
 }
 
 int fp4_grouped_expert_gemm(const float *x, int64_t num_tokens, const int32_t *row_ids,
@@ -276,17 +275,20 @@ int fp4_grouped_expert_gemm(const float *x, int64_t num_tokens, const int32_t *r
 }
 
 // Shared checks of the two halves of the tensor-core path.
-static int check_tc_call(int recipe, int64_t total_rows, int64_t n, int64_t k, const void *ws,
-                         size_t ws_bytes)
+static int check_tc_call(int recipe, int64_t num_tokens, const int32_t *row_ids,
+                         int64_t total_rows, int64_t n, int64_t k, const void *ws, size_t ws_bytes)
 {
-    if (!recipe_ok(recipe))
+    if (!recipe_ok(recipe) || num_tokens < 0)
         return FP4_ERR_ARG;
     const int st = check_shape(total_rows, n, k);
     if (st != FP4_OK)
         return st;
     if (!tc_supported(n, k, recipe, 1))
         return FP4_ERR_SHAPE;
-    if (total_rows > 0 && (!ws || ws_bytes < tc_workspace_bytes(total_rows, k, recipe)))
+    if (!row_ids && num_tokens < total_rows)
+        return FP4_ERR_SHAPE;
+    if (total_rows > 0 &&
+        (!ws || ws_bytes < tc_workspace_bytes(num_tokens, total_rows, k, recipe)))
         return FP4_ERR_WORKSPACE;
     return FP4_OK;
 }
@@ -295,17 +297,14 @@ int fp4_grouped_quantize(const float *x, int64_t num_tokens, const int32_t *row_
                          int64_t total_rows, int64_t k, int recipe, void *workspace,
                          size_t workspace_bytes, void *stream)
 {
-    if (num_tokens < 0)
-        return FP4_ERR_ARG;
-    int st = check_tc_call(recipe, total_rows, 128, k, workspace, workspace_bytes);
+    int st = check_tc_call(recipe, num_tokens, row_ids, total_rows, 128, k, workspace,
+                           workspace_bytes);
     if (st != FP4_OK)
         return st;
     if (total_rows == 0)
         return FP4_OK;
     if (!x)
         return FP4_ERR_ARG;
-    if (!row_ids && num_tokens < total_rows)
-        return FP4_ERR_SHAPE;
     if (!aligned16(x))
         return FP4_ERR_ALIGN;
     GroupedProblem p{};
@@ -324,13 +323,15 @@ int fp4_grouped_quantize(const float *x, int64_t num_tokens, const int32_t *row_
 }
 
 int fp4_grouped_gemm_quantized(const void *workspace, size_t workspace_bytes,
+                               int64_t num_tokens, const int32_t *row_ids,
                                const int32_t *offsets, int num_experts, int64_t total_rows,
                                const uint8_t *w, const uint8_t *wscale, const float *scale2,
                                int recipe, float *out, int64_t n, int64_t k, void *stream)
 {
     if (num_experts < 1 || num_experts > 65535)
         return FP4_ERR_ARG;
-    int st = check_tc_call(recipe, total_rows, n, k, workspace, workspace_bytes);
+    int st = check_tc_call(recipe, num_tokens, row_ids, total_rows, n, k, workspace,
+                           workspace_bytes);
     if (st != FP4_OK)
         return st;
     if (!tc_supported(n, k, recipe, num_experts))
@@ -342,6 +343,8 @@ int fp4_grouped_gemm_quantized(const void *workspace, size_t workspace_bytes,
     if (!aligned16(w) || !aligned16(wscale) || !aligned16(out))
         return FP4_ERR_ALIGN;
     GroupedProblem p{};
+    p.T = num_tokens;
+    p.row_ids = row_ids;
     p.offsets = offsets;
     p.E = num_experts;
     p.P = total_rows;

@@ -64,7 +64,10 @@ namespace tc {
 constexpr int BM = 128;
 constexpr int BN = 192;       // routed rows per tile (MMA N, rounded up to 16 per tile)
 constexpr int BK = 64;
-constexpr int W_STAGES = 14;  // weight ring (nibbles + scales): deep, it streams from HBM
+// Weight ring: a slot holds 256 k (W_KS k-stages) of a tile's 128 weight rows, so every
+// row of the nibble box is one whole 128-byte line and one TMA pair feeds four k-stages.
+constexpr int W_KS = 4;
+constexpr int W_STAGES = 5;   // weight ring slots (20 k-stages ahead): it streams from HBM
 constexpr int A_STAGES = 4;   // converted weight tiles, in tensor memory
 constexpr int B_STAGES = 4;   // activation tiles (mostly L2 hits: shared by a tile's neighbours)
 constexpr int kMaxExperts = 1024;
@@ -99,8 +102,8 @@ static_assert(kACol + A_STAGES * (BK / 2) <= 512, "tensor memory budget");
 // tile (32 rows x 8, 64 x 4, 128 x 2 k-blocks, or BN rows x 1), so small tiles keep many
 // k-stages in flight in the same ring slots.
 constexpr int B_BYTES = 32 * 8 * BK * 2;  // one ring slot (the largest box)
-constexpr int NIB_BYTES = BM * BK / 2;
-constexpr int SC_BYTES = BM * 16;
+constexpr int NIB_BYTES = BM * BK * W_KS / 2;  // 128 rows x 128 bytes, 128-byte swizzle
+constexpr int SC_BYTES = BM * 16;               // 16 scale bytes per row (256 k NVFP4)
 constexpr int W_BYTES = NIB_BYTES + SC_BYTES;
 constexpr int OFF_W = B_STAGES * B_BYTES;
 constexpr int RING_BYTES = OFF_W + W_STAGES * W_BYTES;
@@ -473,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < W_STAGES; ++s) {
             mbar_init(wfull(s), 1);
-            mbar_init(wempty(s), kConvPerStage);
+            mbar_init(wempty(s), kConvPerStage * W_KS);
         }
         for (int s = 0; s < A_STAGES; ++s) {
             mbar_init(afull(s), kConvPerStage);
@@ -542,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int bi = bmap_index(tl.rows);
                 const int kbps = bmap_kblocks(bi);
                 const uint32_t box_bytes = (uint32_t)(bmap_rows(bi) * kbps * BK * 2);
-                const int nload = is_b ? (nkb + kbps - 1) / kbps : nkb;
+                const int nload = is_b ? (nkb + kbps - 1) / kbps : nkb / W_KS;
                 for (int j = 0; j < nload; ++j) {
                     const uint32_t emp = is_b ? bempty(slot) : wempty(slot);
                     const uint32_t ful = is_b ? bfull(slot) : wfull(slot);
@@ -556,10 +559,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     j * kbps, ful);
                     } else {
                         uint8_t *dst = ringW + slot * W_BYTES;
+                        const int k0 = j * W_KS * BK;  // first k of the slot
                         mbar_arrive_expect_tx(ful, W_BYTES);
-                        tma_load_2d(smem_u32(dst), &tmW, j * (BK / 2), yw, ful);
-                        tma_load_2d(smem_u32(dst + NIB_BYTES), &tmS, ((j * BK) / gs) & ~15, yw,
-                                    ful);
+                        tma_load_2d(smem_u32(dst), &tmW, k0 / 2, yw, ful);
+                        tma_load_2d(smem_u32(dst + NIB_BYTES), &tmS, (k0 / gs) & ~15, yw, ful);
                     }
                     issued_mask |= 1u << slot;
                     issued_parity = (issued_parity & ~(1u << slot)) | (phase << slot);
@@ -685,24 +688,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         // half c = h & 1 of the stage (one 16-byte nibble chunk, 16 TMEM columns).
         const int q = warp & 3, h = (warp - 8) >> 2, c = h & 1;
         const int r = q * 32 + lane;
-        // the nibble tile arrives with the 32-byte TMA swizzle: the 16-byte chunk c of row r
-        // sits at chunk c ^ bit 2 of r, so a warp's 32 rows read conflict-free
-        const int nib_off = r * 32 + ((c ^ ((r >> 2) & 1)) << 4);
         const uint32_t a_lane = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(kACol + c * 16);
-        Ring<W_STAGES> rw;
-        Ring<A_STAGES> ra;
-        for (int i = 0; i < (h >> 1); ++i) {
-            rw.next();
-            ra.next();
-        }
         const int ntiles = (int)blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
         const int nst = ntiles * nkb;
+        // g: this CTA's k-stage sequence over its tiles. Every tile has a multiple of W_KS
+        // stages, so W slot g / W_KS holds stage g as its sub-stage g % W_KS.
         for (int g = h >> 1; g < nst; g += kConvTurns) {
             const int kb = g % nkb;
-            if (!mbar_wait(wfull(rw.slot), rw.phase, abort_flag, p.err))
+            const int wseq = g / W_KS, wslot = wseq % W_STAGES;
+            const int aslot = g % A_STAGES;
+            const uint32_t wphase = (uint32_t)(wseq / W_STAGES) & 1u;
+            const uint32_t aphase = (uint32_t)(g / A_STAGES) & 1u;
+            if (!mbar_wait(wfull(wslot), wphase, abort_flag, p.err))
                 break;
-            const uint8_t *w = ringW + rw.slot * W_BYTES;
-            const uint4 nv = *reinterpret_cast<const uint4 *>(w + nib_off);
+            const uint8_t *w = ringW + wslot * W_BYTES;
+            // row r of the nibble box is 128 bytes in the 128-byte swizzle: its 16-byte chunk
+            // j (32 k) sits at chunk j ^ (r & 7); a warp's 32 rows then read conflict-free
+            const int chunk = 2 * (g % W_KS) + c;
+            const uint4 nv = *reinterpret_cast<const uint4 *>(w + r * 128 + ((chunk ^ (r & 7)) << 4));
             uint32_t o[16];
             uint4 *o4 = reinterpret_cast<uint4 *>(o);
             if (gs == 16) {
@@ -736,20 +739,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(wempty(rw.slot));
+                mbar_arrive(wempty(wslot));
             // then wait for the A slot: the conversion overlapped the MMAs still reading it
-            if (!mbar_wait(aempty(ra.slot), ra.phase ^ 1u, abort_flag, p.err))
+            if (!mbar_wait(aempty(aslot), aphase ^ 1u, abort_flag, p.err))
                 break;
             tc_fence_after();
-            tmem_st16(a_lane + (uint32_t)(ra.slot * (BK / 2)), o);
+            tmem_st16(a_lane + (uint32_t)(aslot * (BK / 2)), o);
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(afull(ra.slot));
-            for (int i = 0; i < kConvTurns; ++i) {
-                rw.next();
-                ra.next();
-            }
+                mbar_arrive(afull(aslot));
         }
     } else if (role == ROLE_EPI) {
         // ---------------------------------------------------------- epilogue
@@ -947,7 +946,37 @@ __global__ void __launch_bounds__(256, 3) quant_ws_kernel(const float *__restric
     }
 }
 
-// ------------------------------------------------------------------ host side
+// Expand: routed row p of the GEMM's workspace = token row row_ids[p] of the per-token
+// workspace (its 16-bit operands and, on the f16 route, its row scale), a copy. One warp
+// per routed row; 16-byte loads kept in L2 (the token rows are read about topk times),
+// streaming stores. Row ids outside [0, T) give zero rows and raise FP4_DEVERR_ROW_ID.
+__global__ void __launch_bounds__(256) expand_ws_kernel(const uint4 *__restrict__ tok_act,
+                                                        const float *__restrict__ tok_scale,
+                                                        const int32_t *__restrict__ row_ids,
+                                                        int64_t T, int64_t P, int k,
+                                                        uint4 *__restrict__ act,
+                                                        float *__restrict__ rowscale,
+                                                        unsigned *err)
+{
+    const int lane = threadIdx.x & 31;
+    const int chunks = k / 8;  // 16-byte chunks of a row of k 16-bit values
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t pr = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); pr < P;
+         pr += warps) {
+        const int64_t t = __ldg(row_ids + pr);
+        const bool ok = t >= 0 && t < T;
+        if (!ok && lane == 0)
+            raise_device_error(err, FP4_DEVERR_ROW_ID);
+        const uint4 *src = tok_act + (ok ? t : 0) * chunks;
+        uint4 *dst = act + pr * chunks;
+        for (int c = lane; c < chunks; c += 32) {
+            const uint4 v = ok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+            __stcs(dst + c, v);
+        }
+        if (lane == 0)
+            rowscale[pr] = ok ? __ldg(tok_scale + t) : 1.0f;
+    }
+}
 
 // 3-D map {64 k, rows, k-blocks} over a [rows, k] bf16 matrix, box {64, box_rows, box_kb}.
 static bool make_map_kblocks(CUtensorMap *m, const void *base, uint64_t k, uint64_t rows,
@@ -967,16 +996,33 @@ static bool make_map_kblocks(CUtensorMap *m, const void *base, uint64_t k, uint6
 
 } // namespace tc
 
-// Workspace: [activations P x k x 2 B, 1024-aligned][rowscale P x 4 B][route flag 16 B].
-static size_t ws_act_bytes(int64_t total_rows, int64_t k)
+// Tokens are quantised once when routed rows repeat them (row ids given and fewer tokens
+// than routed rows): into a per-token region, then copied into routed-row order; otherwise
+// the quantise pass reads every routed row's activation directly.
+static bool per_token(const GroupedProblem &p)
 {
-    return ((size_t)total_rows * (size_t)k * 2 + 1023) & ~(size_t)1023;
+    return p.row_ids != nullptr && p.T < p.P;
 }
 
-size_t tc_workspace_bytes(int64_t total_rows, int64_t k, int recipe)
+static size_t ws_act_bytes(int64_t rows, int64_t k)
+{
+    return ((size_t)rows * (size_t)k * 2 + 1023) & ~(size_t)1023;
+}
+
+static size_t ws_rows_bytes(int64_t rows, int64_t k)
+{
+    return ws_act_bytes(rows, k) + (((size_t)rows * 4 + 1023) & ~(size_t)1023);
+}
+
+// Workspace: [routed rows: P x k 16-bit operands | P row scales][route flag, 1 KB]
+// [when tokens repeat: T x k 16-bit operands | T row scales], each part 1024-aligned.
+size_t tc_workspace_bytes(int64_t num_tokens, int64_t total_rows, int64_t k, int recipe)
 {
     (void)recipe;
-    return 1024 + ws_act_bytes(total_rows, k) + (size_t)total_rows * 4 + 16;
+    size_t b = 1024 + ws_rows_bytes(total_rows, k) + 1024;
+    if (num_tokens < total_rows)
+        b += ws_rows_bytes(num_tokens, k);
+    return b;
 }
 
 bool tc_supported(int64_t n, int64_t k, int recipe, int E)
@@ -1005,20 +1051,24 @@ static int device_sms()
     return cached[dev];
 }
 
-// Where the parts of a workspace live (1024-aligned start, as the TMA tiles need).
+// Where the parts of a workspace live.
 struct WsLayout {
-    uint8_t *act;         // [P, k] 16-bit MMA operands
-    float *rowscale;      // [P] f32 (f16 route)
-    unsigned *route_flag; // nonzero: the bf16 route holds
+    uint8_t *act;          // [P, k] 16-bit MMA operands in routed-row order
+    float *rowscale;       // [P] f32 (f16 route)
+    unsigned *route_flag;  // nonzero: the bf16 route holds
+    uint8_t *tok_act;      // [T, k] per token (when tokens repeat)
+    float *tok_scale;      // [T]
 };
 
-static WsLayout ws_layout(const void *workspace, int64_t P, int64_t k)
+static WsLayout ws_layout(const void *workspace, int64_t T, int64_t P, int64_t k)
 {
     WsLayout l;
     l.act = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(workspace) + 1023) &
                                         ~(uintptr_t)1023);
     l.rowscale = reinterpret_cast<float *>(l.act + ws_act_bytes(P, k));
-    l.route_flag = reinterpret_cast<unsigned *>(l.rowscale + P);
+    l.route_flag = reinterpret_cast<unsigned *>(l.act + ws_rows_bytes(P, k));
+    l.tok_act = l.act + ws_rows_bytes(P, k) + 1024;
+    l.tok_scale = reinterpret_cast<float *>(l.tok_act + ws_act_bytes(T, k));
     return l;
 }
 
@@ -1029,7 +1079,12 @@ static WsLayout ws_layout(const void *workspace, int64_t P, int64_t k)
 cudaError_t launch_tc_quantize(const GroupedProblem &p, void *workspace, cudaStream_t s)
 {
     using namespace tc;
-    const WsLayout l = ws_layout(workspace, p.P, p.k);
+    const bool tok = per_token(p);
+    const WsLayout l = ws_layout(workspace, p.T, p.P, p.k);
+    const int64_t S = tok ? p.T : p.P;                 // rows the quantise pass writes
+    const int32_t *rid = tok ? nullptr : p.row_ids;    // per token: row s is x[s]
+    uint2 *qact = reinterpret_cast<uint2 *>(tok ? l.tok_act : l.act);
+    float *qscale = tok ? l.tok_scale : l.rowscale;
     const int sms = device_sms();
     const bool nvfp4 = p.recipe == FP4_NVFP4;
     const int kq = p.k / 128;
@@ -1039,35 +1094,45 @@ cudaError_t launch_tc_quantize(const GroupedProblem &p, void *workspace, cudaStr
         wr <<= 1;
     const bool reg = (kq + wr - 1) / wr <= kQuantRegGroups;
     const int64_t rpc = 8 / wr;
-    const int64_t want = (p.P + rpc - 1) / rpc;
+    const int64_t want = (S + rpc - 1) / rpc;
     const int blocks = (int)(want < (int64_t)sms * 3 ? want : (int64_t)sms * 3);  // 3 CTAs per SM
-    uint2 *ws = reinterpret_cast<uint2 *>(l.act);
     auto kern = reg ? quant_ws_kernel<true> : quant_ws_kernel<false>;
     if (nvfp4) {
         cudaError_t e = cudaMemsetAsync(l.route_flag, 0, sizeof(unsigned), s);
         if (e != cudaSuccess)
             return e;
-        kern<<<blocks, 256, 0, s>>>(p.x, p.T, p.row_ids, p.P, p.k, wr, 1, ws, l.rowscale,
-                                    l.route_flag, nullptr, p.err);
-        // the bf16 fallback: exits at once unless a row was too wide for f16
-        const int fb = 2 * sms < blocks ? 2 * sms : blocks;
-        kern<<<fb, 256, 0, s>>>(p.x, p.T, p.row_ids, p.P, p.k, wr, 0, ws, l.rowscale, nullptr,
-                                l.route_flag, p.err);
-    } else {
-        kern<<<blocks, 256, 0, s>>>(p.x, p.T, p.row_ids, p.P, p.k, wr, 0, ws, l.rowscale, nullptr,
-                                    nullptr, p.err);
+    }
+    if (S > 0) {
+        if (nvfp4) {
+            kern<<<blocks, 256, 0, s>>>(p.x, p.T, rid, S, p.k, wr, 1, qact, qscale, l.route_flag,
+                                        nullptr, p.err);
+            // the bf16 fallback: exits at once unless a row was too wide for f16
+            const int fb = 2 * sms < blocks ? 2 * sms : blocks;
+            kern<<<fb, 256, 0, s>>>(p.x, p.T, rid, S, p.k, wr, 0, qact, qscale, nullptr,
+                                    l.route_flag, p.err);
+        } else {
+            kern<<<blocks, 256, 0, s>>>(p.x, p.T, rid, S, p.k, wr, 0, qact, qscale, nullptr,
+                                        nullptr, p.err);
+        }
+    }
+    if (tok) {
+        const int64_t ew = (p.P + 7) / 8;
+        const int eblocks = (int)(ew < (int64_t)sms * 8 ? ew : (int64_t)sms * 8);
+        expand_ws_kernel<<<eblocks, 256, 0, s>>>(
+            reinterpret_cast<const uint4 *>(l.tok_act), l.tok_scale, p.row_ids, p.T, p.P, p.k,
+            reinterpret_cast<uint4 *>(l.act), l.rowscale, p.err);
     }
     return cudaGetLastError();
 }
 
 // The persistent tensor-core GEMM over a workspace that launch_tc_quantize filled for the
-// same routed rows, k and recipe.
+// same tokens, row ids (present or not), routed rows, k and recipe.
 cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaStream_t s)
 {
     using namespace tc;
     if (!tc_supported(p.n, p.k, p.recipe, p.E))
         return cudaErrorInvalidValue;
-    const WsLayout l = ws_layout(workspace, p.P, p.k);
+    const WsLayout l = ws_layout(workspace, p.T, p.P, p.k);
     const int sms = device_sms();
     const bool nvfp4 = p.recipe == FP4_NVFP4;
     const int gs = nvfp4 ? 16 : 32;
@@ -1078,7 +1143,7 @@ cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaS
                               (uint32_t)bmap_rows(i), (uint32_t)bmap_kblocks(i)))
             return cudaErrorInvalidValue;
     if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w, (uint64_t)p.k / 2,
-                  (uint64_t)p.E * p.n, BK / 2, BM, CU_TENSOR_MAP_SWIZZLE_32B) ||
+                  (uint64_t)p.E * p.n, W_KS * BK / 2, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sc, (uint64_t)p.k / gs,
                   (uint64_t)p.E * p.n, 16, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
@@ -1193,12 +1258,12 @@ extern "C" int fp4_grouped_expert_gemm_noalloc(const float *x, int64_t num_token
         return FP4_ERR_ALIGN;
     if (!tc_supported(n, k, recipe, num_experts))
         return FP4_ERR_SHAPE;
-    const size_t need = tc_workspace_bytes(total_rows, k, recipe);
+    const size_t need = tc_workspace_bytes(num_tokens, total_rows, k, recipe);
     if (need > kNoAllocScratchBytes) {
         char msg[256];
         snprintf(msg, sizeof(msg),
                  "fp4_grouped_expert_gemm_noalloc: the call needs %zu bytes of scratch "
-                 "(1024 + roundup(total_rows*k*2, 1024) + 4*total_rows + 16), the fixed "
+                 "(fp4_grouped_workspace_size), the fixed "
                  "scratch holds %zu",
                  need, kNoAllocScratchBytes);
         set_last_error(msg);

@@ -124,12 +124,14 @@ int fp4_grouped_expert_gemm(const float *x, int64_t num_tokens, const int32_t *r
  * banks of one x, say). fp4_grouped_expert_gemm with a workspace on that path is exactly
  * fp4_grouped_quantize followed by fp4_grouped_gemm_quantized on the same stream.
  *
- * fp4_grouped_quantize -- stage 1 for every routed row (fn quant_rows of
- * dsv4_native_gemm_gate.rs on x[row_ids[p]], x[p] without row ids), written into the
- * workspace as the 16-bit operands of the tensor-core GEMM: f16(code * 2^(m - M_p)) with
- * a per-row power-of-two scale 2^M_p (NVFP4, while every 128-block of the row lies within
+ * fp4_grouped_quantize -- stage 1 (fn quant_rows of dsv4_native_gemm_gate.rs) written into
+ * the workspace as the 16-bit operands of the tensor-core GEMM: f16(code * 2^(m - M)) with
+ * a per-row power-of-two scale 2^M (NVFP4, while every 128-block of the row lies within
  * 2^15 of its largest) or bf16(code * 2^m) (MXFP4, and NVFP4 calls with a wider row). Both
- * are exact. The workspace layout is private to the library.
+ * are exact. When row ids repeat tokens (row_ids given and num_tokens < total_rows) each
+ * token row is quantised once and the result copied to its routed rows; otherwise every
+ * routed row x[row_ids[p]] (x[p]) is quantised. The workspace layout is private to the
+ * library.
  *   x, num_tokens, row_ids, total_rows, k, recipe: as fp4_grouped_expert_gemm
  *   workspace at least fp4_grouped_workspace_size(num_tokens, total_rows, n, k, recipe) bytes
  * Row ids outside [0, num_tokens) set FP4_DEVERR_ROW_ID; such rows quantise as zeros.
@@ -143,13 +145,17 @@ int fp4_grouped_quantize(const float *x, int64_t num_tokens, const int32_t *row_
 /*
  * fp4_grouped_gemm_quantized -- stage 2 on the tensor cores (fn f64_ref of
  * dsv4_native_gemm_gate.rs, f32 accumulation) from a workspace that fp4_grouped_quantize
- * filled earlier on the same stream for the same total_rows, k and recipe; the workspace
- * is only read, so one quantised input serves any number of these calls.
- *   offsets, num_experts, w, wscale, scale2, out, n: as fp4_grouped_expert_gemm
+ * filled earlier on the same stream for the same num_tokens, row ids, total_rows, k and
+ * recipe; the workspace is only read, so one quantised input serves any number of these
+ * calls. (Row ids are checked by fp4_grouped_quantize: outside [0, num_tokens) they set
+ * FP4_DEVERR_ROW_ID and give zero rows.)
+ *   num_tokens, row_ids, offsets, num_experts, w, wscale, scale2, out, n: as
+ *   fp4_grouped_expert_gemm
  * Always the tensor-core path (whatever the rows per expert); error model
  * fp4_error_ops(FP4_PATH_TC, recipe, k).
  */
 int fp4_grouped_gemm_quantized(const void *workspace, size_t workspace_bytes,
+                               int64_t num_tokens, const int32_t *row_ids,
                                const int32_t *offsets, int num_experts, int64_t total_rows,
                                const uint8_t *w, const uint8_t *wscale, const float *scale2,
                                int recipe, float *out, int64_t n, int64_t k, void *stream);
@@ -164,8 +170,10 @@ int fp4_grouped_gemm_quantized(const void *workspace, size_t workspace_bytes,
  * holds until the process exits. The pages have no counterpart of this call.
  *   Arguments: as fp4_grouped_expert_gemm without workspace/workspace_bytes.
  *   Limit: the call needs fp4_grouped_workspace_size(num_tokens, total_rows, n, k, recipe)
- *          = 1024 + roundup(total_rows * k * 2, 1024) + 4 * total_rows + 16 bytes of
- *          scratch, at most 32 MiB (e.g. 2048 routed rows at k = 7168); larger calls return
+ *          = 2048 + R(2 * total_rows * k) + R(4 * total_rows), plus R(2 * num_tokens * k) +
+ *          R(4 * num_tokens) when num_tokens < total_rows, bytes of scratch (R rounds up to
+ *          a multiple of 1024), at most 32 MiB (e.g. 2048 routed rows at k = 7168, or 2048
+ *          routed rows of 256 tokens); larger calls return
  *          FP4_ERR_WORKSPACE (the message in fp4_last_error gives both numbers), shapes the
  *          tensor-core path does not take (k not a multiple of 16*gs, more than 1024
  *          experts) return FP4_ERR_SHAPE. The call itself allocates, frees and synchronises

@@ -86,17 +86,26 @@ def test_host_side_argument_checks(lib):
     assert Q(a16, 4, None, 8, 512, 0, a16, big, None) == fp4.FP4_ERR_SHAPE        # T < P
     assert Q(odd, 8, None, 8, 512, 0, a16, big, None) == fp4.FP4_ERR_ALIGN
     assert Q(None, 0, None, 0, 512, 0, None, 0, None) == fp4.FP4_OK               # empty
-    # fp4_grouped_gemm_quantized(ws, ws_bytes, offsets, E, P, w, wscale, scale2, recipe,
-    #                            out, n, k, stream)
+    # fp4_grouped_gemm_quantized(ws, ws_bytes, T, row_ids, offsets, E, P, w, wscale, scale2,
+    #                            recipe, out, n, k, stream)
     R = lib.fp4_grouped_gemm_quantized
-    assert R(a16, big, a16, 0, 8, a16, a16, a16, 0, a16, 256, 512, None) == fp4.FP4_ERR_ARG
-    assert R(None, 0, a16, 2, 8, a16, a16, a16, 0, a16, 256, 512, None) == fp4.FP4_ERR_WORKSPACE
-    assert R(a16, big, a16, 2, 8, a16, a16, None, 0, a16, 256, 512, None) == fp4.FP4_ERR_ARG
-    assert R(a16, big, None, 2, 8, a16, a16, a16, 0, a16, 256, 512, None) == fp4.FP4_ERR_ARG
-    assert R(a16, big, a16, 2, 8, odd, a16, a16, 0, a16, 256, 512, None) == fp4.FP4_ERR_ALIGN
-    assert R(a16, big, a16, 2, 8, a16, a16, None, 1, a16, 256, 768, None) == fp4.FP4_ERR_SHAPE
-    assert R(a16, big, a16, 2, 8, a16, a16, a16, 0, a16, 0, 512, None) == fp4.FP4_ERR_SHAPE
-    assert R(a16, big, a16, 2, 0, a16, a16, a16, 0, a16, 256, 512, None) == fp4.FP4_OK
+    assert R(a16, big, 8, None, a16, 0, 8, a16, a16, a16, 0, a16, 256, 512, None) == \
+        fp4.FP4_ERR_ARG
+    assert R(None, 0, 8, None, a16, 2, 8, a16, a16, a16, 0, a16, 256, 512, None) == \
+        fp4.FP4_ERR_WORKSPACE
+    assert R(a16, big, 8, None, a16, 2, 8, a16, a16, None, 0, a16, 256, 512, None) == \
+        fp4.FP4_ERR_ARG
+    assert R(a16, big, 8, None, None, 2, 8, a16, a16, a16, 0, a16, 256, 512, None) == \
+        fp4.FP4_ERR_ARG
+    assert R(a16, big, 8, None, a16, 2, 8, odd, a16, a16, 0, a16, 256, 512, None) == \
+        fp4.FP4_ERR_ALIGN
+    assert R(a16, big, 8, None, a16, 2, 8, a16, a16, None, 1, a16, 256, 768, None) == \
+        fp4.FP4_ERR_SHAPE
+    assert R(a16, big, 8, None, a16, 2, 8, a16, a16, a16, 0, a16, 0, 512, None) == \
+        fp4.FP4_ERR_SHAPE
+    assert R(a16, big, 4, None, a16, 2, 8, a16, a16, a16, 0, a16, 256, 512, None) == \
+        fp4.FP4_ERR_SHAPE                                # no row ids, fewer tokens than rows
+    assert R(a16, big, 8, None, a16, 2, 0, a16, a16, a16, 0, a16, 256, 512, None) == fp4.FP4_OK
     # fp4_route_topk(logits, T, E, topk, renorm, ids, weights, stream)
     K = lib.fp4_route_topk
     assert K(a16, 4, 0, 1, 0, a16, a16, None) == fp4.FP4_ERR_ARG

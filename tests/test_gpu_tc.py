@@ -197,11 +197,13 @@ def test_two_phase_calls_match_one_call_and_share_the_quantised_input(recipe):
     ws = fp4.workspace_for(T, r.P, bank.n, k, recipe)
     fp4.fp4_grouped_quantize(proj.x, r.row_ids, r.P, recipe, ws)
     two = torch.empty_like(one)
-    fp4.fp4_grouped_gemm_quantized(ws, r.offsets, bank.w, bank.sc, bank.scale2, recipe, two)
+    fp4.fp4_grouped_gemm_quantized(ws, T, r.row_ids, r.offsets, bank.w, bank.sc, bank.scale2,
+                                   recipe, two)
     assert torch.equal(one, two)
     other = synth.make_bank(recipe, bank.E, bank.n, k, 977, DEV, scale2_value=1.0 / 64.0)
     three = torch.empty_like(one)
-    fp4.fp4_grouped_gemm_quantized(ws, r.offsets, other.w, other.sc, other.scale2, recipe, three)
+    fp4.fp4_grouped_gemm_quantized(ws, T, r.row_ids, r.offsets, other.w, other.sc, other.scale2,
+                                   recipe, three)
     proj2 = synth.Projection("second bank", proj.x, r, other)
     grouped_sampled_check(proj2, three, fp4.PATH_TC, np.arange(r.P), "second bank")
     assert fp4.fp4_get_device_error() == 0
