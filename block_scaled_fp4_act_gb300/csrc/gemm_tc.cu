@@ -71,11 +71,11 @@ constexpr int W_STAGES = 5;   // weight ring slots (20 k-stages ahead): it strea
 constexpr int A_STAGES = 4;   // converted weight tiles, in tensor memory
 constexpr int B_STAGES = 4;   // activation tiles (mostly L2 hits: shared by a tile's neighbours)
 constexpr int kMaxExperts = 1024;
-// Converter warps per TMEM lane quarter; two of them (one per 32-k half) convert each
-// k-stage, so kConvPerQuarter / 2 pairs take turns over the stages.
+// Converter warps per TMEM lane quarter; one of them converts each k-stage of the
+// quarter's 32 weight rows, so they take turns over the stages.
 constexpr int kConvPerQuarter = 4;
-constexpr int kConvTurns = kConvPerQuarter / 2;
-constexpr int kConvPerStage = 8;  // two converter warps per TMEM lane quarter per k-stage
+constexpr int kConvTurns = kConvPerQuarter;
+constexpr int kConvPerStage = 4;  // one converter warp per TMEM lane quarter per k-stage
 constexpr int kThreads = (8 + 4 * kConvPerQuarter) * 32;
 // Warp roles. Warp w issues on SM sub-partition w % 4 and reaches TMEM lanes 32 * (w % 4)
 // .. + 31 only, so every sub-partition holds one epilogue warp and four converter warps
@@ -255,6 +255,21 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
                  "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
                  "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
                  "r"(v[14]), "r"(v[15])
+                 : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Thirty-two 32-bit columns of this warp's 32 TMEM lanes (thread i -> lane base + i).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, "
+                 "%9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, "
+                 "%25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                 "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
+                 "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]),
+                 "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]),
+                 "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
                  : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -684,54 +699,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------- converters
         // Warp w writes TMEM lane quarter q = w % 4 (the only lanes its tcgen05.st reaches):
         // lane i converts weight row 32 q + i. The four converter warps of a quarter take
-        // turns: h = 0, 1 convert the even k-stages, h = 2, 3 the odd ones, each the 32-k
-        // half c = h & 1 of the stage (one 16-byte nibble chunk, 16 TMEM columns).
-        const int q = warp & 3, h = (warp - 8) >> 2, c = h & 1;
+        // turns over the k-stages (h = 0 .. 3 converts stages h, h + 4, ...), each the whole
+        // 64-k stage of its rows: two 16-byte nibble chunks, one 32-column tensor-memory store.
+        const int q = warp & 3, h = (warp - 8) >> 2;
         const int r = q * 32 + lane;
-        const uint32_t a_lane = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(kACol + c * 16);
+        const uint32_t a_lane = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)kACol;
         const int ntiles = (int)blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
         const int nst = ntiles * nkb;
         // g: this CTA's k-stage sequence over its tiles. Every tile has a multiple of W_KS
-        // stages, so W slot g / W_KS holds stage g as its sub-stage g % W_KS.
-        for (int g = h >> 1; g < nst; g += kConvTurns) {
-            const int kb = g % nkb;
-            const int wseq = g / W_KS, wslot = wseq % W_STAGES;
-            const int aslot = g % A_STAGES;
-            const uint32_t wphase = (uint32_t)(wseq / W_STAGES) & 1u;
-            const uint32_t aphase = (uint32_t)(g / A_STAGES) & 1u;
+        // stages, so W slot g / W_KS holds stage g as its sub-stage g % W_KS; kConvTurns is a
+        // multiple of W_KS, so this warp always takes the same sub-stage of a slot.
+        static_assert(kConvTurns % W_KS == 0 && kConvTurns % A_STAGES == 0, "converter turns");
+        const int sub = h % W_KS, aslot = h % A_STAGES;
+        const uint8_t *const nib_row = ringW + r * 128;
+        const int off0 = ((2 * sub) ^ (r & 7)) << 4, off1 = ((2 * sub + 1) ^ (r & 7)) << 4;
+        int wslot = 0;
+        uint32_t wphase = 0, aphase = 0;
+        for (int g = h; g < nst; g += kConvTurns) {
             if (!mbar_wait(wfull(wslot), wphase, abort_flag, p.err))
                 break;
             const uint8_t *w = ringW + wslot * W_BYTES;
             // row r of the nibble box is 128 bytes in the 128-byte swizzle: its 16-byte chunk
             // j (32 k) sits at chunk j ^ (r & 7); a warp's 32 rows then read conflict-free
-            const int chunk = 2 * (g % W_KS) + c;
-            const uint4 nv = *reinterpret_cast<const uint4 *>(w + r * 128 + ((chunk ^ (r & 7)) << 4));
-            uint32_t o[16];
+            const uint4 n0 = *reinterpret_cast<const uint4 *>(nib_row + wslot * W_BYTES + off0);
+            const uint4 n1 = *reinterpret_cast<const uint4 *>(nib_row + wslot * W_BYTES + off1);
+            uint32_t o[32];
             uint4 *o4 = reinterpret_cast<uint4 *>(o);
+            // the slot's 16 scale bytes of row r cover 256 k (NVFP4) or 512 k (MXFP4, the slot
+            // being one half of them: the half of the even/odd slot of a 512-k pair)
             if (gs == 16) {
-                // scales of k-groups 2c and 2c + 1 of this stage (16 per slab row)
-                const uint32_t s01 = *reinterpret_cast<const uint16_t *>(
-                    w + NIB_BYTES + r * 16 + (((kb * BK) >> 4) & 15) + 2 * c);
+                const uint32_t s4 = *reinterpret_cast<const uint32_t *>(w + NIB_BYTES + r * 16 + 4 * sub);
                 if (f16_route) {
-                    const uint32_t h0 = e4m3x2_to_f16x2((s01 & 0xFFu) * 0x101u);
-                    const uint32_t h1 = e4m3x2_to_f16x2((s01 >> 8) * 0x101u);
-                    e2m1x8_scaled_f16(nv.x, h0, o4[0]);
-                    e2m1x8_scaled_f16(nv.y, h0, o4[1]);
-                    e2m1x8_scaled_f16(nv.z, h1, o4[2]);
-                    e2m1x8_scaled_f16(nv.w, h1, o4[3]);
+                    const uint32_t h0 = e4m3x2_to_f16x2((s4 & 0xFFu) * 0x101u);
+                    const uint32_t h1 = e4m3x2_to_f16x2(((s4 >> 8) & 0xFFu) * 0x101u);
+                    const uint32_t h2 = e4m3x2_to_f16x2(((s4 >> 16) & 0xFFu) * 0x101u);
+                    const uint32_t h3 = e4m3x2_to_f16x2((s4 >> 24) * 0x101u);
+                    e2m1x8_scaled_f16(n0.x, h0, o4[0]);
+                    e2m1x8_scaled_f16(n0.y, h0, o4[1]);
+                    e2m1x8_scaled_f16(n0.z, h1, o4[2]);
+                    e2m1x8_scaled_f16(n0.w, h1, o4[3]);
+                    e2m1x8_scaled_f16(n1.x, h2, o4[4]);
+                    e2m1x8_scaled_f16(n1.y, h2, o4[5]);
+                    e2m1x8_scaled_f16(n1.z, h3, o4[6]);
+                    e2m1x8_scaled_f16(n1.w, h3, o4[7]);
                 } else {
-                    const float f0 = e4m3_to_f32(s01 & 0xFFu), f1 = e4m3_to_f32(s01 >> 8);
-                    e2m1x8_scaled_bf16(nv.x, f0, o4[0]);
-                    e2m1x8_scaled_bf16(nv.y, f0, o4[1]);
-                    e2m1x8_scaled_bf16(nv.z, f1, o4[2]);
-                    e2m1x8_scaled_bf16(nv.w, f1, o4[3]);
+                    const float f0 = e4m3_to_f32(s4 & 0xFFu), f1 = e4m3_to_f32((s4 >> 8) & 0xFFu);
+                    const float f2 = e4m3_to_f32((s4 >> 16) & 0xFFu), f3 = e4m3_to_f32(s4 >> 24);
+                    e2m1x8_scaled_bf16(n0.x, f0, o4[0]);
+                    e2m1x8_scaled_bf16(n0.y, f0, o4[1]);
+                    e2m1x8_scaled_bf16(n0.z, f1, o4[2]);
+                    e2m1x8_scaled_bf16(n0.w, f1, o4[3]);
+                    e2m1x8_scaled_bf16(n1.x, f2, o4[4]);
+                    e2m1x8_scaled_bf16(n1.y, f2, o4[5]);
+                    e2m1x8_scaled_bf16(n1.z, f3, o4[6]);
+                    e2m1x8_scaled_bf16(n1.w, f3, o4[7]);
                 }
             } else {
-                const float f = e8m0_to_f32(w[NIB_BYTES + r * 16 + (((kb * BK) >> 5) & 15) + c]);
-                e2m1x8_scaled_bf16(nv.x, f, o4[0]);
-                e2m1x8_scaled_bf16(nv.y, f, o4[1]);
-                e2m1x8_scaled_bf16(nv.z, f, o4[2]);
-                e2m1x8_scaled_bf16(nv.w, f, o4[3]);
+                // the box at x = (8 slot) & ~15 puts this slot's 8 bytes at 8 (slot & 1)
+                const int kb = g % nkb;
+                const uint32_t s2 = *reinterpret_cast<const uint16_t *>(
+                    w + NIB_BYTES + r * 16 + ((2 * kb) & 15));
+                const float f0 = e8m0_to_f32(s2 & 0xFFu), f1 = e8m0_to_f32(s2 >> 8);
+                e2m1x8_scaled_bf16(n0.x, f0, o4[0]);
+                e2m1x8_scaled_bf16(n0.y, f0, o4[1]);
+                e2m1x8_scaled_bf16(n0.z, f0, o4[2]);
+                e2m1x8_scaled_bf16(n0.w, f0, o4[3]);
+                e2m1x8_scaled_bf16(n1.x, f1, o4[4]);
+                e2m1x8_scaled_bf16(n1.y, f1, o4[5]);
+                e2m1x8_scaled_bf16(n1.z, f1, o4[6]);
+                e2m1x8_scaled_bf16(n1.w, f1, o4[7]);
             }
             // Release the weight slot once its values are consumed, behind an async-proxy
             // fence that orders these reads before the TMA refill. (Arriving right after
@@ -744,11 +780,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(aempty(aslot), aphase ^ 1u, abort_flag, p.err))
                 break;
             tc_fence_after();
-            tmem_st16(a_lane + (uint32_t)(aslot * (BK / 2)), o);
+            tmem_st32(a_lane + (uint32_t)(aslot * (BK / 2)), o);
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(afull(aslot));
+            // next stage g + kConvTurns: W slot sequence + kConvTurns / W_KS, A slot the same
+            // (kConvTurns is a multiple of A_STAGES), the A phase flips every kConvTurns /
+            // A_STAGES uses
+            for (int i = 0; i < kConvTurns / W_KS; ++i)
+                if (++wslot == W_STAGES) {
+                    wslot = 0;
+                    wphase ^= 1u;
+                }
+            aphase ^= (uint32_t)((kConvTurns / A_STAGES) & 1);
         }
     } else if (role == ROLE_EPI) {
         // ---------------------------------------------------------- epilogue
