@@ -176,7 +176,8 @@ class ClockSampler:
 # Source files each measured kernel is built from: a traffic figure stays valid only while
 # these are unchanged.
 KERNEL_SOURCES = {
-    "tc_grouped_gemm": ["gemm_tc.cu", "common.cuh", "internal.h", "tma_host.h"],
+    "tc_grouped_gemm": ["gemm_tc.cu", "common.cuh", "tcgen05.cuh", "internal.h", "tma_host.h"],
+    "mx_grouped_gemm": ["gemm_mx.cu", "common.cuh", "tcgen05.cuh", "internal.h", "tma_host.h"],
     "stream_gemm": ["gemm_stream.cu", "common.cuh", "internal.h"],
     "decode_mma": ["gemm_decode.cu", "common.cuh", "internal.h"],
 }

@@ -30,6 +30,36 @@ size_t tc_workspace_bytes(int64_t num_tokens, int64_t total_rows, int64_t k, int
 bool tc_supported(int64_t n, int64_t k, int recipe, int E);
 cudaError_t launch_tc_quantize(const GroupedProblem &p, void *workspace, cudaStream_t s);
 cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaStream_t s);
+size_t mx_workspace_bytes(int64_t num_tokens, int64_t total_rows, int64_t k);
+bool mx_supported(int64_t n, int64_t k, int E, const void *w);
+cudaError_t launch_mx_quantize(const GroupedProblem &p, void *workspace, cudaStream_t s);
+cudaError_t launch_mx_gemm(const GroupedProblem &p, const void *workspace, cudaStream_t s);
+
+// The tensor-core path by recipe: NVFP4 on the 16-bit MMA with converted weights, MXFP4 on
+// the block-scaled 8-bit MMA (weights as stored, e4m3 activation codes).
+static size_t tc_path_workspace(int64_t T, int64_t P, int64_t k, int recipe)
+{
+    return recipe == FP4_MXFP4 ? mx_workspace_bytes(T, P, k) : tc_workspace_bytes(T, P, k, recipe);
+}
+
+static cudaError_t tc_path_quantize(const GroupedProblem &p, void *ws, cudaStream_t s)
+{
+    return p.recipe == FP4_MXFP4 ? launch_mx_quantize(p, ws, s) : launch_tc_quantize(p, ws, s);
+}
+
+static cudaError_t tc_path_gemm(const GroupedProblem &p, const void *ws, cudaStream_t s)
+{
+    return p.recipe == FP4_MXFP4 ? launch_mx_gemm(p, ws, s) : launch_tc_gemm(p, ws, s);
+}
+
+// Shapes (and, for MXFP4, the weight alignment the packed 4-bit TMA form needs) the
+// tensor-core path takes.
+static bool tc_path_supported(int64_t n, int64_t k, int recipe, int E, const void *w)
+{
+    if (!tc_supported(n, k, recipe, E))
+        return false;
+    return recipe != FP4_MXFP4 || mx_supported(n, k, E, w);
+}
 double tc_error_ops(int recipe, int64_t k);
 
 // Path forced by fp4_force_path for calls made on the same host thread.
@@ -79,6 +109,16 @@ static int choose_path(int64_t P, int E, int64_t n, int64_t k, int recipe, bool 
     return FP4_PATH_STREAM;
 }
 
+// As choose_path, for a call whose weights are known (MXFP4 also needs them 32-byte aligned).
+static int choose_path_for(const GroupedProblem &p, bool have_ws)
+{
+    const int path = choose_path(p.P, p.E, p.n, p.k, p.recipe, have_ws);
+    if (path == FP4_PATH_TC && g_forced_path != FP4_PATH_TC &&
+        !tc_path_supported(p.n, p.k, p.recipe, p.E, p.w))
+        return FP4_PATH_STREAM;
+    return path;
+}
+
 // The path that needs no workspace: the warp-MMA decode kernel wherever 4 activation rows
 // of length k fit in its shared memory (k <= 28544; 8 rows per pass where they fit and
 // experts average more than 4), the FMA streaming kernel (1-2 rows per pass) beyond.
@@ -110,11 +150,13 @@ static int run_grouped(GroupedProblem p, void *workspace, size_t ws_bytes, cudaS
         return record(cudaGetLastError() != cudaSuccess ? cudaGetLastError()
                                                           : cudaErrorInvalidDevice);
     const bool have_ws =
-        workspace != nullptr && ws_bytes >= tc_workspace_bytes(p.T, p.P, p.k, p.recipe);
-    const int path = choose_path(p.P, p.E, p.n, p.k, p.recipe, have_ws);
+        workspace != nullptr && ws_bytes >= tc_path_workspace(p.T, p.P, p.k, p.recipe);
+    const int path = choose_path_for(p, have_ws);
     if (path == FP4_PATH_TC) {
         if (!tc_supported(p.n, p.k, p.recipe, p.E))
             return FP4_ERR_SHAPE;
+        if (!tc_path_supported(p.n, p.k, p.recipe, p.E, p.w))
+            return FP4_ERR_ALIGN;
         if (!have_ws)
             return FP4_ERR_WORKSPACE;
         if (p.codes_out) {  // the codes are not a by-product of the quantise pass: one act_quant
@@ -122,10 +164,10 @@ static int run_grouped(GroupedProblem p, void *workspace, size_t ws_bytes, cudaS
             if (st != FP4_OK)
                 return st;
         }
-        const int st = record(launch_tc_quantize(p, workspace, s));
+        const int st = record(tc_path_quantize(p, workspace, s));
         if (st != FP4_OK)
             return st;
-        return record(launch_tc_gemm(p, workspace, s));
+        return record(tc_path_gemm(p, workspace, s));
     }
     return record(launch_streaming(p, s));
 }
@@ -232,7 +274,7 @@ size_t fp4_grouped_workspace_size(int64_t num_tokens, int64_t total_rows, int64_
         return 0;
     if (!tc_supported(n, k, recipe, 1))
         return 0;  // the shape always takes the streaming path, which needs no workspace
-    return tc_workspace_bytes(num_tokens, total_rows, k, recipe);
+    return tc_path_workspace(num_tokens, total_rows, k, recipe);
 }
 
 int fp4_grouped_expert_gemm(const float *x, int64_t num_tokens, const int32_t *row_ids,
@@ -288,7 +330,7 @@ static int check_tc_call(int recipe, int64_t num_tokens, const int32_t *row_ids,
     if (!row_ids && num_tokens < total_rows)
         return FP4_ERR_SHAPE;
     if (total_rows > 0 &&
-        (!ws || ws_bytes < tc_workspace_bytes(num_tokens, total_rows, k, recipe)))
+        (!ws || ws_bytes < tc_path_workspace(num_tokens, total_rows, k, recipe)))
         return FP4_ERR_WORKSPACE;
     return FP4_OK;
 }
@@ -319,7 +361,7 @@ int fp4_grouped_quantize(const float *x, int64_t num_tokens, const int32_t *row_
     p.err = device_error_word();
     if (!p.err)
         return record(cudaErrorInvalidDevice);
-    return record(launch_tc_quantize(p, workspace, (cudaStream_t)stream));
+    return record(tc_path_quantize(p, workspace, (cudaStream_t)stream));
 }
 
 int fp4_grouped_gemm_quantized(const void *workspace, size_t workspace_bytes,
@@ -340,7 +382,8 @@ int fp4_grouped_gemm_quantized(const void *workspace, size_t workspace_bytes,
         return FP4_OK;
     if (!offsets || !w || !wscale || !out || (recipe == FP4_NVFP4 && !scale2))
         return FP4_ERR_ARG;
-    if (!aligned16(w) || !aligned16(wscale) || !aligned16(out))
+    if (!aligned16(w) || !aligned16(wscale) || !aligned16(out) ||
+        !tc_path_supported(n, k, recipe, num_experts, w))
         return FP4_ERR_ALIGN;
     GroupedProblem p{};
     p.T = num_tokens;
@@ -359,7 +402,7 @@ int fp4_grouped_gemm_quantized(const void *workspace, size_t workspace_bytes,
     p.err = device_error_word();
     if (!p.err)
         return record(cudaErrorInvalidDevice);
-    return record(launch_tc_gemm(p, workspace, (cudaStream_t)stream));
+    return record(tc_path_gemm(p, workspace, (cudaStream_t)stream));
 }
 
 int fp4_route_topk(const float *logits, int64_t num_tokens, int num_experts, int topk,

@@ -49,6 +49,7 @@
 // use (a bounded wait on the slot's empty barrier), and then releases the next tile's
 // first stage with a row count of -1, which stops the MMA warp.
 #include "common.cuh"
+#include "tcgen05.cuh"
 #include "tma_host.h"
 
 #include <cuda.h>
@@ -151,90 +152,11 @@ __device__ __forceinline__ int64_t offset_at(const Params &p, int e)
     return p.offsets ? (int64_t)__ldg(p.offsets + e) : (e == 0 ? 0 : p.P);
 }
 
-// ------------------------------------------------------------------ PTX wrappers
+// ------------------------------------------------------------------ kind::f16 MMA
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-// Whole-warp forms: lane 0 waits, the warp takes its answer (keeps the warp converged).
-__device__ __forceinline__ bool warp_mbar_wait(uint32_t bar, uint32_t parity,
-                                               volatile int *abort_flag, unsigned *err)
-{
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0)
-        ok = mbar_wait(bar, parity, abort_flag, err);
-    return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-}
-
-__device__ __forceinline__ bool warp_mbar_drain(uint32_t bar, uint32_t parity)
-{
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0)
-        ok = mbar_drain(bar, parity);
-    return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            int z, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                 " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before()
-{
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tc_fence_after()
-{
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
-{
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     dst_smem),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
-{
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 operands, f32 accumulator.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-
-// Warp-collective forms for a converged warp: one elected lane issues. Operands computed
-// by the whole warp stay warp-uniform, which keeps the issue loop short.
-__device__ __forceinline__ void mma_f16kind_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                                 uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
-                 "setp.ne.b32 p, %4, 0;\n\t"
-                 "elect.sync r|e, 0xffffffff;\n\t"
-                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-
-// As mma_f16kind_warp with the A operand in tensor memory (a_tmem: lane 0, first column).
+// One elected lane of a converged warp issues D[tmem] (+)= A[tmem] * B[smem]^T (kind::f16,
+// f32 accumulator; a_tmem: lane 0, first column). Operands computed by the whole warp stay
+// warp-uniform, which keeps the issue loop short.
 __device__ __forceinline__ void mma_f16kind_tmem_a_warp(uint32_t d_tmem, uint32_t a_tmem,
                                                         uint64_t b_desc, uint32_t idesc,
                                                         uint32_t accumulate)
@@ -245,78 +167,6 @@ __device__ __forceinline__ void mma_f16kind_tmem_a_warp(uint32_t d_tmem, uint32_
                  "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
                  "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
                  : "memory");
-}
-
-// Sixteen 32-bit columns of this warp's 32 TMEM lanes (thread i -> lane base + i).
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16])
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, "
-                 "%9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
-                 "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
-                 "r"(v[14]), "r"(v[15])
-                 : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// Thirty-two 32-bit columns of this warp's 32 TMEM lanes (thread i -> lane base + i).
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32])
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, "
-                 "%9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, "
-                 "%25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
-                 "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
-                 "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]),
-                 "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]),
-                 "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-                 : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void mma_commit_warp(uint32_t bar)
-{
-    asm volatile("{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
-                 "elect.sync r|e, 0xffffffff;\n\t"
-                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                 "\n\t}" ::"r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
-{
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, "
-                 "%9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, "
-                 "%25, %26, %27, %28, %29, %30, %31}, [%32];"
-                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
-                   "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),
-                   "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]),
-                   "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
-                   "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
-                   "=r"(v[30]), "=r"(v[31])
-                 : "r"(taddr)
-                 : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle layout
-// (8-row groups of 128-byte rows, 16-byte chunks XOR-ed with the row index mod 8),
-// stride between 8-row groups 1024 bytes, tcgen05 descriptor version 1.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr)
-{
-    uint64_t d = (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)(16u >> 4) << 16;    // leading byte offset (unused for swizzled K-major)
-    d |= (uint64_t)(1024u >> 4) << 32;  // stride byte offset
-    d |= (uint64_t)1 << 46;             // descriptor version
-    d |= (uint64_t)2 << 61;             // 128-byte swizzle
-    return d;
 }
 
 // Instruction descriptor of kind::f16: f32 accumulator, A and B both bf16 (fmt 1) or both
@@ -412,19 +262,6 @@ __device__ __forceinline__ Tile tile_at(int t, const int *prefix, const Params &
 
 // ------------------------------------------------------------------ the kernel
 
-// Ring cursor: slot index and phase parity of a stage sequence over an N-slot ring.
-template <int N>
-struct Ring {
-    int slot = 0;
-    uint32_t phase = 0;
-    __device__ __forceinline__ void next()
-    {
-        if (++slot == N) {
-            slot = 0;
-            phase ^= 1u;
-        }
-    }
-};
 
 // Activation tensor maps for tiles of <= 32, 64, 128 and 256 rows: 3-D views {64 k,
 // rows, k-blocks} of the [P, k] bf16 workspace with boxes {64, 32 << i, 8 >> i}.
@@ -1275,6 +1112,10 @@ static uint8_t *noalloc_scratch(cudaError_t *status)
 }
 
 void set_last_error(const char *msg);
+size_t mx_workspace_bytes(int64_t num_tokens, int64_t total_rows, int64_t k);
+bool mx_supported(int64_t n, int64_t k, int E, const void *w);
+cudaError_t launch_mx_quantize(const GroupedProblem &p, void *workspace, cudaStream_t s);
+cudaError_t launch_mx_gemm(const GroupedProblem &p, const void *workspace, cudaStream_t s);
 
 } // namespace fp4moe
 
@@ -1303,7 +1144,10 @@ extern "C" int fp4_grouped_expert_gemm_noalloc(const float *x, int64_t num_token
         return FP4_ERR_ALIGN;
     if (!tc_supported(n, k, recipe, num_experts))
         return FP4_ERR_SHAPE;
-    const size_t need = tc_workspace_bytes(num_tokens, total_rows, k, recipe);
+    if (recipe == FP4_MXFP4 && !mx_supported(n, k, num_experts, w))
+        return FP4_ERR_ALIGN;
+    const size_t need = recipe == FP4_MXFP4 ? mx_workspace_bytes(num_tokens, total_rows, k)
+                                            : tc_workspace_bytes(num_tokens, total_rows, k, recipe);
     if (need > kNoAllocScratchBytes) {
         char msg[256];
         snprintf(msg, sizeof(msg),
@@ -1342,9 +1186,12 @@ extern "C" int fp4_grouped_expert_gemm_noalloc(const float *x, int64_t num_token
     p.err = device_error_word();
     if (!p.err)
         return FP4_ERR_LAUNCH;
-    cudaError_t e = launch_tc_quantize(p, scratch, (cudaStream_t)stream);
+    const bool mxr = recipe == FP4_MXFP4;
+    cudaError_t e = mxr ? launch_mx_quantize(p, scratch, (cudaStream_t)stream)
+                        : launch_tc_quantize(p, scratch, (cudaStream_t)stream);
     if (e == cudaSuccess)
-        e = launch_tc_gemm(p, scratch, (cudaStream_t)stream);
+        e = mxr ? launch_mx_gemm(p, scratch, (cudaStream_t)stream)
+                : launch_tc_gemm(p, scratch, (cudaStream_t)stream);
     if (e != cudaSuccess) {
         char msg[256];
         snprintf(msg, sizeof(msg), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
