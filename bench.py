@@ -178,6 +178,7 @@ class ClockSampler:
 KERNEL_SOURCES = {
     "tc_grouped_gemm": ["gemm_tc.cu", "common.cuh", "tcgen05.cuh", "internal.h", "tma_host.h"],
     "mx_grouped_gemm": ["gemm_mx.cu", "common.cuh", "tcgen05.cuh", "internal.h", "tma_host.h"],
+    "tc_quantize": ["gemm_tc.cu", "common.cuh", "internal.h"],
     "stream_gemm": ["gemm_stream.cu", "common.cuh", "internal.h"],
     "decode_mma": ["gemm_decode.cu", "common.cuh", "internal.h"],
 }
