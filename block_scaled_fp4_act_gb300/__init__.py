@@ -89,6 +89,8 @@ def lib():
         L.fp4_error_ops.restype = ctypes.c_double
         L.fp4_force_path.argtypes = [i32]
         L.fp4_force_path.restype = None
+        L.fp4_test_stall_next_gemm.argtypes = [i64]
+        L.fp4_test_stall_next_gemm.restype = None
         L.fp4_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
         L.fp4_get_device_error.restype = i32
         L.fp4_last_error.argtypes = []
@@ -405,6 +407,12 @@ def fp4_error_ops(path, recipe, k):
 
 def fp4_force_path(path):
     lib().fp4_force_path(int(path))
+
+
+def fp4_test_stall_next_gemm(wait_limit_cycles):
+    """Test hook: the next tensor-core GEMM launched from this thread stalls one pipeline
+    wait, gives up after wait_limit_cycles and reports FP4_DEVERR_TIMEOUT."""
+    lib().fp4_test_stall_next_gemm(int(wait_limit_cycles))
 
 
 def fp4_get_device_error(stream=None):

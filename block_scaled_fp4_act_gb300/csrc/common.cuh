@@ -212,9 +212,10 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
     return ok != 0;
 }
 
-// Bounded wait. Returns false if this CTA is aborting (flag set here or elsewhere).
+// Bounded wait: gives up after `limit` clock64 cycles, setting the abort flag and the
+// TIMEOUT bit. Returns false if this CTA is aborting (flag set here or elsewhere).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          unsigned *err)
+                                          unsigned *err, long long limit = kTimeoutCycles)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -224,7 +225,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
             return true;
         if (*abort_flag)
             return false;
-        if (clock64() - t0 > kTimeoutCycles) {
+        if (clock64() - t0 > limit) {
             *abort_flag = 1;
             raise_device_error(err, FP4_DEVERR_TIMEOUT);
             return false;

@@ -64,6 +64,18 @@ double tc_error_ops(int recipe, int64_t k);
 
 // Path forced by fp4_force_path for calls made on the same host thread.
 static thread_local int g_forced_path = FP4_PATH_AUTO;
+// Wait limit of a stalled launch requested by fp4_test_stall_next_gemm (0: none).
+static thread_local long long g_stall_limit = 0;
+
+long long take_stall_request(int *stall)
+{
+    const long long limit = g_stall_limit;
+    if (limit <= 0)
+        return kTimeoutCycles;
+    g_stall_limit = 0;
+    *stall = 1;
+    return limit;
+}
 static thread_local char g_last_error[256] = "";
 
 static int record(cudaError_t e)
@@ -487,6 +499,18 @@ double fp4_error_ops(int path, int recipe, int64_t k)
 void fp4_force_path(int path)
 {
     g_forced_path = path == FP4_PATH_STREAM || path == FP4_PATH_TC ? path : FP4_PATH_AUTO;
+}
+
+void fp4_test_stall_next_gemm(int64_t wait_limit_cycles)
+{
+    const long long lo = 1000000LL;  // no wait of a healthy launch comes near this
+    if (wait_limit_cycles <= 0) {
+        g_stall_limit = 0;
+        return;
+    }
+    g_stall_limit = wait_limit_cycles < lo ? lo
+                    : wait_limit_cycles > kTimeoutCycles ? kTimeoutCycles
+                                                         : (long long)wait_limit_cycles;
 }
 
 int fp4_get_device_error(void *stream, unsigned *bits)

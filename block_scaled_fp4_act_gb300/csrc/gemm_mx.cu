@@ -89,6 +89,11 @@ struct Params {
     int mt;
     float *out;
     unsigned *err;
+    // bounded-wait limit in clock64 cycles; stall != 0 (a test request) makes the first
+    // scale-factor warp of CTA 0 withhold its first arrival, so this launch times out and
+    // aborts
+    long long wait_limit;
+    int stall;
 };
 
 __device__ __forceinline__ int64_t offset_at(const Params &p, int e)
@@ -296,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int x16 = (int)(tl.row0 & ~(int64_t)15);
                 for (int kb = 0; kb < nkb && ok; ++kb) {
                     if (kb % kbps == 0) {
-                        if (!mbar_wait(bempty(slot), phase ^ 1u, abort_flag, p.err)) {
+                        if (!mbar_wait(bempty(slot), phase ^ 1u, abort_flag, p.err, p.wait_limit)) {
                             ok = false;
                             break;
                         }
@@ -310,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             phase ^= 1u;
                         }
                     }
-                    if (!mbar_wait(sbempty(sslot), sphase ^ 1u, abort_flag, p.err)) {
+                    if (!mbar_wait(sbempty(sslot), sphase ^ 1u, abort_flag, p.err, p.wait_limit)) {
                         ok = false;
                         break;
                     }
@@ -343,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Tile tl = tile_at(t, prefix, p);
                 const int yw = tl.e * p.n + tl.m * BM;
                 for (int kb = 0; kb < nkb; ++kb) {
-                    if (!mbar_wait(wempty(slot), phase ^ 1u, abort_flag, p.err)) {
+                    if (!mbar_wait(wempty(slot), phase ^ 1u, abort_flag, p.err, p.wait_limit)) {
                         ok = false;
                         break;
                     }
@@ -426,16 +431,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Tile tl = tile_at(t, prefix, p);
             const int buf = it & 1;
             tile_info[it % kTileInfo] = tl.rows;
-            bool ok = warp_mbar_wait(acce(buf), ((it >> 1) & 1) ^ 1u, abort_flag, p.err);
+            bool ok = warp_mbar_wait(acce(buf), ((it >> 1) & 1) ^ 1u, abort_flag, p.err, p.wait_limit);
             const int kbmask = bmap_kblocks(bmap_index(tl.rows)) - 1;
             for (int kb = 0; kb < nkb; ++kb) {
                 const int j = kb & kbmask;
                 if (ok && j == 0)
-                    ok = warp_mbar_wait(bfull(rb.slot), rb.phase, abort_flag, p.err);
+                    ok = warp_mbar_wait(bfull(rb.slot), rb.phase, abort_flag, p.err, p.wait_limit);
                 if (ok)
-                    ok = warp_mbar_wait(wfull(rw.slot), rw.phase, abort_flag, p.err);
+                    ok = warp_mbar_wait(wfull(rw.slot), rw.phase, abort_flag, p.err, p.wait_limit);
                 if (ok)
-                    ok = warp_mbar_wait(sffull(rf.slot), rf.phase, abort_flag, p.err);
+                    ok = warp_mbar_wait(sffull(rf.slot), rf.phase, abort_flag, p.err, p.wait_limit);
                 if (!ok) {
                     aborted = true;
                     if (!warp_mbar_drain(sfempty(rf.slot), rf.phase ^ 1u)) {
@@ -477,8 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int xoff = (int)(tl.row0 & 15);
             // g is the next stage of this turn; tile ti holds stages ti * nkb .. + nkb - 1
             for (int kb = g - ti * nkb; kb < nkb; kb += kSfTurns) {
-                if (!mbar_wait(wfull(ws), wph, abort_flag, p.err) ||
-                    !mbar_wait(sbfull(ss), sph, abort_flag, p.err)) {
+                if (!mbar_wait(wfull(ws), wph, abort_flag, p.err, p.wait_limit) ||
+                    !mbar_wait(sbfull(ss), sph, abort_flag, p.err, p.wait_limit)) {
                     ok = false;
                     break;
                 }
@@ -498,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(wempty(ws));
                     mbar_arrive(sbempty(ss));
                 }
-                if (!mbar_wait(sfempty(fs), fph ^ 1u, abort_flag, p.err)) {
+                if (!mbar_wait(sfempty(fs), fph ^ 1u, abort_flag, p.err, p.wait_limit)) {
                     ok = false;
                     break;
                 }
@@ -509,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0)
+                if (lane == 0 && !(p.stall && blockIdx.x == 0 && warp == 8 && g == h))
                     mbar_arrive(sffull(fs));
                 // next stage of this turn: kSfTurns stages later
                 g += kSfTurns;
@@ -537,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
             const Tile tl = tile_at(t, prefix, p);
             const int buf = it & 1;
-            if (!mbar_wait(accf(buf), (it >> 1) & 1, abort_flag, p.err))
+            if (!mbar_wait(accf(buf), (it >> 1) & 1, abort_flag, p.err, p.wait_limit))
                 break;
             tc_fence_after();
             const int col = tl.m * BM + q * 32 + lane;
@@ -772,6 +777,8 @@ cudaError_t launch_mx_gemm(const GroupedProblem &p, const void *workspace, cudaS
     kp.mt = (p.n + BM - 1) / BM;
     kp.out = p.out;
     kp.err = p.err;
+    kp.stall = 0;
+    kp.wait_limit = take_stall_request(&kp.stall);
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);

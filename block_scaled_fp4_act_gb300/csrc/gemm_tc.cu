@@ -1,35 +1,38 @@
-// gemm_tc.cu -- tensor-core grouped expert GEMM for prefill-sized row counts (sm_103a:
-// TMA, mbarrier pipeline, tcgen05.mma with the accumulator in tensor memory).
+// gemm_tc.cu -- NVFP4 tensor-core grouped expert GEMM for prefill-sized row counts
+// (sm_103a: TMA, mbarrier pipeline, tcgen05.mma with the accumulator in tensor memory),
+// its quantise pass, and the allocation-free entry point.
 //
 // Arithmetic (memra-engine 0.98.0, src/bin/dsv4_native_gemm_gate.rs, fn f64_ref): every
 // product e4m3(a) * s_a * E2M1(w) * ws is formed exactly and summed in f32. The MMA
-// kind that accepts FP8 A operands has only ue8m0 scales per 32, and the kind with e4m3
-// scales per 16 wants FP4 on both sides, so the exact route on this hardware is the bf16
-// MMA (kind::f16): both operands carry their scales and stay exact in bf16.
-//   A (M side) = weights:     bf16(E2M1 * e4m3 scale)  NVFP4 (<= 6 significant bits;
-//                             f16 on the f16 route below)
-//                             bf16(E2M1 * 2^(e-127))   MXFP4
-//   B (N side) = activations: bf16(e4m3 code * pow2 scale), written by the quantise pass
-//   D (TMEM)   = f32 [128 weight rows x N routed rows]; epilogue multiplies by scale2.
+// kind that accepts FP8 operands has only ue8m0 scales per 32, and the kind with e4m3
+// scales per 16 wants FP4 on both sides, so the exact route for NVFP4 on this hardware is
+// the 16-bit MMA (kind::f16): both operands carry their scales and stay exact.
+//   A (M side) = weights:     f16(E2M1 * e4m3 scale) on the f16 route, bf16 otherwise
+//                             (<= 6 significant bits either way)
+//   B (N side) = activations: f16(code * 2^(m - M)) or bf16(code * 2^m), written by the
+//                             quantise pass (M: the routed row's largest block exponent)
+//   D (TMEM)   = f32 [128 weight rows x N routed rows]; the epilogue multiplies by the
+//                row scale 2^M (f16 route) and scale2.
+// (MXFP4 runs on the block-scaled 8-bit MMA instead: gemm_mx.cu.)
 //
 // Kernel structure: persistent, one CTA (24 warps) per SM, static round-robin over
 // tiles (expert, 192-row block of its routed rows, 128-row block of its weights),
 // weight-row block fastest so consecutive tiles share the activation block in L2.
-// Rings decouple the streams: a 14-deep shared-memory weight ring (nibbles + scales,
-// 6 KB a stage: weights stream from HBM once per tile), a 4-deep activation ring in
-// shared memory and a 4-deep ring of converted weight tiles in tensor memory. The MMA
-// reads its A operand (the converted weights) from tensor memory: shared memory then
-// carries only the activation tiles, the raw weights and their TMA writes, and its
-// bandwidth (about 70% busy when the converted weights went through it too) stops
-// being the limit.
+// Rings decouple the streams: a 5-slot shared-memory weight ring (each slot 256 k of the
+// tile's 128 weight rows: 128-byte nibble lines in the 128-byte swizzle + 16 scale bytes
+// per row; the weights stream from HBM once per tile), a 4-slot activation ring in shared
+// memory and a 4-stage ring of converted 64-k weight stages in tensor memory, from which
+// the MMA reads its A operand.
+//   warp 0      TMA producer of activation slots (16-bit, 128B swizzle, k-block-major)
 //   warp 1      TMEM owner and MMA issuer (whole warp, one elected lane issues), 4 MMAs
 //               of K=16 per stage
-//   warp 3      relay: does the MMA side's mbarrier waits and releases each A slot to
+//   warp 2      TMA producer of the weight slots (nibble box + scale box)
+//   warp 3      relay: does the MMA side's mbarrier waits and releases each A stage to
 //               warp 1 through a hardware named barrier
-//   warp 0      TMA producer of activation slots (bf16, 128B swizzle, k-block-major)
-//   warp 2      TMA producer of nibble (32-byte swizzle) and scale tiles
-//   warps 8-23  converters: nibbles x scales -> 16-bit A operand, tcgen05.st into TMEM
-//   warps 4-7   epilogue: tcgen05.ld of the accumulator, x scale2, coalesced f32 stores
+//   warps 4-7   epilogue: tcgen05.ld of the accumulator, x row scale x scale2, coalesced
+//               f32 stores
+//   warps 8-23  converters, four per TMEM lane quarter taking turns over the k-stages:
+//               nibbles x scales -> 16-bit A operand, tcgen05.st into TMEM
 // Two accumulators (2 x 192 TMEM columns) let the epilogue of one tile overlap the
 // main loop of the next. The MMA N of a tile is its routed-row count rounded up to 16,
 // so an expert's ragged last block costs at most 15 padded rows.
@@ -41,13 +44,14 @@
 // 256 without it). The relay warp takes those waits and passes readiness on with
 // bar.arrive / bar.sync, which do not go through that queue.
 //
-// Every mbarrier wait is bounded (about a second of clock64 cycles); on expiry the CTA
-// sets the TIMEOUT bit of the device error word, stops all roles, waits (bounded) for
-// its own copies and MMAs in flight, frees its tensor memory and returns. The MMA warp's
-// named-barrier waits cannot time out, so on abort the relay keeps releasing slots to the
-// end of the current tile, each only after the MMA warp has consumed the slot's previous
-// use (a bounded wait on the slot's empty barrier), and then releases the next tile's
-// first stage with a row count of -1, which stops the MMA warp.
+// Every mbarrier wait is bounded (about a second of clock64 cycles, or the shorter limit
+// of a test launch); on expiry the CTA sets the TIMEOUT bit of the device error word,
+// stops all roles, waits (bounded) for its own copies and MMAs in flight, frees its
+// tensor memory and returns. The MMA warp's named-barrier waits cannot time out, so on
+// abort the relay keeps releasing stages to the end of the current tile, each only after
+// the MMA warp has consumed the slot's previous use (a bounded wait on the slot's empty
+// barrier), and then releases the next tile's first stage with a row count of -1, which
+// stops the MMA warp.
 #include "common.cuh"
 #include "tcgen05.cuh"
 #include "tma_host.h"
@@ -134,7 +138,6 @@ struct Params {
     int64_t P;
     int n;
     int k;
-    int recipe;
     int mt;  // weight-row blocks per expert
     const float *scale2;  // nullable: scale2_host is used
     float scale2_host;
@@ -144,6 +147,10 @@ struct Params {
     // f16(code * 2^(m - M_p)) and rowscale[p] = 2^M_p; nonzero (or no flag) means bf16.
     const unsigned *route_flag;
     const float *rowscale;
+    // bounded-wait limit in clock64 cycles; stall != 0 (a test request) makes the first
+    // converter warp of CTA 0 withhold its first arrival, so this launch times out and aborts
+    long long wait_limit;
+    int stall;
 };
 
 // CSR offset e, or the single-expert offsets {0, P} when the call has none.
@@ -376,7 +383,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int total = prefix[E];
     const bool f16_route = p.route_flag != nullptr && *((volatile const unsigned *)p.route_flag) == 0u;
     const int nkb = p.k / BK;
-    const int gs = p.recipe == FP4_NVFP4 ? 16 : 32;
     uint8_t *const ringB = smem;
     uint8_t *const ringW = smem + OFF_W;
 
@@ -401,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < nload; ++j) {
                     const uint32_t emp = is_b ? bempty(slot) : wempty(slot);
                     const uint32_t ful = is_b ? bfull(slot) : wfull(slot);
-                    if (!mbar_wait(emp, phase ^ 1u, abort_flag, p.err)) {
+                    if (!mbar_wait(emp, phase ^ 1u, abort_flag, p.err, p.wait_limit)) {
                         ok = false;
                         break;
                     }
@@ -414,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int k0 = j * W_KS * BK;  // first k of the slot
                         mbar_arrive_expect_tx(ful, W_BYTES);
                         tma_load_2d(smem_u32(dst), &tmW, k0 / 2, yw, ful);
-                        tma_load_2d(smem_u32(dst + NIB_BYTES), &tmS, (k0 / gs) & ~15, yw, ful);
+                        tma_load_2d(smem_u32(dst + NIB_BYTES), &tmS, k0 / 16, yw, ful);
                     }
                     issued_mask |= 1u << slot;
                     issued_parity = (issued_parity & ~(1u << slot)) | (phase << slot);
@@ -498,14 +504,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int buf = it & 1;
             // published before the arrival that releases the tile's first stage
             tile_info[it % kTileInfo] = tl.rows;
-            bool ok = warp_mbar_wait(acce(buf), ((it >> 1) & 1) ^ 1u, abort_flag, p.err);
+            bool ok = warp_mbar_wait(acce(buf), ((it >> 1) & 1) ^ 1u, abort_flag, p.err, p.wait_limit);
             const int kbmask = bmap_kblocks(bmap_index(tl.rows)) - 1;
             for (int kb = 0; kb < nkb; ++kb) {
                 const int j = kb & kbmask;
                 if (ok && j == 0)
-                    ok = warp_mbar_wait(bfull(rb.slot), rb.phase, abort_flag, p.err);
+                    ok = warp_mbar_wait(bfull(rb.slot), rb.phase, abort_flag, p.err, p.wait_limit);
                 if (ok)
-                    ok = warp_mbar_wait(afull(ra.slot), ra.phase, abort_flag, p.err);
+                    ok = warp_mbar_wait(afull(ra.slot), ra.phase, abort_flag, p.err, p.wait_limit);
                 if (!ok) {
                     // Aborting: keep the MMA warp moving to the end of this tile, then stop
                     // it at the next tile start. Release a slot only after the MMAs of its
@@ -553,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int wslot = 0;
         uint32_t wphase = 0, aphase = 0;
         for (int g = h; g < nst; g += kConvTurns) {
-            if (!mbar_wait(wfull(wslot), wphase, abort_flag, p.err))
+            if (!mbar_wait(wfull(wslot), wphase, abort_flag, p.err, p.wait_limit))
                 break;
             const uint8_t *w = ringW + wslot * W_BYTES;
             // row r of the nibble box is 128 bytes in the 128-byte swizzle: its 16-byte chunk
@@ -562,9 +568,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint4 n1 = *reinterpret_cast<const uint4 *>(nib_row + wslot * W_BYTES + off1);
             uint32_t o[32];
             uint4 *o4 = reinterpret_cast<uint4 *>(o);
-            // the slot's 16 scale bytes of row r cover 256 k (NVFP4) or 512 k (MXFP4, the slot
-            // being one half of them: the half of the even/odd slot of a 512-k pair)
-            if (gs == 16) {
+            // the slot's 16 scale bytes of row r cover its 256 k; this stage's four are word sub
+            {
                 const uint32_t s4 = *reinterpret_cast<const uint32_t *>(w + NIB_BYTES + r * 16 + 4 * sub);
                 if (f16_route) {
                     const uint32_t h0 = e4m3x2_to_f16x2((s4 & 0xFFu) * 0x101u);
@@ -591,20 +596,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     e2m1x8_scaled_bf16(n1.z, f3, o4[6]);
                     e2m1x8_scaled_bf16(n1.w, f3, o4[7]);
                 }
-            } else {
-                // the box at x = (8 slot) & ~15 puts this slot's 8 bytes at 8 (slot & 1)
-                const int kb = g % nkb;
-                const uint32_t s2 = *reinterpret_cast<const uint16_t *>(
-                    w + NIB_BYTES + r * 16 + ((2 * kb) & 15));
-                const float f0 = e8m0_to_f32(s2 & 0xFFu), f1 = e8m0_to_f32(s2 >> 8);
-                e2m1x8_scaled_bf16(n0.x, f0, o4[0]);
-                e2m1x8_scaled_bf16(n0.y, f0, o4[1]);
-                e2m1x8_scaled_bf16(n0.z, f0, o4[2]);
-                e2m1x8_scaled_bf16(n0.w, f0, o4[3]);
-                e2m1x8_scaled_bf16(n1.x, f1, o4[4]);
-                e2m1x8_scaled_bf16(n1.y, f1, o4[5]);
-                e2m1x8_scaled_bf16(n1.z, f1, o4[6]);
-                e2m1x8_scaled_bf16(n1.w, f1, o4[7]);
             }
             // Release the weight slot once its values are consumed, behind an async-proxy
             // fence that orders these reads before the TMA refill. (Arriving right after
@@ -614,13 +605,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0)
                 mbar_arrive(wempty(wslot));
             // then wait for the A slot: the conversion overlapped the MMAs still reading it
-            if (!mbar_wait(aempty(aslot), aphase ^ 1u, abort_flag, p.err))
+            if (!mbar_wait(aempty(aslot), aphase ^ 1u, abort_flag, p.err, p.wait_limit))
                 break;
             tc_fence_after();
             tmem_st32(a_lane + (uint32_t)(aslot * (BK / 2)), o);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0)
+            if (lane == 0 && !(p.stall && blockIdx.x == 0 && warp == 8 && g == h))
                 mbar_arrive(afull(aslot));
             // next stage g + kConvTurns: W slot sequence + kConvTurns / W_KS, A slot the same
             // (kConvTurns is a multiple of A_STAGES), the A phase flips every kConvTurns /
@@ -639,13 +630,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
             const Tile tl = tile_at(t, prefix, p);
             const int buf = it & 1;
-            if (!mbar_wait(accf(buf), (it >> 1) & 1, abort_flag, p.err))
+            if (!mbar_wait(accf(buf), (it >> 1) & 1, abort_flag, p.err, p.wait_limit))
                 break;
             tc_fence_after();
             const int col = tl.m * BM + q * 32 + lane;
             const bool colok = col < p.n;
-            const float s2 =
-                (gs == 16) ? (p.scale2 ? __ldg(p.scale2 + tl.e) : p.scale2_host) : 1.0f;
+            const float s2 = p.scale2 ? __ldg(p.scale2 + tl.e) : p.scale2_host;
             float *orow = p.out + tl.row0 * (int64_t)p.n + col;
             for (int c0 = 0; c0 < tl.rows; c0 += 32) {
                 uint32_t v[32];
@@ -722,7 +712,7 @@ __device__ __forceinline__ uint2 ws_word(uint32_t q, float mul, bool f16)
 //       largest block exponent; exact while every block lies within 2^15 of M_p. A row
 //       with a wider spread sets *route_flag and is not written: the bf16 pass then
 //       rewrites every row (the GEMM takes one operand type per call).
-//   bf16 route (MXFP4, and the f16 route's fallback): bf16(code * 2^m_b), always exact.
+//   bf16 route (the f16 route's fallback): bf16(code * 2^m_b), always exact.
 // A CTA of 8 warps takes 8 / wr rows at a time; the wr warps of a row split its 128-groups
 // (warp i of the row takes groups i, i + wr, ...). With REG (at most kQuantRegGroups
 // groups per warp) the row stays in registers between the scale reduction and the
@@ -954,13 +944,15 @@ static WsLayout ws_layout(const void *workspace, int64_t T, int64_t P, int64_t k
     return l;
 }
 
-// Quantise pass of the tensor-core path: every routed row into the workspace. NVFP4 first
-// tries f16 with a per-row power-of-two scale (the cheaper weight conversion in the GEMM);
-// if any row's block scales span more than f16 holds exactly, the bf16 pass rewrites all
-// rows. MXFP4 weights times 2^(e-127) need bf16's range, so MXFP4 always takes bf16.
+// Quantise pass of the NVFP4 tensor-core path: every routed row into the workspace. It
+// first tries f16 with a per-row power-of-two scale (the cheaper weight conversion in the
+// GEMM); if any row's block scales span more than f16 holds exactly, the bf16 pass rewrites
+// all rows. (MXFP4 has its own pass and kernel: the block-scaled 8-bit MMA.)
 cudaError_t launch_tc_quantize(const GroupedProblem &p, void *workspace, cudaStream_t s)
 {
     using namespace tc;
+    if (p.recipe != FP4_NVFP4)
+        return cudaErrorInvalidValue;
     const bool tok = per_token(p);
     const WsLayout l = ws_layout(workspace, p.T, p.P, p.k);
     const int64_t S = tok ? p.T : p.P;                 // rows the quantise pass writes
@@ -968,7 +960,6 @@ cudaError_t launch_tc_quantize(const GroupedProblem &p, void *workspace, cudaStr
     uint2 *qact = reinterpret_cast<uint2 *>(tok ? l.tok_act : l.act);
     float *qscale = tok ? l.tok_scale : l.rowscale;
     const int sms = device_sms();
-    const bool nvfp4 = p.recipe == FP4_NVFP4;
     const int kq = p.k / 128;
     // warps per row: enough that each holds at most kQuantRegGroups groups, a power of two <= 8
     int wr = 1;
@@ -979,23 +970,17 @@ cudaError_t launch_tc_quantize(const GroupedProblem &p, void *workspace, cudaStr
     const int64_t want = (S + rpc - 1) / rpc;
     const int blocks = (int)(want < (int64_t)sms * 3 ? want : (int64_t)sms * 3);  // 3 CTAs per SM
     auto kern = reg ? quant_ws_kernel<true> : quant_ws_kernel<false>;
-    if (nvfp4) {
-        cudaError_t e = cudaMemsetAsync(l.route_flag, 0, sizeof(unsigned), s);
-        if (e != cudaSuccess)
-            return e;
-    }
+    cudaError_t e = cudaMemsetAsync(l.route_flag, 0, sizeof(unsigned), s);
+    if (e != cudaSuccess)
+        return e;
     if (S > 0) {
-        if (nvfp4) {
-            kern<<<blocks, 256, 0, s>>>(p.x, p.T, rid, S, p.k, wr, 1, qact, qscale, l.route_flag,
-                                        nullptr, p.err);
-            // the bf16 fallback: exits at once unless a row was too wide for f16
-            const int fb = 2 * sms < blocks ? 2 * sms : blocks;
-            kern<<<fb, 256, 0, s>>>(p.x, p.T, rid, S, p.k, wr, 0, qact, qscale, nullptr,
-                                    l.route_flag, p.err);
-        } else {
-            kern<<<blocks, 256, 0, s>>>(p.x, p.T, rid, S, p.k, wr, 0, qact, qscale, nullptr,
-                                        nullptr, p.err);
-        }
+        kern<<<blocks, 256, 0, s>>>(p.x, p.T, rid, S, p.k, wr, 1, qact, qscale, l.route_flag,
+                                    nullptr, p.err);
+        // the bf16 fallback: exits at once unless a row was too wide for f16 (the host cannot
+        // know without a synchronisation, so it is always enqueued)
+        const int fb = 2 * sms < blocks ? 2 * sms : blocks;
+        kern<<<fb, 256, 0, s>>>(p.x, p.T, rid, S, p.k, wr, 0, qact, qscale, nullptr,
+                                l.route_flag, p.err);
     }
     if (tok) {
         const int64_t ew = (p.P + 7) / 8;
@@ -1007,17 +992,15 @@ cudaError_t launch_tc_quantize(const GroupedProblem &p, void *workspace, cudaStr
     return cudaGetLastError();
 }
 
-// The persistent tensor-core GEMM over a workspace that launch_tc_quantize filled for the
-// same tokens, row ids (present or not), routed rows, k and recipe.
+// The persistent NVFP4 tensor-core GEMM over a workspace that launch_tc_quantize filled
+// for the same tokens, row ids (present or not), routed rows and k.
 cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaStream_t s)
 {
     using namespace tc;
-    if (!tc_supported(p.n, p.k, p.recipe, p.E))
+    if (p.recipe != FP4_NVFP4 || !tc_supported(p.n, p.k, p.recipe, p.E))
         return cudaErrorInvalidValue;
     const WsLayout l = ws_layout(workspace, p.T, p.P, p.k);
     const int sms = device_sms();
-    const bool nvfp4 = p.recipe == FP4_NVFP4;
-    const int gs = nvfp4 ? 16 : 32;
     alignas(64) BMaps tmB;
     alignas(64) CUtensorMap tmW, tmS;
     for (int i = 0; i < 4; ++i)
@@ -1026,7 +1009,7 @@ cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaS
             return cudaErrorInvalidValue;
     if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w, (uint64_t)p.k / 2,
                   (uint64_t)p.E * p.n, W_KS * BK / 2, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sc, (uint64_t)p.k / gs,
+        !make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sc, (uint64_t)p.k / 16,
                   (uint64_t)p.E * p.n, 16, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     Params kp;
@@ -1035,14 +1018,15 @@ cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaS
     kp.P = p.P;
     kp.n = p.n;
     kp.k = p.k;
-    kp.recipe = p.recipe;
     kp.mt = (p.n + BM - 1) / BM;
     kp.scale2 = p.scale2;
     kp.scale2_host = p.scale2_host;
-    kp.route_flag = nvfp4 ? l.route_flag : nullptr;
+    kp.route_flag = l.route_flag;
     kp.rowscale = l.rowscale;
     kp.out = p.out;
     kp.err = p.err;
+    kp.stall = 0;
+    kp.wait_limit = take_stall_request(&kp.stall);
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);

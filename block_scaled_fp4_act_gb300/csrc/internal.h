@@ -34,6 +34,11 @@ struct GroupedProblem {
 // Address of the current device's error word (looked up once per device).
 unsigned *device_error_word();
 
+// The bounded-wait limit (clock64 cycles) for the next tensor-core GEMM launch on this host
+// thread. Sets *stall to 1 and clears the request if fp4_test_stall_next_gemm asked for a
+// stalled launch; otherwise returns the normal limit and leaves *stall alone.
+long long take_stall_request(int *stall);
+
 // Kernel launchers; each returns cudaSuccess or the launch error.
 cudaError_t launch_act_quant(const float *x, uint8_t *codes, float *scales, int64_t rows,
                              int64_t k, cudaStream_t s);

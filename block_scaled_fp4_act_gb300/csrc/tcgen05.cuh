@@ -14,11 +14,12 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
 
 // Whole-warp forms: lane 0 waits, the warp takes its answer (keeps the warp converged).
 __device__ __forceinline__ bool warp_mbar_wait(uint32_t bar, uint32_t parity,
-                                               volatile int *abort_flag, unsigned *err)
+                                               volatile int *abort_flag, unsigned *err,
+                                               long long limit = kTimeoutCycles)
 {
     bool ok = true;
     if ((threadIdx.x & 31) == 0)
-        ok = mbar_wait(bar, parity, abort_flag, err);
+        ok = mbar_wait(bar, parity, abort_flag, err, limit);
     return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
 }
 

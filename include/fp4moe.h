@@ -303,6 +303,19 @@ double fp4_error_ops(int path, int recipe, int64_t k);
 void fp4_force_path(int path);
 
 /*
+ * Test hook for the bounded-wait abort path (off unless called; the pages have no
+ * counterpart: their calls report failure only through the status they return). The next
+ * tensor-core GEMM launch made from the calling host thread (either recipe; it is the GEMM
+ * phase of fp4_grouped_expert_gemm, fp4_grouped_gemm_quantized or the allocation-free
+ * call) runs with one pipeline arrival withheld in its first CTA and with its waits bounded
+ * by wait_limit_cycles clock64 cycles (clamped to [1e6, the normal limit of about 2e9]).
+ * That launch gives up the stalled wait, sets FP4_DEVERR_TIMEOUT, drains its own copies
+ * and MMAs, frees its tensor memory and returns; its outputs are unspecified. The request
+ * is used once; wait_limit_cycles <= 0 withdraws it. Nothing faults or hangs.
+ */
+void fp4_test_stall_next_gemm(int64_t wait_limit_cycles);
+
+/*
  * Synchronises `stream`, then returns FP4_OK or FP4_ERR_DEVICE and stores the device
  * error word (FP4_DEVERR_* bits) of the current device in *bits (nullable), clearing it.
  */
