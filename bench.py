@@ -180,12 +180,12 @@ KERNEL_SOURCES = {
     "mx_grouped_gemm": ["gemm_mx.cu", "common.cuh", "tcgen05.cuh", "internal.h", "tma_host.h"],
     "tc_quantize": ["gemm_tc.cu", "common.cuh", "internal.h"],
     "stream_gemm": ["gemm_stream.cu", "common.cuh", "internal.h"],
-    "decode_mma": ["gemm_decode.cu", "common.cuh", "internal.h"],
+    "decode_tma": ["gemm_decode.cu", "common.cuh", "internal.h", "tma_host.h"],
 }
 
-# The no-workspace path runs the warp-MMA decode kernel for every k up to 28544, which
-# covers each workload here; the FMA streaming kernel takes larger k only.
-STREAM_KERNEL = "decode_mma"
+# The no-workspace path runs the TMA-fed warp-MMA decode kernel for k a multiple of 512 up
+# to 28544, which covers each workload here; the FMA streaming kernel takes larger k only.
+STREAM_KERNEL = "decode_tma"
 
 
 def source_hash(kernel=None):

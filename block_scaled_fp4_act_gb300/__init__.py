@@ -66,6 +66,9 @@ def lib():
         L.fp4_grouped_expert_gemm_noalloc.argtypes = [P, i64, P, P, i32, i64, P, P, P, i32, P,
                                                        i64, i64, P]
         L.fp4_grouped_expert_gemm_noalloc.restype = i32
+        L.fp4_grouped_gate_up_swiglu.argtypes = [P, i64, P, P, i32, i64, P, P, P, i32, f32, P,
+                                                 i64, i64, P, sz, P]
+        L.fp4_grouped_gate_up_swiglu.restype = i32
         L.fp4_grouped_quantize.argtypes = [P, i64, P, i64, i64, i32, P, sz, P]
         L.fp4_grouped_quantize.restype = i32
         L.fp4_grouped_gemm_quantized.argtypes = [P, sz, i64, P, P, i32, i64, P, P, P, i32, P,
@@ -210,6 +213,38 @@ def fp4_grouped_expert_gemm(x, row_ids, offsets, w, wscale, scale2, recipe, out=
                                          _ptr(workspace), ws_bytes, _stream(stream)),
            "fp4_grouped_expert_gemm")
     return out
+
+
+def fp4_grouped_gate_up_swiglu(x, row_ids, offsets, w, wscale, scale2, recipe, limit,
+                               workspace, h=None, stream=None):
+    """The gate/up projection with SwiGLU in its epilogue (tensor-core path).
+
+    w [E, 2*inter, k/2] u8 (gate rows, then up rows, per expert) -> h [P, inter] f32."""
+    import torch
+    T, k = x.shape
+    E, n = w.shape[0], w.shape[1]
+    inter = n // 2
+    _need(x, torch.float32, None, "x")
+    _need(offsets, torch.int32, (E + 1,), "offsets")
+    if row_ids is not None:
+        _need(row_ids, torch.int32, None, "row_ids")
+        P = row_ids.numel()
+    else:
+        P = T
+    _need(w, torch.uint8, (E, n, k // 2), "w")
+    _need(wscale, torch.uint8, (E, n, k // group_size(recipe)), "wscale")
+    if scale2 is not None:
+        _need(scale2, torch.float32, (E,), "scale2")
+    if h is None:
+        h = torch.empty((P, inter), dtype=torch.float32, device=x.device)
+    _need(h, torch.float32, (P, inter), "h")
+    _need(workspace, torch.uint8, None, "workspace")
+    _check(lib().fp4_grouped_gate_up_swiglu(_ptr(x), T, _ptr(row_ids), _ptr(offsets), E, P,
+                                            _ptr(w), _ptr(wscale), _ptr(scale2), int(recipe),
+                                            float(limit), _ptr(h), inter, k, _ptr(workspace),
+                                            workspace.numel(), _stream(stream)),
+           "fp4_grouped_gate_up_swiglu")
+    return h
 
 
 def fp4_grouped_quantize(x, row_ids, total_rows, recipe, workspace, stream=None):

@@ -165,6 +165,17 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
+// SwiGLU of one element with the swiglu_limit clamps (memra-engine 0.98.0,
+// src/bin/dsv4_native_gemm_gate.rs, swiglu_limit saturation cell): up clamped on both
+// sides, gate from above, both before the sigmoid, in f32 in the page's order. Shared by
+// the standalone SwiGLU kernel and the fused gate/up epilogues, so both give the same bits.
+__device__ __forceinline__ float swiglu_one(float gate, float up, float limit)
+{
+    const float u = fminf(fmaxf(up, -limit), limit);
+    const float g = fminf(gate, limit);
+    return g * (1.0f / (1.0f + expf(-g))) * u;
+}
+
 // ---------------------------------------------------------------- mbarriers
 
 // Every pipeline wait is bounded by about a second of clock64 cycles.
@@ -247,6 +258,35 @@ __device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity)
 __device__ __forceinline__ void fence_proxy_async()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Prefetch [addr, addr + bytes) into L2 (addr 16-byte aligned, bytes a multiple of 16), in
+// pieces of at most 16 KB.
+__device__ __forceinline__ void prefetch_l2(const void *addr, uint32_t bytes)
+{
+    const char *a = static_cast<const char *>(addr);
+    for (uint32_t off = 0; off < bytes; off += 16384u) {
+        const uint32_t n = bytes - off < 16384u ? bytes - off : 16384u;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a + off), "r"(n) : "memory");
+    }
+}
+
+// An L2 cache policy that evicts the lines it fetches first (for data read once).
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 2-D TMA tile load as tma_load_2d, with an L2 cache policy.
+__device__ __forceinline__ void tma_load_2d_evict_first(uint32_t dst, const CUtensorMap *map, int x,
+                                                        int y, uint32_t bar, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+                 : "memory");
 }
 
 // 2-D TMA tile load into shared memory, completing on an mbarrier (x: innermost).

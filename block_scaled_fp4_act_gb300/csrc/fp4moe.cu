@@ -26,14 +26,6 @@ unsigned *device_error_word()
 }
 
 int stream_max_rows_per_pass(int k);
-size_t tc_workspace_bytes(int64_t num_tokens, int64_t total_rows, int64_t k, int recipe);
-bool tc_supported(int64_t n, int64_t k, int recipe, int E);
-cudaError_t launch_tc_quantize(const GroupedProblem &p, void *workspace, cudaStream_t s);
-cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaStream_t s);
-size_t mx_workspace_bytes(int64_t num_tokens, int64_t total_rows, int64_t k);
-bool mx_supported(int64_t n, int64_t k, int E, const void *w);
-cudaError_t launch_mx_quantize(const GroupedProblem &p, void *workspace, cudaStream_t s);
-cudaError_t launch_mx_gemm(const GroupedProblem &p, const void *workspace, cudaStream_t s);
 
 // The tensor-core path by recipe: NVFP4 on the 16-bit MMA with converted weights, MXFP4 on
 // the block-scaled 8-bit MMA (weights as stored, e4m3 activation codes).
@@ -47,9 +39,10 @@ static cudaError_t tc_path_quantize(const GroupedProblem &p, void *ws, cudaStrea
     return p.recipe == FP4_MXFP4 ? launch_mx_quantize(p, ws, s) : launch_tc_quantize(p, ws, s);
 }
 
-static cudaError_t tc_path_gemm(const GroupedProblem &p, const void *ws, cudaStream_t s)
+static cudaError_t tc_path_gemm(const GroupedProblem &p, const void *ws, cudaStream_t s,
+                                const SwigluOut *sw = nullptr)
 {
-    return p.recipe == FP4_MXFP4 ? launch_mx_gemm(p, ws, s) : launch_tc_gemm(p, ws, s);
+    return p.recipe == FP4_MXFP4 ? launch_mx_gemm(p, ws, s, sw) : launch_tc_gemm(p, ws, s, sw);
 }
 
 // Shapes (and, for MXFP4, the weight alignment the packed 4-bit TMA form needs) the
@@ -415,6 +408,56 @@ int fp4_grouped_gemm_quantized(const void *workspace, size_t workspace_bytes,
     if (!p.err)
         return record(cudaErrorInvalidDevice);
     return record(tc_path_gemm(p, workspace, (cudaStream_t)stream));
+}
+
+int fp4_grouped_gate_up_swiglu(const float *x, int64_t num_tokens, const int32_t *row_ids,
+                               const int32_t *offsets, int num_experts, int64_t total_rows,
+                               const uint8_t *w, const uint8_t *wscale, const float *scale2,
+                               int recipe, float swiglu_limit, float *h, int64_t inter,
+                               int64_t k, void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!recipe_ok(recipe) || num_experts < 1 || num_experts > 65535 || num_tokens < 0 ||
+        !(swiglu_limit > 0.0f) || !(swiglu_limit <= 3.0e38f))
+        return FP4_ERR_ARG;
+    if (inter < 64 || inter % 64 != 0)
+        return FP4_ERR_SHAPE;
+    const int64_t n = 2 * inter;
+    int st = check_tc_call(recipe, num_tokens, row_ids, total_rows, n, k, workspace,
+                           workspace_bytes);
+    if (st != FP4_OK)
+        return st;
+    if (!tc_supported(n, k, recipe, num_experts))
+        return FP4_ERR_SHAPE;
+    if (total_rows == 0)
+        return FP4_OK;
+    if (!x || !offsets || !w || !wscale || !h || (recipe == FP4_NVFP4 && !scale2))
+        return FP4_ERR_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(wscale) || !aligned16(h) ||
+        !tc_path_supported(n, k, recipe, num_experts, w))
+        return FP4_ERR_ALIGN;
+    GroupedProblem p{};
+    p.x = x;
+    p.T = num_tokens;
+    p.row_ids = row_ids;
+    p.offsets = offsets;
+    p.E = num_experts;
+    p.P = total_rows;
+    p.w = w;
+    p.sc = wscale;
+    p.scale2 = recipe == FP4_NVFP4 ? scale2 : nullptr;
+    p.scale2_host = 1.0f;
+    p.recipe = recipe;
+    p.out = nullptr;
+    p.n = (int)n;
+    p.k = (int)k;
+    p.err = device_error_word();
+    if (!p.err)
+        return record(cudaErrorInvalidDevice);
+    st = record(tc_path_quantize(p, workspace, (cudaStream_t)stream));
+    if (st != FP4_OK)
+        return st;
+    const SwigluOut sw{h, inter, swiglu_limit};
+    return record(tc_path_gemm(p, workspace, (cudaStream_t)stream, &sw));
 }
 
 int fp4_route_topk(const float *logits, int64_t num_tokens, int num_experts, int topk,

@@ -94,6 +94,10 @@ struct Params {
     // aborts
     long long wait_limit;
     int stall;
+    // fused SwiGLU (gate/up bank: rows [0, inter) gate, [inter, 2 inter) up): out is h
+    // [P, inter]; a tile covers 64 h columns (16 gate + 16 up rows per lane quarter)
+    int inter;
+    float limit;
 };
 
 __device__ __forceinline__ int64_t offset_at(const Params &p, int e)
@@ -178,6 +182,10 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8])
                  : "memory");
 }
 
+// SWIGLU: the weight maps have 16-row boxes, eight per stage (block b: gate rows when b is
+// even, up rows when odd), so lane quarter q holds 16 gate rows in lanes 0-15 and the
+// matching up rows in lanes 16-31 (as in the 16-bit kernel).
+template <bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CodeMaps tmB, const __grid_constant__ CUtensorMap tmSB,
                    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmS,
@@ -354,9 +362,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     uint8_t *dst = ringW + slot * W_BYTES;
                     mbar_arrive_expect_tx(wfull(slot), A_TX + SC_BYTES);
-                    tma_load_2d(smem_u32(dst), &tmA, kb * BK, yw, wfull(slot));
-                    tma_load_2d(smem_u32(dst + A_BYTES), &tmS, ((kb * BK) / 32) & ~15, yw,
-                                wfull(slot));
+                    if (SWIGLU) {
+#pragma unroll
+                        for (int b = 0; b < 8; ++b) {
+                            const int yb = tl.e * p.n + (b & 1) * p.inter + tl.m * 64 + (b >> 1) * 16;
+                            tma_load_2d(smem_u32(dst + b * 16 * 128), &tmA, kb * BK, yb, wfull(slot));
+                            tma_load_2d(smem_u32(dst + A_BYTES + b * 16 * 16), &tmS,
+                                        ((kb * BK) / 32) & ~15, yb, wfull(slot));
+                        }
+                    } else {
+                        tma_load_2d(smem_u32(dst), &tmA, kb * BK, yw, wfull(slot));
+                        tma_load_2d(smem_u32(dst + A_BYTES), &tmS, ((kb * BK) / 32) & ~15, yw,
+                                    wfull(slot));
+                    }
                     mask |= 1u << slot;
                     par = (par & ~(1u << slot)) | (phase << slot);
                     if (++slot == W_STAGES) {
@@ -545,16 +563,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(accf(buf), (it >> 1) & 1, abort_flag, p.err, p.wait_limit))
                 break;
             tc_fence_after();
-            const int col = tl.m * BM + q * 32 + lane;
-            const bool colok = col < p.n;
-            float *orow = p.out + tl.row0 * (int64_t)p.n + col;
+            // SWIGLU: lanes 0-15 own h column col, lanes 16-31 hold the matching up rows
+            const int col = SWIGLU ? tl.m * 64 + q * 16 + (lane & 15) : tl.m * BM + q * 32 + lane;
+            const int ldo = SWIGLU ? p.inter : p.n;
+            const bool colok = SWIGLU ? (lane < 16 && col < p.inter) : col < p.n;
+            float *orow = p.out + tl.row0 * (int64_t)ldo + col;
             for (int c0 = 0; c0 < tl.rows; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c0), v);
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj)
-                    if (colok && c0 + jj < tl.rows)
-                        orow[(int64_t)(c0 + jj) * p.n] = __uint_as_float(v[jj]);
+                for (int jj = 0; jj < 32; ++jj) {
+                    const float val = __uint_as_float(v[jj]);
+                    if (SWIGLU) {
+                        const float up = __shfl_xor_sync(0xFFFFFFFFu, val, 16);
+                        if (colok && c0 + jj < tl.rows)
+                            orow[(int64_t)(c0 + jj) * ldo] = swiglu_one(val, up, p.limit);
+                    } else if (colok && c0 + jj < tl.rows) {
+                        orow[(int64_t)(c0 + jj) * ldo] = val;
+                    }
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -721,11 +748,15 @@ cudaError_t launch_mx_quantize(const GroupedProblem &p, void *workspace, cudaStr
     return cudaGetLastError();
 }
 
-cudaError_t launch_mx_gemm(const GroupedProblem &p, const void *workspace, cudaStream_t s)
+cudaError_t launch_mx_gemm(const GroupedProblem &p, const void *workspace, cudaStream_t s,
+                           const SwigluOut *sw)
 {
     using namespace mx;
     if (!mx_supported(p.n, p.k, p.E, p.w))
         return cudaErrorInvalidValue;
+    if (sw && (sw->inter % 64 != 0 || 2 * sw->inter != p.n))
+        return cudaErrorInvalidValue;
+    const uint32_t wbox = sw ? 16 : BM;  // rows per weight box
     const MxLayout l = mx_layout(workspace, p.T, p.P, p.k);
     auto fn = encode_fn();
     if (!fn)
@@ -758,7 +789,7 @@ cudaError_t launch_mx_gemm(const GroupedProblem &p, const void *workspace, cudaS
         // 2-D {k E2M1 values, E n rows}, box {128 values, 128 rows}, padded 4-bit form
         cuuint64_t dims[2] = {(cuuint64_t)p.k, (cuuint64_t)p.E * p.n};
         cuuint64_t strides[1] = {(cuuint64_t)p.k / 2};
-        cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
+        cuuint32_t box[2] = {(cuuint32_t)BK, wbox};
         cuuint32_t es[2] = {1, 1};
         if (fn(&tmA, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<uint8_t *>(p.w), dims,
                strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -766,7 +797,7 @@ cudaError_t launch_mx_gemm(const GroupedProblem &p, const void *workspace, cudaS
             return cudaErrorInvalidValue;
     }
     if (!make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sc, (uint64_t)p.k / 32,
-                  (uint64_t)p.E * p.n, 16, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+                  (uint64_t)p.E * p.n, 16, wbox, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     Params kp;
     kp.offsets = p.offsets;
@@ -774,26 +805,29 @@ cudaError_t launch_mx_gemm(const GroupedProblem &p, const void *workspace, cudaS
     kp.P = p.P;
     kp.n = p.n;
     kp.k = p.k;
-    kp.mt = (p.n + BM - 1) / BM;
-    kp.out = p.out;
+    kp.mt = sw ? (int)(sw->inter / 64) : (p.n + BM - 1) / BM;
+    kp.out = sw ? sw->h : p.out;
     kp.err = p.err;
     kp.stall = 0;
     kp.wait_limit = take_stall_request(&kp.stall);
-    static bool attr_set[64] = {};
+    kp.inter = sw ? (int)sw->inter : 0;
+    kp.limit = sw ? sw->limit : 0.0f;
+    auto kern = sw ? mx_gemm_kernel<true> : mx_gemm_kernel<false>;
+    static bool attr_set[2][64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    if (dev < 0 || dev >= 64 || !attr_set[sw ? 1 : 0][dev]) {
         cudaError_t e =
-            cudaFuncSetAttribute(mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess)
             return e;
         if (dev >= 0 && dev < 64)
-            attr_set[dev] = true;
+            attr_set[sw ? 1 : 0][dev] = true;
     }
     const int sms = mx_sms();
     const int64_t max_tiles = ((p.P + BN - 1) / BN + p.E) * (int64_t)kp.mt;
     const int grid = (int)(max_tiles < sms ? max_tiles : sms);
-    mx_gemm_kernel<<<grid, kThreads, SMEM_BYTES, s>>>(tmB, tmSB, tmA, tmS, kp);
+    kern<<<grid, kThreads, SMEM_BYTES, s>>>(tmB, tmSB, tmA, tmS, kp);
     return cudaGetLastError();
 }
 

@@ -151,6 +151,10 @@ struct Params {
     // converter warp of CTA 0 withhold its first arrival, so this launch times out and aborts
     long long wait_limit;
     int stall;
+    // fused SwiGLU (gate/up bank: rows [0, inter) gate, [inter, 2 inter) up): out is h
+    // [P, inter]; a tile covers 64 h columns (16 gate + 16 up rows per lane quarter)
+    int inter;
+    float limit;
 };
 
 // CSR offset e, or the single-expert offsets {0, P} when the call has none.
@@ -285,6 +289,11 @@ __device__ __forceinline__ int bmap_index(int rows)
 __host__ __device__ constexpr int bmap_rows(int bi) { return bi < 3 ? 32 << bi : BN; }
 __host__ __device__ constexpr int bmap_kblocks(int bi) { return 8 >> bi; }
 
+// SWIGLU: the weight maps have 16-row boxes; each weight slot is filled by eight of them
+// (block b: gate rows when b is even, up rows when odd, 16 h columns from 64 m + 16 (b / 2)),
+// so lane quarter q holds 16 gate rows in its lanes 0-15 and the matching up rows in lanes
+// 16-31, and the epilogue pairs them with one shuffle.
+template <bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ BMaps tmB, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmS, const Params p)
@@ -419,8 +428,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint8_t *dst = ringW + slot * W_BYTES;
                         const int k0 = j * W_KS * BK;  // first k of the slot
                         mbar_arrive_expect_tx(ful, W_BYTES);
-                        tma_load_2d(smem_u32(dst), &tmW, k0 / 2, yw, ful);
-                        tma_load_2d(smem_u32(dst + NIB_BYTES), &tmS, k0 / 16, yw, ful);
+                        if (SWIGLU) {
+#pragma unroll
+                            for (int b = 0; b < 8; ++b) {
+                                const int yb = tl.e * p.n + (b & 1) * p.inter + tl.m * 64 + (b >> 1) * 16;
+                                tma_load_2d(smem_u32(dst + b * 16 * 128), &tmW, k0 / 2, yb, ful);
+                                tma_load_2d(smem_u32(dst + NIB_BYTES + b * 16 * 16), &tmS, k0 / 16, yb,
+                                            ful);
+                            }
+                        } else {
+                            tma_load_2d(smem_u32(dst), &tmW, k0 / 2, yw, ful);
+                            tma_load_2d(smem_u32(dst + NIB_BYTES), &tmS, k0 / 16, yw, ful);
+                        }
                     }
                     issued_mask |= 1u << slot;
                     issued_parity = (issued_parity & ~(1u << slot)) | (phase << slot);
@@ -633,10 +652,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(accf(buf), (it >> 1) & 1, abort_flag, p.err, p.wait_limit))
                 break;
             tc_fence_after();
-            const int col = tl.m * BM + q * 32 + lane;
-            const bool colok = col < p.n;
+            // SWIGLU: lanes 0-15 own h column col, lanes 16-31 hold the matching up rows
+            const int col = SWIGLU ? tl.m * 64 + q * 16 + (lane & 15) : tl.m * BM + q * 32 + lane;
+            const int ldo = SWIGLU ? p.inter : p.n;
+            const bool colok = SWIGLU ? (lane < 16 && col < p.inter) : col < p.n;
             const float s2 = p.scale2 ? __ldg(p.scale2 + tl.e) : p.scale2_host;
-            float *orow = p.out + tl.row0 * (int64_t)p.n + col;
+            float *orow = p.out + tl.row0 * (int64_t)ldo + col;
             for (int c0 = 0; c0 < tl.rows; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c0), v);
@@ -648,8 +669,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int jj = 0; jj < 32; ++jj) {
                     // f16_route is uniform over the CTA, so every lane takes the shuffle
                     const float r = f16_route ? __shfl_sync(0xFFFFFFFFu, rs, jj) : 1.0f;
-                    if (colok && c0 + jj < tl.rows)
-                        orow[(int64_t)(c0 + jj) * p.n] = (__uint_as_float(v[jj]) * r) * s2;
+                    const float val = (__uint_as_float(v[jj]) * r) * s2;
+                    if (SWIGLU) {
+                        const float up = __shfl_xor_sync(0xFFFFFFFFu, val, 16);
+                        if (colok && c0 + jj < tl.rows)
+                            orow[(int64_t)(c0 + jj) * ldo] = swiglu_one(val, up, p.limit);
+                    } else if (colok && c0 + jj < tl.rows) {
+                        orow[(int64_t)(c0 + jj) * ldo] = val;
+                    }
                 }
             }
             tc_fence_before();
@@ -993,14 +1020,19 @@ cudaError_t launch_tc_quantize(const GroupedProblem &p, void *workspace, cudaStr
 }
 
 // The persistent NVFP4 tensor-core GEMM over a workspace that launch_tc_quantize filled
-// for the same tokens, row ids (present or not), routed rows and k.
-cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaStream_t s)
+// for the same tokens, row ids (present or not), routed rows and k. With sw, the bank is a
+// gate/up bank of n = 2 inter rows and the epilogue writes h = SwiGLU(gate, up) [P, inter].
+cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaStream_t s,
+                           const SwigluOut *sw)
 {
     using namespace tc;
     if (p.recipe != FP4_NVFP4 || !tc_supported(p.n, p.k, p.recipe, p.E))
         return cudaErrorInvalidValue;
+    if (sw && (sw->inter % 64 != 0 || 2 * sw->inter != p.n))
+        return cudaErrorInvalidValue;
     const WsLayout l = ws_layout(workspace, p.T, p.P, p.k);
     const int sms = device_sms();
+    const uint32_t wbox = sw ? 16 : BM;  // rows per weight box
     alignas(64) BMaps tmB;
     alignas(64) CUtensorMap tmW, tmS;
     for (int i = 0; i < 4; ++i)
@@ -1008,9 +1040,9 @@ cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaS
                               (uint32_t)bmap_rows(i), (uint32_t)bmap_kblocks(i)))
             return cudaErrorInvalidValue;
     if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w, (uint64_t)p.k / 2,
-                  (uint64_t)p.E * p.n, W_KS * BK / 2, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                  (uint64_t)p.E * p.n, W_KS * BK / 2, wbox, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sc, (uint64_t)p.k / 16,
-                  (uint64_t)p.E * p.n, 16, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+                  (uint64_t)p.E * p.n, 16, wbox, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     Params kp;
     kp.offsets = p.offsets;
@@ -1018,29 +1050,32 @@ cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaS
     kp.P = p.P;
     kp.n = p.n;
     kp.k = p.k;
-    kp.mt = (p.n + BM - 1) / BM;
+    kp.mt = sw ? (int)(sw->inter / 64) : (p.n + BM - 1) / BM;
     kp.scale2 = p.scale2;
     kp.scale2_host = p.scale2_host;
     kp.route_flag = l.route_flag;
     kp.rowscale = l.rowscale;
-    kp.out = p.out;
+    kp.out = sw ? sw->h : p.out;
     kp.err = p.err;
     kp.stall = 0;
     kp.wait_limit = take_stall_request(&kp.stall);
-    static bool attr_set[64] = {};
+    kp.inter = sw ? (int)sw->inter : 0;
+    kp.limit = sw ? sw->limit : 0.0f;
+    auto kern = sw ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
+    static bool attr_set[2][64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (dev < 0 || dev >= 64 || !attr_set[sw ? 1 : 0][dev]) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess)
             return e;
         if (dev >= 0 && dev < 64)
-            attr_set[dev] = true;
+            attr_set[sw ? 1 : 0][dev] = true;
     }
     const int64_t max_tiles = ((p.P + BN - 1) / BN + p.E) * (int64_t)kp.mt;
     const int grid = (int)(max_tiles < sms ? max_tiles : sms);
-    tc_gemm_kernel<<<grid, kThreads, SMEM_BYTES, s>>>(tmB, tmW, tmS, kp);
+    kern<<<grid, kThreads, SMEM_BYTES, s>>>(tmB, tmW, tmS, kp);
     return cudaGetLastError();
 }
 
@@ -1096,10 +1131,6 @@ static uint8_t *noalloc_scratch(cudaError_t *status)
 }
 
 void set_last_error(const char *msg);
-size_t mx_workspace_bytes(int64_t num_tokens, int64_t total_rows, int64_t k);
-bool mx_supported(int64_t n, int64_t k, int E, const void *w);
-cudaError_t launch_mx_quantize(const GroupedProblem &p, void *workspace, cudaStream_t s);
-cudaError_t launch_mx_gemm(const GroupedProblem &p, const void *workspace, cudaStream_t s);
 
 } // namespace fp4moe
 

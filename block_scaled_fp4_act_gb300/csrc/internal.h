@@ -34,6 +34,28 @@ struct GroupedProblem {
 // Address of the current device's error word (looked up once per device).
 unsigned *device_error_word();
 
+// Fused SwiGLU output of a gate/up projection on the tensor-core path: the bank holds
+// 2 inter rows per expert (gate rows, then up rows) and the call writes
+// h = SwiGLU(gate, up) with the swiglu_limit clamps, [P, inter] f32, instead of [P, 2 inter].
+struct SwigluOut {
+    float *h;
+    int64_t inter;  // a multiple of 64
+    float limit;
+};
+
+// The tensor-core path (gemm_tc.cu: NVFP4 on the 16-bit MMA; gemm_mx.cu: MXFP4 on the
+// block-scaled 8-bit MMA): workspace size, shape support, the quantise phase and the GEMM.
+size_t tc_workspace_bytes(int64_t num_tokens, int64_t total_rows, int64_t k, int recipe);
+bool tc_supported(int64_t n, int64_t k, int recipe, int E);
+cudaError_t launch_tc_quantize(const GroupedProblem &p, void *workspace, cudaStream_t s);
+cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaStream_t s,
+                           const SwigluOut *sw = nullptr);
+size_t mx_workspace_bytes(int64_t num_tokens, int64_t total_rows, int64_t k);
+bool mx_supported(int64_t n, int64_t k, int E, const void *w);
+cudaError_t launch_mx_quantize(const GroupedProblem &p, void *workspace, cudaStream_t s);
+cudaError_t launch_mx_gemm(const GroupedProblem &p, const void *workspace, cudaStream_t s,
+                           const SwigluOut *sw = nullptr);
+
 // The bounded-wait limit (clock64 cycles) for the next tensor-core GEMM launch on this host
 // thread. Sets *stall to 1 and clears the request if fp4_test_stall_next_gemm asked for a
 // stalled launch; otherwise returns the normal limit and leaves *stall alone.

@@ -14,13 +14,6 @@
 
 namespace fp4moe {
 
-__device__ __forceinline__ float swiglu_one(float gate, float up, float limit)
-{
-    const float u = fminf(fmaxf(up, -limit), limit);
-    const float g = fminf(gate, limit);
-    return g * (1.0f / (1.0f + expf(-g))) * u;
-}
-
 // h of one lane's four elements, then the group's scale and codes (act_quant_kernel's steps).
 __device__ __forceinline__ void swiglu_group(const float4 gv, const float4 uv, float limit,
                                              int64_t gi, int64_t o, int lane,

@@ -230,6 +230,30 @@ int fp4_swiglu_quant(const float *gate, const float *up, int64_t ld, float limit
                      int64_t inter, float *h_out, uint8_t *codes, float *scales, void *stream);
 
 /*
+ * fp4_grouped_gate_up_swiglu -- the gate/up projection with SwiGLU in its epilogue: the
+ * grouped call of fp4_grouped_expert_gemm over a gate/up bank, writing
+ * h = SwiGLU(gate, up) with the swiglu_limit clamps (the arithmetic of fp4_swiglu_quant,
+ * dsv4_native_gemm_gate.rs swiglu_limit saturation cell) instead of the [P, 2*inter]
+ * gate/up output. The down projection then takes h as its input rows
+ * (fp4_grouped_expert_gemm with row_ids = NULL), whose own quantise pass is the page's
+ * requantisation of h. Tensor-core path only.
+ *   w, wscale  a gate/up bank [E, 2*inter, k/2], [E, 2*inter, k/gs]: rows [0, inter) of
+ *              an expert are its gate rows, rows [inter, 2*inter) its up rows (the page's
+ *              layout of w1 and w3 stacked)
+ *   h          [total_rows, inter] f32 out, in routed-row order; every element equals,
+ *              bit for bit, fp4_swiglu_quant's h of this call's gate/up output
+ *   inter      a multiple of 64; workspace: fp4_grouped_workspace_size(num_tokens,
+ *              total_rows, 2*inter, k, recipe) bytes
+ * Other arguments and checks as fp4_grouped_expert_gemm; shapes the tensor-core path does
+ * not take return FP4_ERR_SHAPE (use fp4_grouped_expert_gemm and fp4_swiglu_quant then).
+ */
+int fp4_grouped_gate_up_swiglu(const float *x, int64_t num_tokens, const int32_t *row_ids,
+                               const int32_t *offsets, int num_experts, int64_t total_rows,
+                               const uint8_t *w, const uint8_t *wscale, const float *scale2,
+                               int recipe, float swiglu_limit, float *h, int64_t inter,
+                               int64_t k, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * The routing front-end: the steps before and after the grouped projections.
  *
  * fp4_route_topk -- the router (memra-engine 0.125.0, src/bin/qwen4exp_gpu_gate.rs,

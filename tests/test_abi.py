@@ -106,6 +106,21 @@ def test_host_side_argument_checks(lib):
     assert R(a16, big, 4, None, a16, 2, 8, a16, a16, a16, 0, a16, 256, 512, None) == \
         fp4.FP4_ERR_SHAPE                                # no row ids, fewer tokens than rows
     assert R(a16, big, 8, None, a16, 2, 0, a16, a16, a16, 0, a16, 256, 512, None) == fp4.FP4_OK
+    # fp4_grouped_gate_up_swiglu(x, T, row_ids, offsets, E, P, w, wscale, scale2, recipe,
+    #                            limit, h, inter, k, ws, ws_bytes, stream)
+    G = lib.fp4_grouped_gate_up_swiglu
+    assert G(a16, 8, None, a16, 2, 8, a16, a16, a16, 0, 0.0, a16, 128, 512, a16, big, None) == \
+        fp4.FP4_ERR_ARG                                  # limit <= 0
+    assert G(a16, 8, None, a16, 2, 8, a16, a16, a16, 0, 7.0, a16, 100, 512, a16, big, None) == \
+        fp4.FP4_ERR_SHAPE                                # inter % 64
+    assert G(a16, 8, None, a16, 2, 8, a16, a16, a16, 0, 7.0, a16, 128, 512, None, 0, None) == \
+        fp4.FP4_ERR_WORKSPACE
+    assert G(None, 8, None, a16, 2, 8, a16, a16, a16, 0, 7.0, a16, 128, 512, a16, big, None) == \
+        fp4.FP4_ERR_ARG
+    assert G(a16, 8, None, a16, 2, 8, a16, a16, a16, 0, 7.0, odd, 128, 512, a16, big, None) == \
+        fp4.FP4_ERR_ALIGN
+    assert G(a16, 8, None, a16, 2, 0, a16, a16, a16, 0, 7.0, a16, 128, 512, a16, big, None) == \
+        fp4.FP4_OK                                       # no routed rows
     # fp4_route_topk(logits, T, E, topk, renorm, ids, weights, stream)
     K = lib.fp4_route_topk
     assert K(a16, 4, 0, 1, 0, a16, a16, None) == fp4.FP4_ERR_ARG

@@ -18,7 +18,7 @@ import torch
 import oracle
 import block_scaled_fp4_act_gb300 as fp4
 from block_scaled_fp4_act_gb300 import synth
-from parity_util import check_gemm, gemm_bound, to_np
+from parity_util import check_gemm, gemm_bound, grouped_sampled_check, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -95,3 +95,67 @@ def test_saturation_cell_chain(recipe, path):
     assert fp4.fp4_get_device_error() == 0
     print("chain recipe %d path %d: gate sat %d, up sat %d, w2 worst err/bound %.3g" % (
         recipe, path, int((g_np[0] > limit).sum()), int((np.abs(u_np[0]) > limit).sum()), worst))
+
+
+@pytest.mark.parametrize("recipe", [fp4.NVFP4, fp4.MXFP4])
+def test_saturation_cell_chain_fused_epilogue(recipe):
+    """The same cell over routed rows of several experts, with SwiGLU in the gate/up
+    epilogue (fp4_grouped_gate_up_swiglu): its h must equal, bit for bit, fp4_swiglu_quant's
+    h of the unfused gate/up output; the gate/up output, h and the down projection of h
+    (whose quantise pass is the requantisation) are checked against the oracle."""
+    fp4.build.build()
+    E, T, topk, hidden, inter, limit = 3, 96, 2, 2048, 1024, 7.0
+    gen = torch.Generator().manual_seed(57 + recipe)
+    x = torch.randn(T, hidden, generator=gen)
+    x[::7] *= 50.0                                              # saturation rows
+    choices = torch.stack([torch.randperm(E, generator=gen)[:topk] for _ in range(T)])
+    r = synth.routing_from_choices(choices, E)
+    gu_bank = synth.make_bank(recipe, E, 2 * inter, hidden, 61 + recipe, "cpu",
+                              scale2_value=5.9945243e-5 * 64)
+    dn_bank = synth.make_bank(recipe, E, hidden, inter, 67 + recipe, "cpu",
+                              scale2_value=5.9945243e-5 * 64)
+    routing = synth.Routing(r.offsets.to(DEV), r.row_ids.to(DEV))
+    gu = synth.Bank(recipe, gu_bank.w.to(DEV), gu_bank.sc.to(DEV), gu_bank.scale2.to(DEV))
+    dn = synth.Bank(recipe, dn_bank.w.to(DEV), dn_bank.sc.to(DEV), dn_bank.scale2.to(DEV))
+    xd = x.to(DEV)
+    P = r.P
+
+    # unfused: the gate/up projection on the tensor cores, then fp4_swiglu_quant
+    ws = fp4.workspace_for(T, P, 2 * inter, hidden, recipe)
+    fp4.fp4_force_path(fp4.PATH_TC)
+    try:
+        gu_out = fp4.fp4_grouped_expert_gemm(xd, routing.row_ids, routing.offsets, gu.w, gu.sc,
+                                             gu.scale2, recipe, workspace=ws)
+    finally:
+        fp4.fp4_force_path(fp4.PATH_AUTO)
+    _, _, h_unf = fp4.fp4_swiglu_quant(gu_out[:, :inter], gu_out[:, inter:], limit, want_h=True)
+
+    # fused
+    h = fp4.fp4_grouped_gate_up_swiglu(xd, routing.row_ids, routing.offsets, gu.w, gu.sc,
+                                       gu.scale2, recipe, limit, ws)
+    assert torch.equal(h, h_unf), float((h - h_unf).abs().max())
+
+    # the gate/up leg against the oracle, the clamps engaged, h against the oracle's SwiGLU
+    proj_gu = synth.Projection("gu", xd, routing, gu)
+    grouped_sampled_check(proj_gu, gu_out, fp4.PATH_TC, np.arange(P), "fused chain gate/up")
+    g_np, u_np = to_np(gu_out[:, :inter]), to_np(gu_out[:, inter:])
+    assert (g_np > limit).sum() > 0 and (np.abs(u_np) > limit).sum() > 0
+    assert (g_np < -limit).sum() > 0
+    h_ref = oracle.swiglu(g_np, u_np, limit)
+    assert np.max(np.abs(to_np(h).astype(np.float64) - h_ref)) <= H_TOL * np.max(np.abs(h_ref))
+
+    # the down projection takes h as its routed rows (no row ids): its quantise pass is the
+    # requantisation; checked against the oracle's act_quant + f64 reference of h
+    ws_dn = fp4.workspace_for(P, P, hidden, inter, recipe)
+    fp4.fp4_force_path(fp4.PATH_TC)
+    try:
+        d = fp4.fp4_grouped_expert_gemm(h, None, routing.offsets, dn.w, dn.sc, dn.scale2, recipe,
+                                        workspace=ws_dn)
+    finally:
+        fp4.fp4_force_path(fp4.PATH_AUTO)
+    proj_dn = synth.Projection("dn", h, synth.Routing(routing.offsets, routing.row_ids), dn,
+                               row_ids_used=False)
+    worst, rel = grouped_sampled_check(proj_dn, d, fp4.PATH_TC, np.arange(P), "fused chain down")
+    assert fp4.fp4_get_device_error() == 0
+    print("fused chain recipe %d: h bit-equal to the unfused chain; down worst err/bound %.3g" % (
+        recipe, worst))

@@ -254,6 +254,34 @@ def test_grouped_small_all_outputs(recipe, path):
     assert fp4.fp4_get_device_error() == 0
 
 
+@pytest.mark.parametrize("recipe", [fp4.NVFP4, fp4.MXFP4])
+def test_grouped_decode_many_experts_ragged_passes(recipe):
+    """The weight-streaming decode path over hundreds of experts holding 0-19 routed rows
+    each (passes of up to 8 rows, item runs that split a pass across CTAs), ragged n and a
+    k of several 512-k ring stages: every output against the oracle."""
+    gen = torch.Generator().manual_seed(31 + recipe)
+    E, T, n, k = 300, 64, 200, 1024
+    sizes = torch.randint(0, 20, (E,), generator=gen)
+    sizes[::7] = 0
+    offsets = torch.zeros(E + 1, dtype=torch.int32)
+    offsets[1:] = torch.cumsum(sizes, 0).to(torch.int32)
+    P = int(offsets[-1])
+    row_ids = torch.randint(0, T, (P,), generator=gen, dtype=torch.int32)
+    bank = synth.make_bank(recipe, E, n, k, 777 + recipe, "cpu", scale2_value=5.9945243e-5)
+    x = torch.randn(T, k, generator=gen) * 2
+    proj = synth.Projection("many", x.to(DEV), synth.Routing(offsets.to(DEV), row_ids.to(DEV)),
+                            synth.Bank(recipe, bank.w.to(DEV), bank.sc.to(DEV),
+                                       bank.scale2.to(DEV)))
+    fp4.fp4_force_path(fp4.PATH_STREAM)
+    try:
+        out, used = run_projection(proj)
+    finally:
+        fp4.fp4_force_path(fp4.PATH_AUTO)
+    assert used == fp4.PATH_STREAM
+    grouped_sampled_check(proj, out, used, np.arange(P), "decode many experts")
+    assert fp4.fp4_get_device_error() == 0
+
+
 def test_grouped_row_equals_single_row_launch():
     """P-ROW: a routed row's output equals the single-expert call on that row alone."""
     proj = _small_grouped(fp4.NVFP4)
