@@ -683,6 +683,7 @@ def run_ours(args, world, rank, local):
     # the step after the gate/up projection: SwiGLU + e4m3 requantisation of its output
     if args.workload == "c4" and not args.no_swiglu:
         result["swiglu_quant"] = measure_swiglu(fp4, device, peaks, peak_src)
+        result["moe_chain"] = measure_moe_chain(fp4, device, peaks, peak_src)
 
     # the routing front-end (before and after the projections)
     if args.workload == "c4" and not args.no_routing:
@@ -820,6 +821,77 @@ def measure_swiglu(fp4, device, peaks, peak_src, rows=32768, inter=1024, limit=7
                          "bytes_per_call": nbytes, "kernel": "swiglu_quant",
                          "peak_source": peak_src},
             "gpu_launches": iters}
+
+
+def measure_moe_chain(fp4, device, peaks, peak_src, T=4096, E=256, topk=8, hidden=7168,
+                      inter=2048, limit=7.0, steps=10):
+    """The prefill MoE layer body on the tensor-core path, gate/up projection -> SwiGLU ->
+    down projection (NVFP4, Zipf(1.1) top-8 routing, gate/up bank [2*inter, hidden], down
+    bank [hidden, inter]), two ways: unfused (gate/up output [P, 2*inter] written, then
+    fp4_swiglu_quant writes h) and fused (fp4_grouped_gate_up_swiglu writes h from the
+    gate/up epilogue). The down call quantises h itself (the requantisation)."""
+    import torch
+    from block_scaled_fp4_act_gb300 import synth
+    r = synth.zipf_topk(T, E, topk, 2004, device)
+    gen = torch.Generator(device=device).manual_seed(4)
+    x = synth.bf16_rounded(torch.randn(T, hidden, generator=gen, device=device))
+    gu = synth.make_bank(fp4.NVFP4, E, 2 * inter, hidden, 1104, device)
+    dn = synth.make_bank(fp4.NVFP4, E, hidden, inter, 1105, device)
+    P = r.P
+    ws1 = fp4.workspace_for(T, P, 2 * inter, hidden, fp4.NVFP4, device=device)
+    ws2 = fp4.workspace_for(P, P, hidden, inter, fp4.NVFP4, device=device)
+    gu_out = torch.empty(P, 2 * inter, device=device)
+    h = torch.empty(P, inter, device=device)
+    d = torch.empty(P, hidden, device=device)
+    codes = torch.empty(P, inter, dtype=torch.uint8, device=device)
+    scales = torch.empty(P, inter // 128, dtype=torch.float32, device=device)
+
+    def down():
+        fp4.fp4_grouped_expert_gemm(h, None, r.offsets, dn.w, dn.sc, dn.scale2, fp4.NVFP4,
+                                    out=d, workspace=ws2)
+
+    def unfused():
+        fp4.fp4_grouped_expert_gemm(x, r.row_ids, r.offsets, gu.w, gu.sc, gu.scale2, fp4.NVFP4,
+                                    out=gu_out, workspace=ws1)
+        fp4.fp4_swiglu_quant(gu_out[:, :inter], gu_out[:, inter:], limit, codes=codes,
+                             scales=scales, h_out=h)
+        down()
+
+    def fused():
+        fp4.fp4_grouped_gate_up_swiglu(x, r.row_ids, r.offsets, gu.w, gu.sc, gu.scale2,
+                                       fp4.NVFP4, limit, ws1, h=h)
+        down()
+
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name, fn in (("unfused", unfused), ("fused", fused)):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res[name] = e0.elapsed_time(e1) / steps
+    h_fused = h.clone()
+    unfused()
+    torch.cuda.synchronize()
+    same = bool(torch.equal(h, h_fused))
+    flops = 2.0 * P * (2 * inter) * hidden + 2.0 * P * hidden * inter
+    out = {"workload": "prefill MoE layer body, NVFP4: %d experts, %d tokens top-%d Zipf(1.1), "
+                       "gate/up [2x%d, %d] -> SwiGLU (swiglu_limit %g) -> down [%d, %d]" % (
+                           E, T, topk, inter, hidden, limit, hidden, inter),
+           "unfused_ms": round(res["unfused"], 4), "fused_ms": round(res["fused"], 4),
+           "saving_ms": round(res["unfused"] - res["fused"], 4),
+           "fused_tflops": round(flops / (res["fused"] * 1e-3) / 1e12, 1),
+           "h_bit_equal": same, "steps": steps,
+           "what": "fused: h from the gate/up epilogue; unfused: gate/up output written, then "
+                   "fp4_swiglu_quant"}
+    del gu, dn, ws1, ws2, gu_out, h, d, x
+    torch.cuda.empty_cache()
+    return out
 
 
 def measure_routing(fp4, device, peaks, peak_src, T=4096, E=256, topk=8, n=7168, iters=50):

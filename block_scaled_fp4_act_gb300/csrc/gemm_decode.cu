@@ -181,24 +181,30 @@ __device__ __forceinline__ void decode_prologue(const GroupedProblem &p, int64_t
         }
     }
     consumer_sync<NT>();
-    // phase 3: rescale in place: f16(code * 2^(m - M)) or bf16(code * 2^m), both exact
+    // phase 3: rescale in place: f16(code * 2^(m - M)) or bf16(code * 2^m), both exact;
+    // eight elements (16 bytes, inside one 128-block) per thread and step
     const bool f16 = *route_f16 != 0;
-    const int half = k >> 1;
-    for (int e2 = threadIdx.x; e2 < rows * half; e2 += NT) {
-        const int r = e2 / half, kk = (e2 - r * half) * 2;
-        uint32_t *pv = reinterpret_cast<uint32_t *>(act + (size_t)r * ld + kk);
-        const float s = ascale[r * kq + (kk >> 7)];
-        const uint32_t hv = *pv;
-        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hv));
-        uint32_t o;
-        if (f16) {
-            const float m = s * pow2_reciprocal(rowscale[r]);  // 2^(m - M) >= 2^-15, exact
-            const __half2 v = __floats2half2_rn(f.x * m, f.y * m);
-            o = *reinterpret_cast<const uint32_t *>(&v);
-        } else {
-            asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o) : "f"(f.y * s), "f"(f.x * s));
+    const int tid = threadIdx.x % NT;
+    for (int r = 0; r < rows; ++r) {
+        const float rinv = f16 ? pow2_reciprocal(rowscale[r]) : 1.0f;
+        for (int c = tid; c < (k >> 3); c += NT) {
+            uint4 *pv = reinterpret_cast<uint4 *>(act + (size_t)r * ld + c * 8);
+            const float s = ascale[r * kq + (c >> 4)];
+            const float m = f16 ? s * rinv : s;  // f16: 2^(m - M) >= 2^-15, exact
+            uint4 v = *pv;
+            uint32_t *w = &v.x;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[j]));
+                if (f16) {
+                    const __half2 h2 = __floats2half2_rn(f.x * m, f.y * m);
+                    w[j] = *reinterpret_cast<const uint32_t *>(&h2);
+                } else {
+                    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w[j]) : "f"(f.y * m), "f"(f.x * m));
+                }
+            }
+            *pv = v;
         }
-        *pv = o;
     }
     consumer_sync<NT>();
 }
