@@ -448,6 +448,10 @@ constexpr int kMinStages = 3;
 constexpr int kMaxExperts = 1024;
 constexpr int kPairBarrier = 2;                       // named barriers 2 .. 9: warp pairs
 constexpr int kPassCache = 8;                         // passes whose token ids are cached
+// Stages a producer keeps in flight (issued, not landed). On GB300 a read stream through
+// TMA reaches its peak with about 64 KB in flight per SM; more only lengthens the memory
+// queue, and with it the wait of every other read (the activation rows of a prologue).
+constexpr int kInFlight = 2;
 // the configuration the library launches: consumer warps and accumulator chains per warp
 constexpr int kWarps = 16;
 constexpr int kChains = 2;
@@ -649,14 +653,25 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1)
             // stream through TMA reaches about 0.92 of the copy bandwidth with this hint,
             // 0.82 without)
             const uint64_t policy = l2_evict_first_policy();
-            int slot = 0;
-            uint32_t phase = 0, issued = 0, parity = 0;
+            int slot = 0, oslot = 0, inflight = 0;  // oslot: the oldest stage still in flight
+            uint32_t phase = 0, ophase = 0, issued = 0, parity = 0;
             bool ok = true;
             for (int t = t0; t < t1 && ok; ++t) {
                 int e, pass, m;
                 item(t, e, pass, m);
                 const int y = e * n + m * BM;
                 for (int j = 0; j < nst; ++j) {
+                    if (inflight == kInFlight) {
+                        if (!mbar_wait(full(oslot), ophase, abort_flag, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        --inflight;
+                        if (++oslot == S) {
+                            oslot = 0;
+                            ophase ^= 1u;
+                        }
+                    }
                     if (!mbar_wait(empty(slot), phase ^ 1u, abort_flag, p.err)) {
                         ok = false;
                         break;
@@ -670,6 +685,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1)
                     tma_load_2d_evict_first(d0 + 2 * NIB_BOX, &tmS, j * (KS / GS), y, fb, policy);
                     issued |= 1u << slot;
                     parity = (parity & ~(1u << slot)) | (phase << slot);
+                    ++inflight;
                     if (++slot == S) {
                         slot = 0;
                         phase ^= 1u;
