@@ -669,13 +669,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int jj = 0; jj < 32; ++jj) {
                     // f16_route is uniform over the CTA, so every lane takes the shuffle
                     const float r = f16_route ? __shfl_sync(0xFFFFFFFFu, rs, jj) : 1.0f;
-                    const float val = (__uint_as_float(v[jj]) * r) * s2;
-                    if (SWIGLU) {
+                    if constexpr (SWIGLU) {
+                        const float val = (__uint_as_float(v[jj]) * r) * s2;
                         const float up = __shfl_xor_sync(0xFFFFFFFFu, val, 16);
                         if (colok && c0 + jj < tl.rows)
                             orow[(int64_t)(c0 + jj) * ldo] = swiglu_one(val, up, p.limit);
-                    } else if (colok && c0 + jj < tl.rows) {
-                        orow[(int64_t)(c0 + jj) * ldo] = val;
+                    } else {
+                        if (colok && c0 + jj < tl.rows)
+                            orow[(int64_t)(c0 + jj) * ldo] = (__uint_as_float(v[jj]) * r) * s2;
                     }
                 }
             }
