@@ -18,9 +18,9 @@
 // Kernel structure: persistent, one CTA (24 warps) per SM, static round-robin over
 // tiles (expert, 192-row block of its routed rows, 128-row block of its weights),
 // weight-row block fastest so consecutive tiles share the activation block in L2.
-// Rings decouple the streams: a 5-slot shared-memory weight ring (each slot 256 k of the
+// Rings decouple the streams: a 4-slot shared-memory weight ring (each slot 256 k of the
 // tile's 128 weight rows: 128-byte nibble lines in the 128-byte swizzle + 16 scale bytes
-// per row; the weights stream from HBM once per tile), a 4-slot activation ring in shared
+// per row; the weights stream from HBM once per tile), a 6-slot activation ring in shared
 // memory and a 4-stage ring of converted 64-k weight stages in tensor memory, from which
 // the MMA reads its A operand.
 //   warp 0      TMA producer of activation slots (16-bit, 128B swizzle, k-block-major)
@@ -72,9 +72,11 @@ constexpr int BK = 64;
 // Weight ring: a slot holds 256 k (W_KS k-stages) of a tile's 128 weight rows, so every
 // row of the nibble box is one whole 128-byte line and one TMA pair feeds four k-stages.
 constexpr int W_KS = 4;
-constexpr int W_STAGES = 5;   // weight ring slots (20 k-stages ahead): it streams from HBM
+constexpr int W_STAGES = 3;   // weight ring slots (12 k-stages ahead): it streams from HBM
 constexpr int A_STAGES = 4;   // converted weight tiles, in tensor memory
-constexpr int B_STAGES = 4;   // activation tiles (mostly L2 hits: shared by a tile's neighbours)
+// Activation slots. A 192-row tile takes a slot per k-stage, so the ring's slot count is
+// its prefetch depth; measured on GB300, 4 slots held 192-row tiles to ~2x the MMA time.
+constexpr int B_STAGES = 5;
 constexpr int kMaxExperts = 1024;
 // Converter warps per TMEM lane quarter; one of them converts each k-stage of the
 // quarter's 32 weight rows, so they take turns over the stages.
@@ -106,7 +108,7 @@ static_assert(kACol + A_STAGES * (BK / 2) <= 512, "tensor memory budget");
 // Activation tiles are loaded k-block-major: one TMA box holds up to 8 k-blocks of a small
 // tile (32 rows x 8, 64 x 4, 128 x 2 k-blocks, or BN rows x 1), so small tiles keep many
 // k-stages in flight in the same ring slots.
-constexpr int B_BYTES = 32 * 8 * BK * 2;  // one ring slot (the largest box)
+constexpr int B_BYTES = 32 * 8 * BK * 2;  // one ring slot (the largest box: 32 rows x 8 k-blocks)
 constexpr int NIB_BYTES = BM * BK * W_KS / 2;  // 128 rows x 128 bytes, 128-byte swizzle
 constexpr int SC_BYTES = BM * 16;               // 16 scale bytes per row (256 k NVFP4)
 constexpr int W_BYTES = NIB_BYTES + SC_BYTES;
@@ -287,6 +289,7 @@ __device__ __forceinline__ int bmap_index(int rows)
 
 // Rows and k-blocks of activation box bi.
 __host__ __device__ constexpr int bmap_rows(int bi) { return bi < 3 ? 32 << bi : BN; }
+// k-blocks a slot holds: as many as fit in its 32 KB
 __host__ __device__ constexpr int bmap_kblocks(int bi) { return 8 >> bi; }
 
 // SWIGLU: the weight maps have 16-row boxes; each weight slot is filled by eight of them
@@ -477,12 +480,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int buf = it & 1;
             const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
             const int bi = bmap_index(rows);
-            const int kbmask = bmap_kblocks(bi) - 1;
+            const int kbps = bmap_kblocks(bi);
             const uint32_t kb_desc = (uint32_t)(bmap_rows(bi) * BK * 2) >> 4;  // one k-block
+            int j = 0;  // k-block of the current activation slot
             // one k-stage; the relay has seen: accumulator free (kb 0), activation slot full
             // (j 0), converted weight slot full
             auto stage = [&](int kb) {
-                const int j = kb & kbmask;
                 const int as = (int)(st % A_STAGES);
                 tc_fence_after();
                 const uint32_t a_tmem = a_tmem0 + (uint32_t)(as * (BK / 2));
@@ -494,9 +497,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             (kb | kk) != 0 ? 1u : 0u);
                 mma_commit_warp(aempty(as));
                 ++st;
-                if (j == kbmask || kb == nkb - 1) {
+                if (j == kbps - 1 || kb == nkb - 1) {
                     mma_commit_warp(bempty(bslot));
                     bslot = bslot + 1 == B_STAGES ? 0 : bslot + 1;
+                    j = 0;
+                } else {
+                    ++j;
                 }
             };
             stage(0);
@@ -524,9 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // published before the arrival that releases the tile's first stage
             tile_info[it % kTileInfo] = tl.rows;
             bool ok = warp_mbar_wait(acce(buf), ((it >> 1) & 1) ^ 1u, abort_flag, p.err, p.wait_limit);
-            const int kbmask = bmap_kblocks(bmap_index(tl.rows)) - 1;
+            const int kbps = bmap_kblocks(bmap_index(tl.rows));
+            int j = 0;  // k-block of the current activation slot
             for (int kb = 0; kb < nkb; ++kb) {
-                const int j = kb & kbmask;
                 if (ok && j == 0)
                     ok = warp_mbar_wait(bfull(rb.slot), rb.phase, abort_flag, p.err, p.wait_limit);
                 if (ok)
@@ -544,8 +550,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 named_arrive(kNamedAReady + ra.slot, kNamedThreads);
                 ra.next();
-                if (j == kbmask || kb == nkb - 1)
+                if (j == kbps - 1 || kb == nkb - 1) {
                     rb.next();
+                    j = 0;
+                } else {
+                    ++j;
+                }
             }
             if (stuck)
                 break;
