@@ -282,6 +282,30 @@ def test_grouped_decode_many_experts_ragged_passes(recipe):
     assert fp4.fp4_get_device_error() == 0
 
 
+@pytest.mark.parametrize("E", [1024, 1025])
+def test_grouped_decode_expert_limit(E):
+    """The most experts the TMA-fed decode kernel takes (1024), and one more (the
+    per-lane-load kernel then runs): routed rows on a few hundred experts, every output."""
+    gen = torch.Generator().manual_seed(E)
+    n, k, T = 64, 512, 32
+    sizes = torch.zeros(E, dtype=torch.int64)
+    hot = torch.randperm(E, generator=gen)[:300]
+    sizes[hot] = torch.randint(1, 4, (300,), generator=gen)
+    offsets = torch.zeros(E + 1, dtype=torch.int32)
+    offsets[1:] = torch.cumsum(sizes, 0).to(torch.int32)
+    P = int(offsets[-1])
+    row_ids = torch.randint(0, T, (P,), generator=gen, dtype=torch.int32)
+    bank = synth.make_bank(fp4.NVFP4, E, n, k, 555, "cpu", scale2_value=5.9945243e-5)
+    x = torch.randn(T, k, generator=gen)
+    proj = synth.Projection("limit", x.to(DEV), synth.Routing(offsets.to(DEV), row_ids.to(DEV)),
+                            synth.Bank(fp4.NVFP4, bank.w.to(DEV), bank.sc.to(DEV),
+                                       bank.scale2.to(DEV)))
+    out, used = run_projection(proj, workspace=None)
+    assert used == fp4.PATH_STREAM
+    grouped_sampled_check(proj, out, used, np.arange(P), "decode %d experts" % E)
+    assert fp4.fp4_get_device_error() == 0
+
+
 def test_grouped_row_equals_single_row_launch():
     """P-ROW: a routed row's output equals the single-expert call on that row alone."""
     proj = _small_grouped(fp4.NVFP4)

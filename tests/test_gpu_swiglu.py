@@ -101,3 +101,38 @@ def test_swiglu_prefill_shape_sampled():
     g = gu[idx, :inter]
     u = gu[idx, inter:]
     _check(g, u, 7.0, codes[idx], scales[idx], h[idx], "prefill sampled")
+
+
+@pytest.mark.parametrize("recipe", [0, 1])
+@pytest.mark.parametrize("inter", [64, 192])
+def test_fused_gate_up_swiglu_ragged(recipe, inter):
+    """fp4_grouped_gate_up_swiglu with inter a multiple of 64 but not of 128 (one and three
+    64-column tiles), ragged and empty experts: h against the oracle's SwiGLU of the same
+    call's unfused gate/up output (computed on the tensor cores too), within 2e-6 max|h|."""
+    from block_scaled_fp4_act_gb300 import synth
+    fp4.build.build()
+    gen = torch.Generator().manual_seed(90 + inter + recipe)
+    sizes = [0, 37, 200, 1, 0, 65]
+    E, T, k, limit = len(sizes), 96, 512, 6.0
+    offsets = torch.zeros(E + 1, dtype=torch.int32)
+    offsets[1:] = torch.cumsum(torch.tensor(sizes), 0).to(torch.int32)
+    P = int(offsets[-1])
+    row_ids = torch.randint(0, T, (P,), generator=gen, dtype=torch.int32)
+    bank = synth.make_bank(recipe, E, 2 * inter, k, 91 + recipe, "cpu")
+    x = torch.randn(T, k, generator=gen) * 3
+    x[::5] *= 50.0
+    xd, rid, off = x.to(DEV), row_ids.to(DEV), offsets.to(DEV)
+    w, sc, s2 = bank.w.to(DEV), bank.sc.to(DEV), bank.scale2.to(DEV)
+    ws = fp4.workspace_for(T, P, 2 * inter, k, recipe)
+    fp4.fp4_force_path(fp4.PATH_TC)
+    try:
+        gu = fp4.fp4_grouped_expert_gemm(xd, rid, off, w, sc, s2, recipe, workspace=ws)
+    finally:
+        fp4.fp4_force_path(fp4.PATH_AUTO)
+    h = fp4.fp4_grouped_gate_up_swiglu(xd, rid, off, w, sc, s2, recipe, limit, ws)
+    g_np, u_np = gu[:, :inter].cpu().numpy(), gu[:, inter:].cpu().numpy()
+    assert (g_np > limit).any() and (np.abs(u_np) > limit).any()
+    ref = oracle.swiglu(g_np, u_np, limit)
+    err = np.max(np.abs(h.cpu().numpy().astype(np.float64) - ref))
+    assert err <= H_TOL * np.max(np.abs(ref)), err
+    assert fp4.fp4_get_device_error() == 0
