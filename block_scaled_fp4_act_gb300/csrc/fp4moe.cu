@@ -98,11 +98,11 @@ static bool recipe_ok(int r)
 
 // Rows per expert (on average) at or above which the tensor-core path, workspace pass
 // included, is faster than the warp-MMA decode kernel. Measured on GB300 (bench.py
-// --path-sweep: 64 NVFP4 experts, [3072, 4096], L2 flushed): decode 140 / 230 / 433 us at
-// 4 / 8 / 16 rows per expert, tensor cores 225 / 225 / 227 us. The decode kernel
-// re-converts the weights once per pass of up to 8 rows; the tensor-core kernel once per
-// 192-row tile.
-constexpr int64_t kTcMinRowsPerExpert = 8;
+// --path-sweep: 64 NVFP4 experts, [3072, 4096], L2 flushed): decode 107 / 117 / 193 us at
+// 4 / 8 / 16 rows per expert, tensor cores 180 us throughout. The decode kernel streams
+// the weights once per pass of up to 8 rows, so from 9 rows it streams them twice; the
+// tensor-core kernel converts them once per 192-row tile.
+constexpr int64_t kTcMinRowsPerExpert = 9;
 
 static int choose_path(int64_t P, int E, int64_t n, int64_t k, int recipe, bool have_ws)
 {
@@ -124,9 +124,10 @@ static int choose_path_for(const GroupedProblem &p, bool have_ws)
     return path;
 }
 
-// The path that needs no workspace: the warp-MMA decode kernel wherever 4 activation rows
-// of length k fit in its shared memory (k <= 28544; 8 rows per pass where they fit and
-// experts average more than 4), the FMA streaming kernel (1-2 rows per pass) beyond.
+// The path that needs no workspace: the warp-MMA decode kernels wherever 4 activation rows
+// of length k fit in shared memory (k <= 28544; 8 rows per pass where they fit and experts
+// average more than 4): TMA-fed where k is a multiple of 512, per-lane loads otherwise;
+// the FMA streaming kernel (1-2 rows per pass) beyond.
 static cudaError_t launch_streaming(const GroupedProblem &p, cudaStream_t s)
 {
     if (decode_fits(p.k))

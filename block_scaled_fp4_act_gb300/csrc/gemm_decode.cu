@@ -27,6 +27,11 @@
 //
 // Summation: one f32 accumulation per MMA (k/16 of them), then the row scale (exact) and
 // scale2, the same depth as the tcgen05 path.
+//
+// Two kernels share this MMA step (mma_block): decode_tma_kernel, whose weights arrive by
+// TMA into a shared-memory ring (k a multiple of 512, at most 1024 experts, 16-byte aligned
+// banks; its lanes read the same bytes from the ring), and decode_mma_kernel, whose lanes
+// load their bytes from global memory themselves (every other shape).
 #include "common.cuh"
 #include "tma_host.h"
 

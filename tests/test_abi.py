@@ -187,9 +187,9 @@ def test_status_strings_and_error_model(lib):
 def test_path_choice_by_shape(lib):
     # decode-sized (about one row per expert) always streams
     assert fp4.fp4_gemm_path(64, 64, 3072, 4096, fp4.NVFP4, True) == fp4.PATH_STREAM
-    # the tensor-core path from 8 routed rows per expert on average, given a workspace
-    assert fp4.fp4_gemm_path(7 * 64, 64, 3072, 4096, fp4.NVFP4, True) == fp4.PATH_STREAM
-    assert fp4.fp4_gemm_path(8 * 64, 64, 3072, 4096, fp4.NVFP4, True) == fp4.PATH_TC
+    # the tensor-core path from 9 routed rows per expert on average, given a workspace
+    assert fp4.fp4_gemm_path(8 * 64, 64, 3072, 4096, fp4.NVFP4, True) == fp4.PATH_STREAM
+    assert fp4.fp4_gemm_path(9 * 64, 64, 3072, 4096, fp4.NVFP4, True) == fp4.PATH_TC
     # without a workspace there is only the streaming path
     assert fp4.fp4_gemm_path(32768, 256, 2048, 7168, fp4.NVFP4, False) == fp4.PATH_STREAM
     fp4.fp4_force_path(fp4.PATH_TC)
