@@ -125,10 +125,11 @@ int fp4_grouped_expert_gemm(const float *x, int64_t num_tokens, const int32_t *r
  * fp4_grouped_quantize followed by fp4_grouped_gemm_quantized on the same stream.
  *
  * fp4_grouped_quantize -- stage 1 (fn quant_rows of dsv4_native_gemm_gate.rs) written into
- * the workspace as the 16-bit operands of the tensor-core GEMM: f16(code * 2^(m - M)) with
- * a per-row power-of-two scale 2^M (NVFP4, while every 128-block of the row lies within
- * 2^15 of its largest) or bf16(code * 2^m) (MXFP4, and NVFP4 calls with a wider row). Both
- * are exact. When row ids repeat tokens (row_ids given and num_tokens < total_rows) each
+ * the workspace as the operands of the tensor-core GEMM. NVFP4: the 16-bit operands
+ * f16(code * 2^(m - M)) with a per-row power-of-two scale 2^M (while every 128-block of the
+ * row lies within 2^15 of its largest) or bf16(code * 2^m) (calls with a wider row), both
+ * exact. MXFP4: the e4m3 codes themselves and each block's scale exponent as a byte (the
+ * block-scaled 8-bit MMA's own operand and scale formats). When row ids repeat tokens (row_ids given and num_tokens < total_rows) each
  * token row is quantised once and the result copied to its routed rows; otherwise every
  * routed row x[row_ids[p]] (x[p]) is quantised. The workspace layout is private to the
  * library.
@@ -170,9 +171,12 @@ int fp4_grouped_gemm_quantized(const void *workspace, size_t workspace_bytes,
  * holds until the process exits. The pages have no counterpart of this call.
  *   Arguments: as fp4_grouped_expert_gemm without workspace/workspace_bytes.
  *   Limit: the call needs fp4_grouped_workspace_size(num_tokens, total_rows, n, k, recipe)
- *          = 2048 + R(2 * total_rows * k) + R(4 * total_rows), plus R(2 * num_tokens * k) +
- *          R(4 * num_tokens) when num_tokens < total_rows, bytes of scratch (R rounds up to
- *          a multiple of 1024), at most 32 MiB (e.g. 2048 routed rows at k = 7168, or 2048
+ *          bytes of scratch, at most 32 MiB: for NVFP4 2048 + R(2 * total_rows * k) +
+ *          R(4 * total_rows), plus R(2 * num_tokens * k) + R(4 * num_tokens) when
+ *          num_tokens < total_rows; for MXFP4 1024 + R(total_rows * k) +
+ *          R(k/128 * P16(total_rows)), plus R(num_tokens * k) + R(k/128 * P16(num_tokens))
+ *          when num_tokens < total_rows (R rounds up to a multiple of 1024, P16 to a
+ *          multiple of 16) (e.g. 2048 routed rows at k = 7168, or 2048
  *          routed rows of 256 tokens); larger calls return
  *          FP4_ERR_WORKSPACE (the message in fp4_last_error gives both numbers), shapes the
  *          tensor-core path does not take (k not a multiple of 16*gs, more than 1024
