@@ -23,6 +23,11 @@ Functions and the page passages they follow (memra-engine docs.rs source pages):
                       |gpu - f64| <= n_ops * 2^-24 * sum|p_scaled|
   max_rel             the `rel` convention of kernel_check.rs:
                       max|gpu - ref| / max(max|ref|, 1e-3)
+  act_quant_w4a4      0.71.0 kernel_check.rs, NVFP4 W4A4 MMQ GEMM section: two-level
+                      scaling (row scale + e4m3 micro-scale per 16; readings in oracle.c)
+  act_quant_w4a4_v1   same section, the sub-block-only quantiser it is compared with
+  gemm_ref_w4a4       f64 GEMM of the dequantised W4A4 operands (+ sum of |products|)
+  per_token_rel       same section, the dynamic-range arm's per-token relative error
 
 Pins (tests/test_oracle_pins.py) tie every function to something other than itself.
 """
@@ -73,6 +78,14 @@ def _load():
         lib.orc_route_csr.restype = i32
         lib.orc_moe_combine.argtypes = [P, P, P, i64, i32, i64, P, P]
         lib.orc_moe_combine.restype = None
+        lib.orc_e2m1_encode.argtypes = [f32]
+        lib.orc_e2m1_encode.restype = u8
+        lib.orc_act_quant_w4a4.argtypes = [P, i64, i64, P, P, P]
+        lib.orc_act_quant_w4a4.restype = None
+        lib.orc_act_quant_w4a4_v1.argtypes = [P, i64, i64, P, P]
+        lib.orc_act_quant_w4a4_v1.restype = None
+        lib.orc_gemm_ref_w4a4.argtypes = [P, P, P, P, P, f32, i64, i64, i64, P, P]
+        lib.orc_gemm_ref_w4a4.restype = None
         _lib = lib
     return _lib
 
@@ -238,6 +251,93 @@ def grouped_ref_sampled(x, row_ids, offsets, w, sc, scale2, recipe, sample_p, sa
     return out, absp
 
 
+# --------------------------------------------------------------------------- W4A4 variant
+
+def e2m1_encode(values):
+    """Element-wise nearest E2M1 code (ties to the even code, saturating at 6, sign kept)."""
+    lib = _load()
+    v = _c(values, np.float32)
+    out = np.empty(v.shape, dtype=np.uint8)
+    flat_v, flat_o = v.reshape(-1), out.reshape(-1)
+    enc = lib.orc_e2m1_encode
+    for i in range(flat_v.size):
+        flat_o[i] = enc(float(flat_v[i]))
+    return out
+
+
+def act_quant_w4a4(x):
+    """Two-level W4A4 activation quantisation: x f32 [rows, k] (k % 16 == 0) ->
+    (codes u8 [rows, k/2] nibble pairs, scales u8 [rows, k/16] e4m3, rowscale f32 [rows])."""
+    x = _c(x, np.float32)
+    rows, k = x.shape
+    assert k % 16 == 0
+    codes = np.empty((rows, k // 2), dtype=np.uint8)
+    scales = np.empty((rows, k // 16), dtype=np.uint8)
+    rs = np.empty(rows, dtype=np.float32)
+    _load().orc_act_quant_w4a4(_ptr(x), rows, k, _ptr(codes), _ptr(scales), _ptr(rs))
+    return codes, scales, rs
+
+
+def act_quant_w4a4_v1(x):
+    """The page's sub-block-only quantiser (V1): (codes [rows, k/2], scales [rows, k/16])."""
+    x = _c(x, np.float32)
+    rows, k = x.shape
+    assert k % 16 == 0
+    codes = np.empty((rows, k // 2), dtype=np.uint8)
+    scales = np.empty((rows, k // 16), dtype=np.uint8)
+    _load().orc_act_quant_w4a4_v1(_ptr(x), rows, k, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def unpack_nibbles(packed):
+    """[rows, k/2] nibble pairs -> [rows, k] nibbles (low nibble = even k)."""
+    packed = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(packed.shape[:-1] + (packed.shape[-1] * 2,), dtype=np.uint8)
+    out[..., 0::2] = packed & 0x0F
+    out[..., 1::2] = packed >> 4
+    return out
+
+
+def dequant_w4a4(codes, scales, rowscale=None):
+    """x^ f64 [rows, k] = E2M1(code) * e4m3(scale of its 16-block) * rowscale."""
+    q = e2m1_decode(unpack_nibbles(codes))
+    s = np.repeat(e4m3_decode(scales), 16, axis=-1)
+    x = q * s
+    if rowscale is not None:
+        x = x * np.asarray(rowscale, dtype=np.float64)[:, None]
+    return x
+
+
+def gemm_ref_w4a4(codes, scales, rowscale, w, sc, scale2):
+    """f64 W4A4 reference: codes [g,k/2], scales [g,k/16], rowscale [g] or None,
+    w [n,k/2], sc [n,k/16] e4m3, scale2 -> (out f64 [g,n], absp f64 [g,n])."""
+    codes, scales = _c(codes, np.uint8), _c(scales, np.uint8)
+    w, sc = _c(w, np.uint8), _c(sc, np.uint8)
+    g, k2 = codes.shape
+    k = 2 * k2
+    n = w.shape[0]
+    assert scales.shape == (g, k // 16) and w.shape == (n, k2) and sc.shape == (n, k // 16)
+    rs = None if rowscale is None else _c(rowscale, np.float32)
+    out = np.empty((g, n), dtype=np.float64)
+    absp = np.empty((g, n), dtype=np.float64)
+    _load().orc_gemm_ref_w4a4(_ptr(codes), _ptr(scales), _ptr(rs), _ptr(w), _ptr(sc),
+                              float(scale2), g, n, k, _ptr(out), _ptr(absp))
+    return out, absp
+
+
+def per_token_rel(y, ref):
+    """The dynamic-range arm's measure: max over rows of max|y - ref| / max|ref| (rows
+    whose reference is all zero count 0)."""
+    y = np.asarray(y, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    worst = 0.0
+    for i in range(ref.shape[0]):
+        s = float(np.max(np.abs(ref[i]))) if ref.shape[1] else 0.0
+        if s > 0.0:
+            worst = max(worst, float(np.max(np.abs(y[i] - ref[i]))) / s)
+    return worst
+
+
 # --------------------------------------------------------------------------- routing front-end
 
 def route_topk(logits, topk, renormalize=False):
@@ -319,4 +419,5 @@ def lib_path():
 __all__ = ["NVFP4", "MXFP4", "e4m3_decode", "e2m1_decode", "e8m0_decode", "e4m3_encode",
            "pow2_ceil", "e4m3_threshold", "act_quant", "gemm_ref", "grouped_ref_sampled",
            "route_topk", "route_csr", "moe_combine", "within_bound", "max_rel", "lib_path",
-           "U32"]
+           "U32", "e2m1_encode", "act_quant_w4a4", "act_quant_w4a4_v1", "unpack_nibbles",
+           "dequant_w4a4", "gemm_ref_w4a4", "per_token_rel"]

@@ -27,6 +27,29 @@
  *   [G]  same page as [Q], the swiglu_limit saturation cell and the f64 check of main:
  *        h = g * (1 / (1 + exp(-g))) * u with u = clamp(up, -L, L) and g = min(gate, L)
  *        (up clamped on both sides, gate on one side, both before the sigmoid).
+ *   [W]  memra-engine 0.71.0, src/bin/kernel_check.rs, the NVFP4 W4A4 MMQ GEMM section:
+ *        E2M1 activations with two-level scaling (a per-token row scale from the row amax,
+ *        applied after the sum, and a UE4M3 micro-scale of amax_sub / 6 per 16 values), the
+ *        sub-block-only quantiser ("V1") it is compared with, and the dynamic-range arm
+ *        where the row scale must beat sub-block-only scaling per token.
+ *
+ * Readings for [W] (the page names the two levels but prints neither formula):
+ *   row scale      r = amax_row / (6 * 448) in f32, so that the loudest sub-block's
+ *                  micro-scale lands on the top of the e4m3 range; r = 0 for a zero row,
+ *                  whose codes and micro-scales are all zero.
+ *   normalised row y = x / r (f32), sub-block amax m = max |y| over its 16 values.
+ *   micro-scale    s = e4m3 code nearest to m / 6 (f32 division, then the e4m3 encoding
+ *                  above, ties to the even code); S its value.
+ *   code           E2M1 value nearest to y / S (f32 division), ties to the even code,
+ *                  magnitudes above 6 saturate to 6, sign kept (negative values that
+ *                  round to zero give the code 0x8); every code of a block with S = 0 is 0.
+ *   V1             the same without the row scale: s = nearest e4m3 code to amax_sub / 6,
+ *                  raised to the smallest positive code (0x01) when that rounds to zero and
+ *                  amax_sub > 0 (the page: the micro-scale clamps), saturating at 448.
+ *   The page's "/2 in ue4m3_to_fp32" belongs to a storage that keeps the E2M1 grid doubled;
+ *   with the plain E2M1 grid used here the micro-scale is the plain e4m3 value.
+ *   Dequantised activation x^ = E2M1(code) * S * r; the W4A4 reference is f64 over
+ *   x^ and the NVFP4 weight E2M1 * e4m3 * scale2, every product exact.
  *
  * Readings where the pages import a helper without printing it (each is a plain
  * definition written out here):
@@ -117,7 +140,7 @@ uint8_t orc_e4m3_encode(float v)
     const double a = fabs((double)v);
     int c;
     if (a >= g_grid[126]) {
-        c = 126; /* only reached at |v| = 448 inside the contract (inputs are clamped) */
+        c = 126; /* |v| = 448 under [Q]'s clamp; the W4A4 micro-scale can pass 448 by an ulp */
     } else {
         int lo = 0, hi = 126; /* invariant: g_grid[lo] <= a < g_grid[hi] */
         while (hi - lo > 1) {
@@ -461,4 +484,132 @@ void orc_moe_combine(const float *out, const int32_t *pair_rows, const float *we
             y[t * n + c] = acc;
             absy[t * n + c] = aabs;
         }
+}
+
+/* ------------------------------------------------------------------ W4A4 [W] */
+
+uint8_t orc_e2m1_encode(float v)
+{
+    /* Nearest E2M1 magnitude by exhaustive search over the eight non-negative codes (their
+     * values increase with the code); on a tie the even code wins. Magnitudes of 6 and
+     * above saturate to 6 (code 7) directly: far above 6 every distance rounds alike. */
+    init_tables();
+    const int neg = signbit(v) ? 1 : 0;
+    const double a = fabs((double)v);
+    if (a >= 6.0)
+        return (uint8_t)(7 | (neg ? 0x8 : 0x0));
+    int best = 0;
+    double bestd = a - g_e2m1[0];
+    for (int c = 1; c < 8; ++c) {
+        const double d = fabs(a - g_e2m1[c]);
+        if (d < bestd || (d == bestd && (c & 1) == 0 && (best & 1) != 0)) {
+            best = c;
+            bestd = d;
+        }
+    }
+    return (uint8_t)(best | (neg ? 0x8 : 0x0));
+}
+
+/* Quantise the 16 values v[0..15] against the micro-scale of e4m3 code s into codes16
+ * (one nibble per value, unpacked). */
+static void e2m1_block(const float *v, uint8_t s, uint8_t *codes16)
+{
+    const float S = (float)g_e4m3[s];
+    for (int i = 0; i < 16; ++i)
+        codes16[i] = S == 0.0f ? 0 : orc_e2m1_encode(v[i] / S);
+}
+
+static void pack_nibbles(const uint8_t *codes16, uint8_t *dst8)
+{
+    for (int i = 0; i < 8; ++i)
+        dst8[i] = (uint8_t)(codes16[2 * i] | (codes16[2 * i + 1] << 4));
+}
+
+void orc_act_quant_w4a4(const float *x, int64_t rows, int64_t k, uint8_t *codes, uint8_t *scales,
+                        float *rowscale)
+{
+    init_tables();
+    const int64_t nb = k / 16;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *row = x + r * k;
+        float amax = 0.0f;
+        for (int64_t i = 0; i < k; ++i)
+            if (fabsf(row[i]) > amax)
+                amax = fabsf(row[i]);
+        const float rs = amax / 2688.0f; /* 6 * 448 */
+        rowscale[r] = rs;
+        for (int64_t j = 0; j < nb; ++j) {
+            float y[16];
+            uint8_t c16[16];
+            uint8_t s = 0;
+            if (rs != 0.0f) {
+                float m = 0.0f;
+                for (int i = 0; i < 16; ++i) {
+                    y[i] = row[j * 16 + i] / rs;
+                    if (fabsf(y[i]) > m)
+                        m = fabsf(y[i]);
+                }
+                s = orc_e4m3_encode(m / 6.0f);
+                e2m1_block(y, s, c16);
+            } else {
+                memset(c16, 0, sizeof c16);
+            }
+            scales[r * nb + j] = s;
+            pack_nibbles(c16, codes + r * (k / 2) + j * 8);
+        }
+    }
+}
+
+void orc_act_quant_w4a4_v1(const float *x, int64_t rows, int64_t k, uint8_t *codes,
+                           uint8_t *scales)
+{
+    init_tables();
+    const int64_t nb = k / 16;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t j = 0; j < nb; ++j) {
+            const float *v = x + r * k + j * 16;
+            float m = 0.0f;
+            for (int i = 0; i < 16; ++i)
+                if (fabsf(v[i]) > m)
+                    m = fabsf(v[i]);
+            uint8_t s = orc_e4m3_encode(m / 6.0f);
+            if (s == 0 && m > 0.0f)
+                s = 0x01;
+            uint8_t c16[16];
+            e2m1_block(v, s, c16);
+            scales[r * nb + j] = s;
+            pack_nibbles(c16, codes + r * (k / 2) + j * 8);
+        }
+    }
+}
+
+void orc_gemm_ref_w4a4(const uint8_t *codes, const uint8_t *scales, const float *rowscale,
+                       const uint8_t *w, const uint8_t *sc, float scale2, int64_t g, int64_t n,
+                       int64_t k, double *out, double *absp)
+{
+    init_tables();
+    const int64_t nb = k / 16;
+    for (int64_t row = 0; row < g; ++row) {
+        const double rs = rowscale ? (double)rowscale[row] : 1.0;
+        const double outer = rs * (double)scale2;
+        for (int64_t col = 0; col < n; ++col) {
+            double acc = 0.0, aabs = 0.0;
+            for (int64_t j = 0; j < nb; ++j) {
+                const double sa = g_e4m3[scales[row * nb + j]];
+                const double sw = g_e4m3[sc[col * nb + j]];
+                for (int i = 0; i < 16; ++i) {
+                    const int64_t kk = j * 16 + i;
+                    const uint8_t ab = codes[row * (k / 2) + (kk >> 1)];
+                    const uint8_t wb = w[col * (k / 2) + (kk >> 1)];
+                    const uint8_t an = (kk & 1) ? (uint8_t)(ab >> 4) : (uint8_t)(ab & 0x0F);
+                    const uint8_t wn = (kk & 1) ? (uint8_t)(wb >> 4) : (uint8_t)(wb & 0x0F);
+                    const double p = g_e2m1[an] * sa * g_e2m1[wn] * sw * outer;
+                    acc += p;
+                    aabs += fabs(p);
+                }
+            }
+            out[row * n + col] = acc;
+            absp[row * n + col] = aabs;
+        }
+    }
 }

@@ -53,6 +53,20 @@ int orc_route_csr(const int32_t *ids, int64_t T, int topk, int E, int32_t *offse
 void orc_moe_combine(const float *out, const int32_t *pair_rows, const float *weights,
                      int64_t T, int topk, int64_t n, double *y, double *absy);
 
+/* W4A4 (two-level scaling; readings in oracle.c): x [rows,k] f32, k % 16 == 0 ->
+ * codes [rows,k/2] nibble pairs (low nibble = even k), scales [rows,k/16] e4m3 bytes,
+ * rowscale [rows] f32. The V1 form has no row scale. */
+uint8_t orc_e2m1_encode(float v);
+void orc_act_quant_w4a4(const float *x, int64_t rows, int64_t k, uint8_t *codes, uint8_t *scales,
+                        float *rowscale);
+void orc_act_quant_w4a4_v1(const float *x, int64_t rows, int64_t k, uint8_t *codes,
+                           uint8_t *scales);
+/* f64 reference of the W4A4 GEMM: out/absp [g,n]; rowscale nullable (1); w [n,k/2],
+ * sc [n,k/16] e4m3 bytes, scale2 the weight tensor's factor. */
+void orc_gemm_ref_w4a4(const uint8_t *codes, const uint8_t *scales, const float *rowscale,
+                       const uint8_t *w, const uint8_t *sc, float scale2, int64_t g, int64_t n,
+                       int64_t k, double *out, double *absp);
+
 #ifdef __cplusplus
 }
 #endif

@@ -638,3 +638,215 @@ def test_moe_combine_closed_forms():
     np.testing.assert_allclose(y, want, rtol=1e-13, atol=1e-13)
     np.testing.assert_allclose(absy, np.einsum("tj,tjc->tc", np.abs(w.astype(np.float64)),
                                                np.abs(out[prow].astype(np.float64))), rtol=1e-13)
+
+
+# ----------------------------------------------------------------- W4A4 variant
+# NVFP4 W4A4 MMQ GEMM section of memra-engine 0.71.0 src/bin/kernel_check.rs: two-level
+# activation scaling (row scale + e4m3 micro-scale per 16), its sub-block-only form (V1),
+# the informational rel band and the dynamic-range arm.
+
+def _w4a4_examples(golden_dir):
+    out = []
+    with open(os.path.join(golden_dir, "w4a4_examples.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            ident, vals, rs, sc, by, v1sc, v1by = [p.strip() for p in line.split("|")]
+            x = np.zeros(32, dtype=np.float32)
+            if vals != "-":
+                for item in vals.split(","):
+                    i, v = item.split(":")
+                    x[int(i)] = np.float32(float(v))
+            if "/" in rs:
+                a, b = rs.split("/")
+                rsv = np.float32(float(a)) / np.float32(float(b))
+            else:
+                rsv = np.float32(float(rs))
+
+            def table(spec, size):
+                t = np.zeros(size, dtype=np.uint8)
+                if spec != "-":
+                    for item in spec.split(","):
+                        i, v = item.split(":")
+                        t[int(i)] = int(v, 16)
+                return t
+            scales, codes = table(sc, 2), table(by, 16)
+            v1s = scales if v1sc == "=" else table(v1sc, 2)
+            v1c = codes if v1by == "=" else table(v1by, 16)
+            out.append((ident, x, rsv, scales, codes, v1s, v1c))
+    return out
+
+
+def test_w4a4_quant_worked_examples(golden_dir):
+    ex = _w4a4_examples(golden_dir)
+    assert len(ex) >= 5
+    for ident, x, rs, scales, codes, v1s, v1c in ex:
+        c, s, r = oracle.act_quant_w4a4(x[None, :])
+        assert r[0] == rs, (ident, r[0], rs)
+        assert np.array_equal(s[0], scales), (ident, s[0], scales)
+        assert np.array_equal(c[0], codes), (ident, [hex(v) for v in c[0]])
+        c1, s1 = oracle.act_quant_w4a4_v1(x[None, :])
+        assert np.array_equal(s1[0], v1s), (ident, s1[0], v1s)
+        assert np.array_equal(c1[0], v1c), (ident, [hex(v) for v in c1[0]])
+
+
+def test_e2m1_encode_thresholds_and_ties(golden_dir):
+    """Midpoints of the E2M1 grid (values from the golden grid file): the tie goes to the
+    even code, one f32 ulp either side goes to the nearer neighbour; above 6 saturates."""
+    grid = golden_e2m1(golden_dir)[:8]
+    for c in range(7):
+        mid = np.float32((grid[c] + grid[c + 1]) / 2)
+        even = c if c % 2 == 0 else c + 1
+        assert oracle.e2m1_encode([mid])[0] == even, (c, mid)
+        assert oracle.e2m1_encode([np.nextafter(mid, np.float32(0))])[0] == c
+        assert oracle.e2m1_encode([np.nextafter(mid, np.float32(10))])[0] == c + 1
+        assert oracle.e2m1_encode([-mid])[0] == even | 8
+    assert oracle.e2m1_encode([6.0, 6.5, 100.0, 3e38])[:].tolist() == [7, 7, 7, 7]
+    assert oracle.e2m1_encode([-0.0, -1e-30, 0.0])[:].tolist() == [8, 8, 0]
+    # brute force on random values: nearest grid value, ties cannot occur off the midpoints
+    v = np.random.default_rng(3).uniform(-8, 8, 4000).astype(np.float32)
+    got = oracle.e2m1_encode(v)
+    mag = np.abs(v.astype(np.float64))
+    want = np.argmin(np.abs(mag[:, None] - grid[None, :]), axis=1)
+    assert np.array_equal(got & 7, want)
+    assert np.array_equal(got >> 3, (v < 0).astype(np.uint8))
+
+
+def _w4a4_rows(rng, rows, k):
+    x = rng.uniform(-1, 1, (rows, k)).astype(np.float32) * np.float32(0.1)
+    x[1] *= np.float32(1e-5)                          # a quiet token
+    x[2, 16:48] = 0.0                                 # two all-zero blocks
+    x[3] = (rng.standard_t(3, k) * 10).astype(np.float32)
+    x[4, ::37] *= 300.0                               # outlier channels
+    x[5] = 0.0                                        # a zero row
+    return x
+
+
+def test_w4a4_quant_block_brute_force_and_invariants(golden_dir):
+    """Each code is the nearest E2M1 point (brute force over the golden grid) to the
+    row-normalised value over its block's micro-scale, both quotients formed in numpy f32;
+    the micro-scale is the e4m3 code nearest max|y|/6 (torch's e4m3 rounding); the block
+    holding the row's amax gets 0x7E and that element a magnitude-6 code."""
+    grid = golden_e2m1(golden_dir)[:8]
+    rng = np.random.default_rng(11)
+    rows, k = 6, 256
+    x = _w4a4_rows(rng, rows, k)
+    codes, scales, rs = oracle.act_quant_w4a4(x)
+    nib = oracle.unpack_nibbles(codes)
+    for r in range(rows):
+        amax = np.max(np.abs(x[r]))
+        assert rs[r] == np.float32(amax) / np.float32(2688.0)
+        if rs[r] == 0:
+            assert not scales[r].any() and not codes[r].any()
+            continue
+        y = x[r] / rs[r]                               # numpy f32 division
+        for j in range(k // 16):
+            yb = y[16 * j:16 * j + 16]
+            m = np.max(np.abs(yb))
+            assert scales[r, j] == torch_encode([m / np.float32(6.0)])[0], (r, j)
+            S = np.float32(torch_e4m3([scales[r, j]])[0])
+            qb = nib[r, 16 * j:16 * j + 16]
+            if S == 0:
+                assert not qb.any()
+                continue
+            t = (yb / S).astype(np.float64)
+            d = np.abs(np.abs(t)[:, None] - grid[None, :])
+            want = np.argmin(d, axis=1)
+            tie = np.sort(d, axis=1)[:, 1] - np.sort(d, axis=1)[:, 0] == 0
+            assert np.array_equal((qb & 7)[~tie], want[~tie]), (r, j)
+        jmax = int(np.argmax(np.abs(x[r]))) // 16
+        assert scales[r, jmax] == 0x7E
+        assert nib[r, int(np.argmax(np.abs(x[r])))] & 7 == 7
+
+
+def _w4a4_weights(rng, n, k):
+    w = rng.integers(0, 256, (n, k // 2), dtype=np.uint8)
+    sc = torch_encode(np.exp2(rng.uniform(-3, 1, (n, k // 16))).astype(np.float32))
+    return w, sc
+
+
+def test_w4a4_gemm_ref_is_dequantised_matmul(golden_dir):
+    """The reference equals a float64 matmul of the dequantised operands, each decoded
+    here from the golden E2M1 grid and torch's e4m3 (not the oracle's decoders)."""
+    table = golden_e2m1(golden_dir)
+    rng = np.random.default_rng(12)
+    g, n, k = 6, 24, 256
+    x = _w4a4_rows(rng, g, k)
+    codes, scales, rs = oracle.act_quant_w4a4(x)
+    w, sc = _w4a4_weights(rng, n, k)
+    s2 = np.float32(5.9945243e-5 * 64)
+    out, absp = oracle.gemm_ref_w4a4(codes, scales, rs, w, sc, s2)
+    xa = _dense_weights(codes, table) * np.repeat(torch_e4m3(scales), 16, axis=1) \
+        * rs.astype(np.float64)[:, None]
+    wd = _dense_weights(w, table) * np.repeat(torch_e4m3(sc), 16, axis=1) * float(s2)
+    want = xa @ wd.T
+    wabs = np.abs(xa) @ np.abs(wd).T
+    assert np.all(np.abs(out - want) <= 1e-12 * wabs)
+    assert np.allclose(absp, wabs, rtol=1e-12, atol=0)
+
+
+def test_w4a4_gemm_ref_exact_rational(golden_dir):
+    table = golden_e2m1(golden_dir)
+    rng = np.random.default_rng(13)
+    g, n, k = 2, 3, 64
+    x = _w4a4_rows(rng, 6, k)[[0, 3]]
+    codes, scales, rs = oracle.act_quant_w4a4(x)
+    w, sc = _w4a4_weights(rng, n, k)
+    s2 = np.float32(1 / 64)
+    out, absp = oracle.gemm_ref_w4a4(codes, scales, rs, w, sc, s2)
+    an = _dense_weights(codes, table)
+    wn = _dense_weights(w, table)
+    for r in range(g):
+        for c in range(n):
+            acc = Fraction(0)
+            ab = Fraction(0)
+            for kk in range(k):
+                p = (Fraction(float(an[r, kk])) * Fraction(float(torch_e4m3([scales[r, kk // 16]])[0]))
+                     * Fraction(float(wn[c, kk])) * Fraction(float(torch_e4m3([sc[c, kk // 16]])[0]))
+                     * Fraction(float(rs[r])) * Fraction(float(s2)))
+                acc += p
+                ab += abs(p)
+            assert abs(out[r, c] - float(acc)) <= k * 2.0 ** -52 * float(ab)
+            assert abs(absp[r, c] - float(ab)) <= k * 2.0 ** -52 * float(ab)
+
+
+def _dense_nvfp4(w, sc, s2, table):
+    return _dense_weights(w, table) * np.repeat(torch_e4m3(sc), 16, axis=1) * float(s2)
+
+
+def test_w4a4_informational_band_and_two_level_gain():
+    """The section's arms on synthetic NVFP4 weights: uniform 0.1-scale activations stay in
+    the informational band (rel < 0.2 against the unquantised activations), and on
+    activations whose tokens span 1e-3..1e3 the two-level quantiser beats the sub-block
+    one per token (the section's hard gate)."""
+    table = np.array([oracle.e2m1_decode(i) for i in range(16)]).reshape(-1)
+    rng = np.random.default_rng(14)
+    n, k = 64, 512
+    w, sc = _w4a4_weights(rng, n, k)
+    s2 = np.float32(1 / 64)
+    wd = _dense_nvfp4(w, sc, s2, table)
+    x = (rng.uniform(-1, 1, (16, k)) * 0.1).astype(np.float32)
+    cpu = x.astype(np.float64) @ wd.T
+    c, s, r = oracle.act_quant_w4a4(x)
+    out, _ = oracle.gemm_ref_w4a4(c, s, r, w, sc, s2)
+    rel = oracle.max_rel(out, cpu)
+    assert 0.0 < rel < 0.2, rel
+    tokens = np.arange(16)
+    dec = np.power(10.0, (tokens % 7) - 3).astype(np.float32)
+    xd = (rng.uniform(-1, 1, (16, k)) * 0.1).astype(np.float32) * dec[:, None]
+    cpu = xd.astype(np.float64) @ wd.T
+    c, s, r = oracle.act_quant_w4a4(xd)
+    two, _ = oracle.gemm_ref_w4a4(c, s, r, w, sc, s2)
+    c1, s1 = oracle.act_quant_w4a4_v1(xd)
+    one, _ = oracle.gemm_ref_w4a4(c1, s1, None, w, sc, s2)
+    rel2, rel1 = oracle.per_token_rel(two, cpu), oracle.per_token_rel(one, cpu)
+    assert rel2 < 0.2 and rel2 < rel1, (rel2, rel1)
+    # the quiet tokens are where V1 fails: their micro-scales clamp and whole rows vanish
+    assert rel1 > 0.5
+
+
+def test_per_token_rel_closed_form():
+    ref = np.array([[1.0, -2.0], [0.0, 0.0], [10.0, 5.0]])
+    y = np.array([[1.5, -2.0], [3.0, 0.0], [10.0, 4.0]])
+    assert oracle.per_token_rel(y, ref) == 0.25
