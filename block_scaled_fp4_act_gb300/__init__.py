@@ -86,6 +86,20 @@ def lib():
         L.fp4_gemm_mirror.restype = i32
         L.fp4_swiglu_quant.argtypes = [P, P, i64, f32, i64, i64, P, P, P, P]
         L.fp4_swiglu_quant.restype = i32
+        L.act_quant_w4a4.argtypes = [P, P, P, P, i64, i64, P]
+        L.act_quant_w4a4.restype = i32
+        L.fp4_w4a4_workspace_size.argtypes = [i64, i64, i64]
+        L.fp4_w4a4_workspace_size.restype = sz
+        L.fp4_grouped_expert_gemm_w4a4.argtypes = [P, i64, P, P, i32, i64, P, P, P, P, i64,
+                                                   i64, P, sz, P]
+        L.fp4_grouped_expert_gemm_w4a4.restype = i32
+        L.fp4_w4a4_quantize.argtypes = [P, i64, P, i64, i64, P, sz, P]
+        L.fp4_w4a4_quantize.restype = i32
+        L.fp4_w4a4_gemm_quantized.argtypes = [P, sz, i64, P, P, i32, i64, P, P, P, P, i64, i64,
+                                              P]
+        L.fp4_w4a4_gemm_quantized.restype = i32
+        L.fp4_w4a4_error_ops.argtypes = [i64]
+        L.fp4_w4a4_error_ops.restype = ctypes.c_double
         L.fp4_gemm_path.argtypes = [i64, i32, i64, i64, i32, i32]
         L.fp4_gemm_path.restype = i32
         L.fp4_error_ops.argtypes = [i32, i32, i64]
@@ -429,6 +443,111 @@ def fp4_moe_combine(out, pair_rows, weights, y=None, stream=None):
     _check(lib().fp4_moe_combine(_ptr(out), P, _ptr(pair_rows), _ptr(weights), T, int(topk), n,
                                  _ptr(y), _stream(stream)), "fp4_moe_combine")
     return y
+
+
+# --------------------------------------------------------------------------- W4A4 variant
+
+def act_quant_w4a4(x, codes=None, scales=None, rowscale=None, stream=None):
+    """Two-level W4A4 quantisation: x [rows, k] f32 -> (codes [rows, k/2] u8 nibble pairs,
+    scales [rows, k/16] u8 e4m3, rowscale [rows] f32)."""
+    import torch
+    rows, k = x.shape
+    _need(x, torch.float32, None, "x")
+    if codes is None:
+        codes = torch.empty((rows, k // 2), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((rows, k // 16), dtype=torch.uint8, device=x.device)
+    if rowscale is None:
+        rowscale = torch.empty((rows,), dtype=torch.float32, device=x.device)
+    _need(codes, torch.uint8, (rows, k // 2), "codes")
+    _need(scales, torch.uint8, (rows, k // 16), "scales")
+    _need(rowscale, torch.float32, (rows,), "rowscale")
+    _check(lib().act_quant_w4a4(_ptr(x), _ptr(codes), _ptr(scales), _ptr(rowscale), rows, k,
+                                _stream(stream)), "act_quant_w4a4")
+    return codes, scales, rowscale
+
+
+def fp4_w4a4_workspace_size(num_tokens, total_rows, k):
+    return int(lib().fp4_w4a4_workspace_size(int(num_tokens), int(total_rows), int(k)))
+
+
+def w4a4_workspace_for(num_tokens, total_rows, k, device=None):
+    """A uint8 CUDA tensor sized for the W4A4 grouped calls of this shape."""
+    import torch
+    b = fp4_w4a4_workspace_size(num_tokens, total_rows, k)
+    return torch.empty((max(b, 1),), dtype=torch.uint8, device=device or "cuda")
+
+
+def fp4_grouped_expert_gemm_w4a4(x, row_ids, offsets, w, wscale, scale2, out=None,
+                                 workspace=None, stream=None):
+    """All experts of one NVFP4 projection with W4A4 activations: x [T,k] f32, row_ids [P]
+    int32 or None, offsets [E+1] int32, w [E,n,k/2] u8, wscale [E,n,k/16] u8, scale2 [E] f32
+    -> out [P,n] f32."""
+    import torch
+    T, k = x.shape
+    E, n = w.shape[0], w.shape[1]
+    P = row_ids.shape[0] if row_ids is not None else T
+    _need(x, torch.float32, None, "x")
+    if row_ids is not None:
+        _need(row_ids, torch.int32, (P,), "row_ids")
+    _need(offsets, torch.int32, (E + 1,), "offsets")
+    _need(w, torch.uint8, (E, n, k // 2), "w")
+    _need(wscale, torch.uint8, (E, n, k // 16), "wscale")
+    _need(scale2, torch.float32, (E,), "scale2")
+    if out is None:
+        out = torch.empty((P, n), dtype=torch.float32, device=x.device)
+    _need(out, torch.float32, (P, n), "out")
+    if workspace is None:
+        workspace = w4a4_workspace_for(T, P, k, x.device)
+    _need(workspace, torch.uint8, None, "workspace")
+    _check(lib().fp4_grouped_expert_gemm_w4a4(_ptr(x), T, _ptr(row_ids), _ptr(offsets), E, P,
+                                              _ptr(w), _ptr(wscale), _ptr(scale2), _ptr(out), n,
+                                              k, _ptr(workspace), workspace.numel(),
+                                              _stream(stream)),
+           "fp4_grouped_expert_gemm_w4a4")
+    return out
+
+
+def fp4_w4a4_quantize(x, row_ids, total_rows, workspace, stream=None):
+    """The W4A4 quantise pass into `workspace` (see fp4_grouped_expert_gemm_w4a4)."""
+    import torch
+    T, k = x.shape
+    _need(x, torch.float32, None, "x")
+    if row_ids is not None:
+        _need(row_ids, torch.int32, (total_rows,), "row_ids")
+    _need(workspace, torch.uint8, None, "workspace")
+    _check(lib().fp4_w4a4_quantize(_ptr(x), T, _ptr(row_ids), int(total_rows), k,
+                                   _ptr(workspace), workspace.numel(), _stream(stream)),
+           "fp4_w4a4_quantize")
+    return workspace
+
+
+def fp4_w4a4_gemm_quantized(workspace, num_tokens, row_ids, offsets, w, wscale, scale2, out,
+                            stream=None):
+    """The W4A4 GEMM from a workspace fp4_w4a4_quantize filled for the same tokens, row
+    ids, routed rows and k -> out [P,n] f32 (caller-owned)."""
+    import torch
+    E, n = w.shape[0], w.shape[1]
+    k = w.shape[2] * 2
+    P = out.shape[0]
+    if row_ids is not None:
+        _need(row_ids, torch.int32, (P,), "row_ids")
+    _need(workspace, torch.uint8, None, "workspace")
+    _need(offsets, torch.int32, (E + 1,), "offsets")
+    _need(w, torch.uint8, (E, n, k // 2), "w")
+    _need(wscale, torch.uint8, (E, n, k // 16), "wscale")
+    _need(scale2, torch.float32, (E,), "scale2")
+    _need(out, torch.float32, (P, n), "out")
+    _check(lib().fp4_w4a4_gemm_quantized(_ptr(workspace), workspace.numel(), int(num_tokens),
+                                         _ptr(row_ids), _ptr(offsets), E, P, _ptr(w),
+                                         _ptr(wscale), _ptr(scale2), _ptr(out), n, k,
+                                         _stream(stream)),
+           "fp4_w4a4_gemm_quantized")
+    return out
+
+
+def fp4_w4a4_error_ops(k):
+    return float(lib().fp4_w4a4_error_ops(int(k)))
 
 
 def fp4_gemm_path(total_rows, num_experts, n, k, recipe, have_workspace=True):

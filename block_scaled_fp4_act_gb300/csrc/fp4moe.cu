@@ -527,6 +527,150 @@ int fp4_moe_combine(const float *out, int64_t total_rows, const int32_t *pair_ro
                                      err, (cudaStream_t)stream));
 }
 
+// ------------------------------------------------------------------ W4A4 variant
+
+int act_quant_w4a4(const float *x, uint8_t *codes, uint8_t *scales, float *rowscale, int64_t rows,
+                   int64_t k, void *stream)
+{
+    if (rows < 0 || k < 0)
+        return FP4_ERR_ARG;
+    if (k == 0 || k % 16 != 0 || k > (1 << 20) || rows > ((int64_t)1 << 31))
+        return FP4_ERR_SHAPE;
+    if (rows == 0)
+        return FP4_OK;
+    if (!x || !codes || !scales || !rowscale)
+        return FP4_ERR_ARG;
+    if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(rowscale))
+        return FP4_ERR_ALIGN;
+    unsigned *err = device_error_word();
+    if (!err)
+        return record(cudaErrorInvalidDevice);
+    return record(launch_act_quant_w4a4(x, nullptr, rows, rows, k, codes, scales, rowscale, err,
+                                        (cudaStream_t)stream));
+}
+
+// Shape checks of the W4A4 calls (k a multiple of 256: the GEMM's stage).
+static int check_w4a4_shape(int64_t num_tokens, bool have_row_ids, int64_t total_rows,
+                            int64_t n, int64_t k)
+{
+    if (num_tokens < 0 || total_rows < 0 || n < 0 || k < 0)
+        return FP4_ERR_ARG;
+    if (k < 256 || k % 256 != 0 || n == 0 || k > (1 << 20) || n > (1 << 24) ||
+        total_rows > ((int64_t)1 << 31))
+        return FP4_ERR_SHAPE;
+    if (!have_row_ids && num_tokens < total_rows)
+        return FP4_ERR_SHAPE;
+    return FP4_OK;
+}
+
+size_t fp4_w4a4_workspace_size(int64_t num_tokens, int64_t total_rows, int64_t k)
+{
+    if (check_w4a4_shape(num_tokens, true, total_rows, 1, k) != FP4_OK)
+        return 0;
+    return w4a4_workspace_bytes(num_tokens, total_rows, k);
+}
+
+int fp4_w4a4_quantize(const float *x, int64_t num_tokens, const int32_t *row_ids,
+                      int64_t total_rows, int64_t k, void *workspace, size_t workspace_bytes,
+                      void *stream)
+{
+    int st = check_w4a4_shape(num_tokens, row_ids != nullptr, total_rows, 1, k);
+    if (st != FP4_OK)
+        return st;
+    if (total_rows == 0)
+        return FP4_OK;
+    if (!x)
+        return FP4_ERR_ARG;
+    if (!workspace || workspace_bytes < w4a4_workspace_bytes(num_tokens, total_rows, k))
+        return FP4_ERR_WORKSPACE;
+    if (!aligned16(x))
+        return FP4_ERR_ALIGN;
+    GroupedProblem p{};
+    p.x = x;
+    p.T = num_tokens;
+    p.row_ids = row_ids;
+    p.E = 1;
+    p.P = total_rows;
+    p.recipe = FP4_NVFP4;
+    p.n = 1;
+    p.k = (int)k;
+    p.err = device_error_word();
+    if (!p.err)
+        return record(cudaErrorInvalidDevice);
+    return record(launch_w4a4_quantize(p, workspace, (cudaStream_t)stream));
+}
+
+int fp4_w4a4_gemm_quantized(const void *workspace, size_t workspace_bytes, int64_t num_tokens,
+                            const int32_t *row_ids, const int32_t *offsets, int num_experts,
+                            int64_t total_rows, const uint8_t *w, const uint8_t *wscale,
+                            const float *scale2, float *out, int64_t n, int64_t k, void *stream)
+{
+    if (num_experts < 1 || num_experts > 65535)
+        return FP4_ERR_ARG;
+    int st = check_w4a4_shape(num_tokens, row_ids != nullptr, total_rows, n, k);
+    if (st != FP4_OK)
+        return st;
+    if (!w4a4_supported(n, k, num_experts))
+        return FP4_ERR_SHAPE;
+    if (total_rows == 0)
+        return FP4_OK;
+    if (!offsets || !w || !wscale || !scale2 || !out)
+        return FP4_ERR_ARG;
+    if (!workspace || workspace_bytes < w4a4_workspace_bytes(num_tokens, total_rows, k))
+        return FP4_ERR_WORKSPACE;
+    if (!aligned16(w) || !aligned16(wscale) || !aligned16(out))
+        return FP4_ERR_ALIGN;
+    GroupedProblem p{};
+    p.T = num_tokens;
+    p.row_ids = row_ids;
+    p.offsets = offsets;
+    p.E = num_experts;
+    p.P = total_rows;
+    p.w = w;
+    p.sc = wscale;
+    p.scale2 = scale2;
+    p.recipe = FP4_NVFP4;
+    p.out = out;
+    p.n = (int)n;
+    p.k = (int)k;
+    p.err = device_error_word();
+    if (!p.err)
+        return record(cudaErrorInvalidDevice);
+    return record(launch_w4a4_gemm(p, workspace, (cudaStream_t)stream));
+}
+
+int fp4_grouped_expert_gemm_w4a4(const float *x, int64_t num_tokens, const int32_t *row_ids,
+                                 const int32_t *offsets, int num_experts, int64_t total_rows,
+                                 const uint8_t *w, const uint8_t *wscale, const float *scale2,
+                                 float *out, int64_t n, int64_t k, void *workspace,
+                                 size_t workspace_bytes, void *stream)
+{
+    if (num_experts < 1 || num_experts > 65535)
+        return FP4_ERR_ARG;
+    int st = check_w4a4_shape(num_tokens, row_ids != nullptr, total_rows, n, k);
+    if (st != FP4_OK)
+        return st;
+    if (!w4a4_supported(n, k, num_experts))
+        return FP4_ERR_SHAPE;
+    if (total_rows == 0)
+        return FP4_OK;
+    if (!x)
+        return FP4_ERR_ARG;
+    st = fp4_w4a4_quantize(x, num_tokens, row_ids, total_rows, k, workspace, workspace_bytes,
+                           stream);
+    if (st != FP4_OK)
+        return st;
+    return fp4_w4a4_gemm_quantized(workspace, workspace_bytes, num_tokens, row_ids, offsets,
+                                   num_experts, total_rows, w, wscale, scale2, out, n, k, stream);
+}
+
+double fp4_w4a4_error_ops(int64_t k)
+{
+    // the k/16 model of the other tensor-core paths (one rounding per 16-group of the f32
+    // accumulation) plus the two epilogue multiplies (r, scale2) and one
+    return (double)(k / 16) + 3.0;
+}
+
 int fp4_gemm_path(int64_t total_rows, int num_experts, int64_t n, int64_t k, int recipe,
                   int have_workspace)
 {

@@ -56,6 +56,18 @@ cudaError_t launch_mx_quantize(const GroupedProblem &p, void *workspace, cudaStr
 cudaError_t launch_mx_gemm(const GroupedProblem &p, const void *workspace, cudaStream_t s,
                            const SwigluOut *sw = nullptr);
 
+// The W4A4 variant (gemm_w4a4.cu): two-level E2M1 activations against NVFP4 weights on
+// the block-scaled 4-bit MMA. w4a4_supported: the shapes the GEMM takes (k % 256 == 0, at
+// most 1024 experts); its weight and scale bases must also be 16-byte aligned.
+// launch_act_quant_w4a4 quantises S source rows (x[rid[s]] or x[s]).
+size_t w4a4_workspace_bytes(int64_t num_tokens, int64_t total_rows, int64_t k);
+bool w4a4_supported(int64_t n, int64_t k, int E);
+cudaError_t launch_act_quant_w4a4(const float *x, const int32_t *rid, int64_t T, int64_t S,
+                                  int64_t k, uint8_t *codes, uint8_t *scales, float *rowscale,
+                                  unsigned *err, cudaStream_t s);
+cudaError_t launch_w4a4_quantize(const GroupedProblem &p, void *workspace, cudaStream_t s);
+cudaError_t launch_w4a4_gemm(const GroupedProblem &p, const void *workspace, cudaStream_t s);
+
 // The bounded-wait limit (clock64 cycles) for the next tensor-core GEMM launch on this host
 // thread. Sets *stall to 1 and clears the request if fp4_test_stall_next_gemm asked for a
 // stalled launch; otherwise returns the normal limit and leaves *stall alone.

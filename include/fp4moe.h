@@ -311,9 +311,88 @@ int fp4_moe_combine(const float *out, int64_t total_rows, const int32_t *pair_ro
                     const float *weights, int64_t num_tokens, int topk, int64_t n, float *y,
                     void *stream);
 
+/*
+ * ---------------------------------------------------------------- W4A4 NVFP4 variant
+ * E2M1 (4-bit) activations against NVFP4 weights (memra-engine 0.71.0,
+ * src/bin/kernel_check.rs, the NVFP4 W4A4 MMQ GEMM section): a different numeric class
+ * from the calls above (the activations lose far more than e4m3 codes do; the section
+ * treats rel ~ 0.1 against the unquantised activations as normal). Two-level scaling, in
+ * the reading this library takes (the page names the two levels, not the formulas):
+ *   r = amax_row / 2688 (f32; 2688 = 6 * 448)      the per-token row scale
+ *   y = x / r                                       (f32)
+ *   s = e4m3 nearest to (max|y| over 16 values) / 6 the micro-scale, ties to the even code
+ *   code = E2M1 nearest to y / S (S = value of s)   ties to the even code, |.| >= 6 -> 6,
+ *                                                   sign kept; all zero where S = 0
+ * A zero row has r = 0 and zero codes and scales. The GEMM then computes, on the
+ * block-scaled 4-bit tensor cores (one e4m3 scale per 16 k on each operand, f32
+ * accumulation),
+ *   out[p][c] = (sum_k E2M1(a) S_a * E2M1(w) S_w) * r_p * scale2[e]
+ * with every product exact; error model fp4_w4a4_error_ops(k) against the f64 sum over the
+ * dequantised operands. The weight scale bytes must be non-negative e4m3 (sign bit clear:
+ * the MMA reads them unsigned); NVFP4 scales are.
+ *
+ * act_quant_w4a4 -- the quantisation alone.
+ *   x        [rows, k] f32 in; k a positive multiple of 16
+ *   codes    [rows, k/2] out: E2M1 nibble pairs (low nibble = even k, as the weights)
+ *   scales   [rows, k/16] out: micro-scale e4m3 bytes
+ *   rowscale [rows] f32 out: r
+ * All four pointers 16-byte aligned device memory owned by the caller. Bit-exact with the
+ * oracle. rows == 0 is a no-op.
+ */
+int act_quant_w4a4(const float *x, uint8_t *codes, uint8_t *scales, float *rowscale, int64_t rows,
+                   int64_t k, void *stream);
+
+/* Workspace bytes the W4A4 grouped calls need (0 for shapes they do not take):
+ * 1024 + R(P k/2) + R(P k/16) + R(4 P), plus R(T k/2) + R(T k/16) + R(4 T) when
+ * num_tokens T < total_rows P (R rounds up to a multiple of 1024). */
+size_t fp4_w4a4_workspace_size(int64_t num_tokens, int64_t total_rows, int64_t k);
+
+/*
+ * fp4_grouped_expert_gemm_w4a4 -- all experts of one NVFP4 projection with W4A4
+ * activations, in one call (routing as fp4_grouped_expert_gemm: routed row p reads
+ * x[row_ids[p]], or x[p] without row ids, and belongs to the expert e with
+ * offsets[e] <= p < offsets[e+1]).
+ *   x, num_tokens, row_ids, offsets, num_experts, total_rows: as fp4_grouped_expert_gemm
+ *   w        [num_experts, n, k/2] nibble pairs, 16-byte aligned
+ *   wscale   [num_experts, n, k/16] e4m3 bytes (non-negative), 16-byte aligned
+ *   scale2   [num_experts] f32 (device)
+ *   out      [total_rows, n] f32
+ *   workspace at least fp4_w4a4_workspace_size(num_tokens, total_rows, k) bytes
+ * k must be a multiple of 256 and num_experts at most 1024 (else FP4_ERR_SHAPE). When row
+ * ids repeat tokens (num_tokens < total_rows) each token row is quantised once and copied
+ * to its routed rows. Offsets or row ids that fail the device checks set
+ * fp4_get_device_error bits (bad row ids give zero rows; bad offsets skip the call's rows).
+ * Always the tensor-core kernel, at any number of rows per expert.
+ */
+int fp4_grouped_expert_gemm_w4a4(const float *x, int64_t num_tokens, const int32_t *row_ids,
+                                 const int32_t *offsets, int num_experts, int64_t total_rows,
+                                 const uint8_t *w, const uint8_t *wscale, const float *scale2,
+                                 float *out, int64_t n, int64_t k, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+
+/* fp4_grouped_expert_gemm_w4a4 in its two halves (the quantise pass into the workspace,
+ * then the GEMM that only reads it), for callers that time them apart or run several
+ * projections over one quantised input. Arguments as fp4_grouped_expert_gemm_w4a4; the
+ * workspace of fp4_w4a4_gemm_quantized must have been filled by fp4_w4a4_quantize on the
+ * same stream for the same num_tokens, row ids, total_rows and k. */
+int fp4_w4a4_quantize(const float *x, int64_t num_tokens, const int32_t *row_ids,
+                      int64_t total_rows, int64_t k, void *workspace, size_t workspace_bytes,
+                      void *stream);
+int fp4_w4a4_gemm_quantized(const void *workspace, size_t workspace_bytes, int64_t num_tokens,
+                            const int32_t *row_ids, const int32_t *offsets, int num_experts,
+                            int64_t total_rows, const uint8_t *w, const uint8_t *wscale,
+                            const float *scale2, float *out, int64_t n, int64_t k, void *stream);
+
+/* n_ops of |out - f64 reference over the dequantised operands| <= n_ops 2^-24 sum|p| for
+ * the W4A4 GEMM: k/16 + 3 (one rounding per 16-group of the f32 accumulation, as the other
+ * tensor-core paths, plus the r and scale2 multiplies, plus one). Where r is so small that
+ * those multiplies round in the f32 subnormal range (rows of subnormal inputs), each adds
+ * up to 2^-150 absolute (gradual underflow): 2^-149 on top of the bound. */
+double fp4_w4a4_error_ops(int64_t k);
+
 /* Which path a grouped call of this shape takes (never FP4_PATH_AUTO): the tensor-core
  * path when a workspace is given, the shape is one it supports and the routed rows
- * average at least 8 per expert; the no-workspace path otherwise. */
+ * average at least 9 per expert; the no-workspace path otherwise. */
 int fp4_gemm_path(int64_t total_rows, int num_experts, int64_t n, int64_t k, int recipe,
                   int have_workspace);
 

@@ -387,15 +387,17 @@ def moe_combine(out, pair_rows, weights):
 U32 = 2.0 ** -24
 
 
-def within_bound(gpu, ref, absp, n_ops):
-    """Per-output check of the stated f32 model |gpu - ref| <= n_ops * 2^-24 * absp.
+def within_bound(gpu, ref, absp, n_ops, abs_floor=0.0):
+    """Per-output check of the stated f32 model |gpu - ref| <= n_ops * 2^-24 * absp
+    (+ abs_floor: the absolute error of roundings that land in the f32 subnormal range,
+    2^-150 each under gradual underflow; 0 where no result can be subnormal).
 
     Returns (ok, worst err/bound ratio, index of the worst output)."""
     gpu = np.asarray(gpu, dtype=np.float64).reshape(-1)
     ref = np.asarray(ref, dtype=np.float64).reshape(-1)
     absp = np.asarray(absp, dtype=np.float64).reshape(-1)
     err = np.abs(gpu - ref)
-    bound = n_ops * U32 * absp
+    bound = n_ops * U32 * absp + abs_floor
     ok = bool(np.all(err <= bound))
     with np.errstate(divide="ignore", invalid="ignore"):
         ratio = np.where(bound > 0, err / np.where(bound > 0, bound, 1.0),

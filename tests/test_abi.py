@@ -198,3 +198,48 @@ def test_path_choice_by_shape(lib):
     finally:
         fp4.fp4_force_path(fp4.PATH_AUTO)
     assert fp4.fp4_gemm_path(64, 64, 3072, 4096, fp4.NVFP4, True) == fp4.PATH_STREAM
+
+
+def test_w4a4_host_side_checks(lib):
+    V = ctypes.c_void_p
+    a16 = V(0x10000)           # never dereferenced: every call below fails its checks first
+    odd = V(0x10004)
+    Q = lib.act_quant_w4a4     # (x, codes, scales, rowscale, rows, k, stream)
+    assert Q(a16, a16, a16, a16, 4, 24, None) == fp4.FP4_ERR_SHAPE       # k % 16
+    assert Q(a16, a16, a16, a16, -1, 32, None) == fp4.FP4_ERR_ARG
+    assert Q(None, a16, a16, a16, 4, 32, None) == fp4.FP4_ERR_ARG
+    assert Q(a16, a16, a16, None, 4, 32, None) == fp4.FP4_ERR_ARG
+    assert Q(a16, a16, odd, a16, 4, 32, None) == fp4.FP4_ERR_ALIGN
+    assert Q(None, None, None, None, 0, 32, None) == fp4.FP4_OK           # empty: no-op
+    # workspace size: 1024 + R(P k/2) + R(P k/16) + R(4P) (+ the token rows when T < P)
+    R = lambda b: (b + 1023) // 1024 * 1024
+    k, P, T = 7168, 32768, 4096
+    assert fp4.fp4_w4a4_workspace_size(T, P, k) == \
+        1024 + R(P * k // 2) + R(P * k // 16) + R(4 * P) + R(T * k // 2) + R(T * k // 16) + R(4 * T)
+    assert fp4.fp4_w4a4_workspace_size(P, P, k) == 1024 + R(P * k // 2) + R(P * k // 16) + R(4 * P)
+    assert fp4.fp4_w4a4_workspace_size(8, 8, 128) == 0                    # k % 256
+    # fp4_grouped_expert_gemm_w4a4(x, T, row_ids, offsets, E, P, w, wscale, scale2, out, n, k,
+    #                              ws, ws_bytes, stream)
+    G = lib.fp4_grouped_expert_gemm_w4a4
+    big = 1 << 40
+    assert G(a16, 8, None, a16, 0, 8, a16, a16, a16, a16, 4, 256, a16, big, None) == \
+        fp4.FP4_ERR_ARG                                                  # zero experts
+    assert G(a16, 8, None, a16, 2, 8, a16, a16, a16, a16, 4, 384, a16, big, None) == \
+        fp4.FP4_ERR_SHAPE                                                # k % 256
+    assert G(a16, 8, None, a16, 1025, 8, a16, a16, a16, a16, 4, 256, a16, big, None) == \
+        fp4.FP4_ERR_SHAPE                                                # > 1024 experts
+    assert G(a16, 4, None, a16, 2, 8, a16, a16, a16, a16, 4, 256, a16, big, None) == \
+        fp4.FP4_ERR_SHAPE                                                # T < P, no row ids
+    assert G(a16, 8, None, a16, 2, 8, a16, a16, a16, a16, 4, 256, None, 0, None) == \
+        fp4.FP4_ERR_WORKSPACE
+    assert G(a16, 8, None, a16, 2, 8, a16, a16, a16, a16, 4, 256, a16, 1024, None) == \
+        fp4.FP4_ERR_WORKSPACE
+    assert G(odd, 8, None, a16, 2, 8, a16, a16, a16, a16, 4, 256, a16, big, None) == \
+        fp4.FP4_ERR_ALIGN
+    assert G(None, 0, None, None, 2, 0, None, None, None, None, 4, 256, None, 0, None) == \
+        fp4.FP4_OK                                                       # empty
+    M = lib.fp4_w4a4_gemm_quantized
+    assert M(a16, big, 8, None, a16, 2, 8, a16, a16, None, a16, 4, 256, None) == fp4.FP4_ERR_ARG
+    assert M(a16, big, 8, None, a16, 2, 8, odd, a16, a16, a16, 4, 256, None) == \
+        fp4.FP4_ERR_ALIGN
+    assert fp4.fp4_w4a4_error_ops(7168) == 7168 // 16 + 3

@@ -850,3 +850,15 @@ def test_per_token_rel_closed_form():
     ref = np.array([[1.0, -2.0], [0.0, 0.0], [10.0, 5.0]])
     y = np.array([[1.5, -2.0], [3.0, 0.0], [10.0, 4.0]])
     assert oracle.per_token_rel(y, ref) == 0.25
+
+
+def test_bound_checker_absolute_floor():
+    """The gradual-underflow term: a one-ulp error in the subnormal range passes with the
+    2^-149 floor and fails without it; an error above the floor still fails."""
+    ref = np.array([2.0 ** -140, 1.0])
+    absp = np.array([2.0 ** -140, 1.0])
+    got = ref + np.array([2.0 ** -149, 0.0])
+    assert not oracle.within_bound(got, ref, absp, 4.0)[0]
+    assert oracle.within_bound(got, ref, absp, 4.0, 2.0 ** -149)[0]
+    assert not oracle.within_bound(ref + np.array([2.0 ** -147, 0.0]), ref, absp, 4.0,
+                                   2.0 ** -149)[0]
