@@ -52,6 +52,8 @@ def parse_args():
                     help="skip the SwiGLU + requantisation line (the step after gate/up)")
     ap.add_argument("--no-routing", action="store_true",
                     help="skip the routing front-end line (router, CSR, combine)")
+    ap.add_argument("--no-w4a4", action="store_true",
+                    help="skip the W4A4 variant (E2M1 activations) on the same workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--experts", type=int, default=0, help="override the workload's expert count")
@@ -181,6 +183,7 @@ KERNEL_SOURCES = {
     "tc_quantize": ["gemm_tc.cu", "common.cuh", "internal.h"],
     "stream_gemm": ["gemm_stream.cu", "common.cuh", "internal.h"],
     "decode_tma": ["gemm_decode.cu", "common.cuh", "internal.h", "tma_host.h"],
+    "w4a4_gemm": ["gemm_w4a4.cu", "common.cuh", "tcgen05.cuh", "internal.h", "tma_host.h"],
 }
 
 # The no-workspace path runs the TMA-fed warp-MMA decode kernel for k a multiple of 512 up
@@ -648,6 +651,11 @@ def run_ours(args, world, rank, local):
     if result_quant is not None:
         result["quantize"] = result_quant
 
+    # the W4A4 variant on the same workload (its own numeric class: E2M1 activations)
+    if args.workload == "c4" and not args.no_w4a4:
+        result["w4a4"] = measure_w4a4(fp4, wl, result["config"]["workload"], peaks, peak_src,
+                                      ms_step)
+
     # decode workload alongside: weight GB/s against HBM, L2 flushed between steps
     if args.workload == "c4" and not args.no_decode:
         wd = synth.decode_c3(device=device)
@@ -783,6 +791,92 @@ def measure_mixed(fp4, synth, device, peaks, peak_src, steps=20):
                        "peak_bf16": bf16, "peak_source": peak_src + " bf16 dense (burst); fp8 = 2x"}
     out["gpu_launches"] = steps * sum(c["launches"] for c in calls)
     del calls, wl
+    torch.cuda.empty_cache()
+    return out
+
+
+def w4a4_gemm_bytes(proj):
+    """Algorithmic bytes of one W4A4 GEMM launch: the touched experts' packed weights and
+    e4m3 scales (+ scale2), the routed rows' packed codes, micro-scales and row scales read
+    once, the f32 output written once."""
+    import torch
+    b = proj.bank
+    touched = int(torch.count_nonzero(torch.diff(proj.routing.offsets)).item())
+    P, k = proj.routing.P, b.k
+    return touched * (b.n * (k // 2) + b.n * (k // 16) + 4) + P * (k // 2 + k // 16 + 4) + \
+        P * b.n * 4
+
+
+def w4a4_quant_bytes(proj):
+    """Algorithmic bytes of the W4A4 quantise phase: each token row read once (f32), each
+    routed row's codes, micro-scales and row scale written once."""
+    T, k = proj.x.shape
+    P = proj.routing.P
+    return T * k * 4 + P * (k // 2 + k // 16 + 4)
+
+
+def measure_w4a4(fp4, wl, workload_name, peaks, peak_src, w4a8_ms, steps=20):
+    """The W4A4 NVFP4 variant (two-level E2M1 activations on the block-scaled 4-bit MMA) on
+    the same projections: quantise phase and GEMM timed apart (CUDA events on the current
+    stream), inputs larger than L2. The GEMM streams the expert weights once per tile
+    column, so its roofline is HBM; its tensor rate is shown against the FP4 dense rate
+    (6x the measured bf16 peak, the nominal FP4/bf16 ratio of this GPU)."""
+    import torch
+    calls = []
+    for proj in wl.projections:
+        T, k = proj.x.shape
+        P = proj.routing.P
+        ws = fp4.w4a4_workspace_for(T, P, k, proj.x.device)
+        out = torch.empty(P, proj.bank.n, device=proj.x.device)
+        rid = proj.routing.row_ids if proj.row_ids_used else None
+
+        def quantize(proj=proj, ws=ws, rid=rid):
+            fp4.fp4_w4a4_quantize(proj.x, rid, proj.routing.P, ws)
+
+        def gemm(proj=proj, ws=ws, out=out, rid=rid):
+            fp4.fp4_w4a4_gemm_quantized(ws, proj.x.shape[0], rid, proj.routing.offsets,
+                                        proj.bank.w, proj.bank.sc, proj.bank.scale2, out)
+        repeats = rid is not None and T < P
+        calls.append({"proj": proj, "phases": [("quantize", quantize), ("gemm", gemm)],
+                      "launches": 3 if repeats else 2, "ws": ws, "out": out})
+    for _ in range(3):
+        for c in calls:
+            for _, fn in c["phases"]:
+                fn()
+    torch.cuda.synchronize()
+    _, per, phases = time_steps(calls, steps)
+    assert fp4.fp4_get_device_error() == 0
+    ms = sum(sum(d) / len(d) for d in per)
+    gemm_ms = sum(sum(ph["gemm"]) / len(ph["gemm"]) for ph in phases)
+    quant_ms = sum(sum(ph["quantize"]) / len(ph["quantize"]) for ph in phases)
+    flops = sum(proj_flops(c["proj"]) for c in calls)
+    gbytes = sum(w4a4_gemm_bytes(c["proj"]) for c in calls)
+    qbytes = sum(w4a4_quant_bytes(c["proj"]) for c in calls)
+    hbm = peaks["hbm_gbs"]
+    fp4_peak = 6 * peaks["bf16_tflops"]
+    g_gbs = gbytes / (gemm_ms * 1e-3) / 1e9
+    g_tf = flops / (gemm_ms * 1e-3) / 1e12
+    q_gbs = qbytes / (quant_ms * 1e-3) / 1e9
+    out = {"what": "W4A4 NVFP4 variant: E2M1 activations with a per-token row scale and an "
+                   "e4m3 micro-scale per 16 values (kernel_check.rs, NVFP4 W4A4 MMQ GEMM "
+                   "section), GEMM on tcgen05 kind::mxf4nvf4 with 4X ue4m3 scales",
+           "workload": workload_name, "steps": steps,
+           "ms_per_step": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+           "speedup_vs_w4a8_step": round(w4a8_ms / ms, 3),
+           "per_call_ms": [round(sum(d) / len(d), 4) for d in per],
+           "gemm": {"kernel": "w4a4_gemm_kernel", "ms_per_step": round(gemm_ms, 4),
+                    "tflops": round(g_tf, 1), "frac_of_fp4": round(g_tf / fp4_peak, 4),
+                    "fp4_peak": round(fp4_peak, 1),
+                    "roofline": {"bound": "hbm", "achieved": round(g_gbs, 1), "peak": hbm,
+                                 "unit": "GB/s", "frac": round(g_gbs / hbm, 4),
+                                 "bytes_per_step": gbytes,
+                                 "traffic": ncu_traffic("w4a4_gemm/c4"),
+                                 "peak_source": peak_src + " HBM copy bandwidth"}},
+           "quantize": {"ms_per_step": round(quant_ms, 4), "bytes_per_step": qbytes,
+                        "roofline": {"bound": "hbm", "achieved": round(q_gbs, 1), "peak": hbm,
+                                     "unit": "GB/s", "frac": round(q_gbs / hbm, 4)}},
+           "gpu_launches": steps * sum(c["launches"] for c in calls)}
+    del calls
     torch.cuda.empty_cache()
     return out
 

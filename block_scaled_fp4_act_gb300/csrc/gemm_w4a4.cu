@@ -31,6 +31,11 @@
 //   8 - 15   scale-factor warps (two turns of four, one per lane quarter): read the stage's
 //            scale bytes from shared memory and write the words into a tensor-memory ring
 // Every mbarrier wait is bounded; the abort protocol is the other tensor-core kernels'.
+// Rings (measured on GB300 at the prefill shapes): the weights stream from HBM about 2 us
+// away under load, so the weight ring is the deepest (7 stages, 126 KB; 4 stages were 5%
+// slower); activation slots are 20 KB, the size of the largest box. The GEMM moves its
+// operands as TMA boxes of 16-20 KB; on this GPU a CTA completes about one such box per
+// 270 ns from L2, which with the HBM latency sets the stage rate (~0.4 us per 256 k).
 #include "common.cuh"
 #include "tcgen05.cuh"
 #include "tma_host.h"
@@ -47,7 +52,7 @@ constexpr int BM = 128;
 constexpr int BN = 160;
 constexpr int BK = 256;              // k per stage: four MMAs of K = 64
 constexpr int BKB = BK / 2;          // bytes of one row's stage (packed E2M1)
-constexpr int W_STAGES = 4;          // weight stages: E2M1 box (16 KB) + scale box (2 KB)
+constexpr int W_STAGES = 7;          // weight stages: E2M1 box (16 KB) + scale box (2 KB)
 constexpr int B_STAGES = 4;          // activation code slots (k-block-major)
 constexpr int SB_STAGES = 4;         // activation scale boxes
 constexpr int SF_STAGES = 4;         // scale-factor slots in tensor memory
@@ -58,7 +63,7 @@ constexpr int kWarpB = 0, kWarpMma = 1, kWarpW = 2, kWarpRelay = 3;
 constexpr int A_BYTES = BM * BKB;
 constexpr int SC_BYTES = BM * 16;    // 16 e4m3 bytes (256 k) per weight row
 constexpr int W_BYTES = A_BYTES + SC_BYTES;
-constexpr int B_BYTES = 32 * 8 * BKB;  // one code slot: 32 rows x 8 k-blocks (or 64 x 4, ...)
+constexpr int B_BYTES = BN * BKB;      // one code slot: 32 rows x 4 k-blocks, 64 x 2, 128 or 160 x 1
 constexpr int SB_BYTES = BN * 16;      // one stage's activation scales: 16 bytes per row
 constexpr int OFF_W = B_STAGES * B_BYTES;
 constexpr int OFF_SB = OFF_W + W_STAGES * W_BYTES;
@@ -77,7 +82,9 @@ constexpr int SMEM_BYTES =
     1024 + RING_BYTES + NUM_BARS * 8 + 16 + (kMaxExperts + 1) * 4 + kTileInfo * 4;
 static_assert(B_BYTES % 1024 == 0 && W_BYTES % 1024 == 0 && OFF_W % 1024 == 0, "alignment");
 static_assert(A_BYTES % 1024 == 0 && OFF_SB % 16 == 0 && SB_BYTES % 16 == 0, "alignment");
-static_assert(BN * BKB <= B_BYTES && BN % 16 == 0 && BN <= 8 * 32, "activation box");
+static_assert(BN * BKB <= B_BYTES && 32 * 4 * BKB <= B_BYTES && BN % 16 == 0 && BN <= 8 * 32,
+              "activation box");
+static_assert(BK == 4 * 64, "a stage is the four K = 64 MMAs of mma_stage_nvf4");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(kThreads <= 1024, "block size");
 
@@ -137,7 +144,7 @@ __device__ __forceinline__ int bmap_index(int rows)
     return rows <= 32 ? 0 : rows <= 64 ? 1 : rows <= 128 ? 2 : 3;
 }
 __host__ __device__ constexpr int bmap_rows(int bi) { return bi < 3 ? 32 << bi : BN; }
-__host__ __device__ constexpr int bmap_kblocks(int bi) { return 8 >> bi; }
+__host__ __device__ constexpr int bmap_kblocks(int bi) { return bi < 2 ? 4 >> bi : 1; }
 
 struct CodeMaps {
     CUtensorMap m[4];
@@ -151,16 +158,33 @@ __device__ __forceinline__ uint32_t idesc_nvf4(int n)
     return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_nvf4_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t sfa, uint32_t sfb,
-                                              uint32_t accumulate)
+// One stage from one warp: a single elect.sync, then the elected lane issues the four MMAs
+// (K = 64 each: descriptors advanced by 32 bytes, scale words by their column offsets) and
+// the two commits. (An elect.sync per MMA costs the issuing warp about 100 cycles per MMA;
+// in one block the stage issues at the MMAs' own rate.)
+__device__ __forceinline__ void mma_stage_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t sf0, uint32_t first,
+                                               uint32_t bar_w, uint32_t bar_sf)
 {
     asm volatile("{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
-                 "setp.ne.b32 p, %6, 0;\n\t"
+                 "setp.eq.b32 p, %5, 0;\n\t"
                  "elect.sync r|e, 0xffffffff;\n\t"
                  "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, "
-                 "%2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
-                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+                 "%2, %3, [%4], [%6], p;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %7, "
+                 "%8, %3, [%9], [%10], 1;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %11, "
+                 "%12, %3, [%13], [%14], 1;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %15, "
+                 "%16, %3, [%17], [%18], 1;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%19];\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%20];\n\t"
+                 "}" ::"r"(d_tmem),
+                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sf0), "r"(first), "r"(sf0 + 16u),
+                 "l"(a_desc + 2u), "l"(b_desc + 2u), "r"(sf0 + 4u), "r"(sf0 + 24u),
+                 "l"(a_desc + 4u), "l"(b_desc + 4u), "r"(sf0 + 8u), "r"(sf0 + 32u),
+                 "l"(a_desc + 6u), "l"(b_desc + 6u), "r"(sf0 + 12u), "r"(sf0 + 40u),
+                 "r"(bar_w), "r"(bar_sf)
                  : "memory");
 }
 
@@ -387,12 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t bdesc =
                     bdesc0 + (uint64_t)(bslot * (B_BYTES >> 4) + (uint32_t)j * kb_desc);
                 const uint32_t sf0 = tmem_base + (uint32_t)(kSfCol + sf * kSfSlotCols);
-#pragma unroll
-                for (int kk = 0; kk < BK / 64; ++kk)
-                    mma_nvf4_warp(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
-                                  sf0 + 4u * kk, sf0 + 16u + 8u * kk, (kb | kk) != 0 ? 1u : 0u);
-                mma_commit_warp(wempty(ws));
-                mma_commit_warp(sfempty(sf));
+                mma_stage_nvf4(d_tmem, adesc, bdesc, idesc, sf0, kb == 0 ? 1u : 0u, wempty(ws),
+                               sfempty(sf));
                 ++st;
                 if (j == kbmask || kb == nkb - 1) {
                     mma_commit_warp(bempty(bslot));
