@@ -592,25 +592,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ activation pass
 
-// E2M1 code of t: nearest of 0, 0.5, 1, 1.5, 2, 3, 4, 6 by the midpoints, a tie going to
-// the even code (the comparison is >= where the upper neighbour is even, > where the lower
-// one is), 6 and above saturating to 6; the sign bit copied from t.
-__device__ __forceinline__ uint32_t e2m1_code(float t)
+// Two f32 -> two E2M1 codes in one byte (lo in the low nibble): the hardware conversion
+// rounds to the nearest E2M1 value with ties to the even code, saturates at +-6 and keeps
+// the sign (negative values that round to zero give 0x8), the definition's rounding.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi)
 {
-    const float a = fabsf(t);
-    const uint32_t c = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
-                       (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) +
-                       (uint32_t)(a > 5.0f);
-    return c | ((__float_as_uint(t) >> 28) & 8u);
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+        "cvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    return r;
+}
+
+// The codes of fl(fl(x / r) / S) for two values (the definition's two correctly rounded
+// quotients), from a = x * c with c ~ 1 / (r S): a is within 8 f32 ulps of that quotient
+// (c within 3, the product 1, the two divisions 2), so when a (1 - 2^-20) and a (1 + 2^-20)
+// convert to the same codes, those are the codes of the quotients; otherwise (a value
+// within 2^-20 of a rounding boundary, rarely) the two divisions are done.
+__device__ __forceinline__ uint32_t e2m1x2_scaled(float x0, float x1, float c, float r, float S)
+{
+    const float a0 = x0 * c, a1 = x1 * c;
+    const uint32_t lo = e2m1x2(a0 * (1.0f - 0x1p-20f), a1 * (1.0f - 0x1p-20f));
+    const uint32_t hi = e2m1x2(a0 * (1.0f + 0x1p-20f), a1 * (1.0f + 0x1p-20f));
+    if (lo == hi)
+        return lo;
+    return e2m1x2(__fdiv_rn(__fdiv_rn(x0, r), S), __fdiv_rn(__fdiv_rn(x1, r), S));
 }
 
 constexpr int kQuantThreads = 128;
 
 // Two-level quantisation of source row s (x[rid[s]], or x[s] without row ids), one CTA
 // per row: pass 1 the row amax, pass 2 per 16-block (four consecutive threads, four
-// values each): y = x / r, the micro-scale byte e4m3(max|y| / 6) and the codes. Writes
-// codes[s] (k/2 bytes), scales[s] (k/16 bytes) and rowscale[s]. Bad row ids give a zero
-// row (r = 0) and raise FP4_DEVERR_ROW_ID.
+// values each): the block's max|y| = fl(max|x| / r) (division is monotone, so this is the
+// largest y = fl(x / r)), the micro-scale byte e4m3(max|y| / 6) and the codes of
+// fl(y / S) (e2m1x2_scaled; rows with r below 2^-100, where 1 / (r S) could overflow,
+// divide every value). Writes codes[s] (k/2 bytes), scales[s] (k/16 bytes) and
+// rowscale[s]. Bad row ids give a zero row (r = 0) and raise FP4_DEVERR_ROW_ID.
 __global__ void __launch_bounds__(kQuantThreads) w4a4_quant_kernel(
     const float *__restrict__ x, int64_t T, const int32_t *__restrict__ rid, int64_t S, int k,
     uint8_t *__restrict__ codes, uint8_t *__restrict__ scales, float *__restrict__ rowscale,
@@ -644,24 +663,30 @@ __global__ void __launch_bounds__(kQuantThreads) w4a4_quant_kernel(
             rowscale[s] = r;
         uint16_t *crow = reinterpret_cast<uint16_t *>(codes + s * (int64_t)(k >> 1));
         uint8_t *srow = scales + s * (int64_t)(k >> 4);
+        const bool fast = r >= 0x1p-100f;
+        const float inv_r = fast ? __frcp_rn(r) : 0.0f;
         for (int base = 0; base < chunks; base += kQuantThreads) {
             const int c = base + tid;
             const bool act = c < chunks;  // uniform over each 4-thread block (chunks % 4 == 0)
-            float4 y = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            if (act && r != 0.0f) {
-                const float4 v = __ldg(xr + c);
-                y = make_float4(__fdiv_rn(v.x, r), __fdiv_rn(v.y, r), __fdiv_rn(v.z, r),
-                                __fdiv_rn(v.w, r));
-            }
-            float m = fmaxf(fmaxf(fabsf(y.x), fabsf(y.y)), fmaxf(fabsf(y.z), fabsf(y.w)));
-            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+            float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (act && r != 0.0f)
+                v = __ldg(xr + c);
+            float ax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+            ax = fmaxf(ax, __shfl_xor_sync(0xFFFFFFFFu, ax, 1));
+            ax = fmaxf(ax, __shfl_xor_sync(0xFFFFFFFFu, ax, 2));
+            const float m = r != 0.0f ? __fdiv_rn(ax, r) : 0.0f;
             const uint32_t sbyte = e4m3x2(__fdiv_rn(m, 6.0f), 0.0f) & 0xFFu;
             const float S = e4m3_to_f32(sbyte);
             uint32_t q = 0u;
-            if (S != 0.0f)
-                q = e2m1_code(__fdiv_rn(y.x, S)) | (e2m1_code(__fdiv_rn(y.y, S)) << 4) |
-                    (e2m1_code(__fdiv_rn(y.z, S)) << 8) | (e2m1_code(__fdiv_rn(y.w, S)) << 12);
+            if (S != 0.0f) {
+                if (fast) {
+                    const float cs = inv_r * __frcp_rn(S);
+                    q = e2m1x2_scaled(v.x, v.y, cs, r, S) | (e2m1x2_scaled(v.z, v.w, cs, r, S) << 8);
+                } else {
+                    q = e2m1x2(__fdiv_rn(__fdiv_rn(v.x, r), S), __fdiv_rn(__fdiv_rn(v.y, r), S)) |
+                        (e2m1x2(__fdiv_rn(__fdiv_rn(v.z, r), S), __fdiv_rn(__fdiv_rn(v.w, r), S)) << 8);
+                }
+            }
             if (act) {
                 crow[c] = (uint16_t)q;
                 if ((tid & 3) == 0)
