@@ -74,9 +74,12 @@ constexpr int BK = 64;
 constexpr int W_KS = 4;
 constexpr int W_STAGES = 3;   // weight ring slots (12 k-stages ahead): it streams from HBM
 constexpr int A_STAGES = 4;   // converted weight tiles, in tensor memory
-// Activation slots. A 192-row tile takes a slot per k-stage, so the ring's slot count is
-// its prefetch depth; measured on GB300, 4 slots held 192-row tiles to ~2x the MMA time.
-constexpr int B_STAGES = 5;
+// Activation slots of 48 KB: a 192-row tile takes two k-stages per slot (one TMA copy), a
+// 32-row tile twelve. On GB300 a CTA completes about one TMA copy per ~270 ns whatever its
+// size, so fewer, larger copies pay: three 48 KB slots were 2.9% faster on the prefill
+// projections than five 32 KB slots (which, with 192-row tiles at one k-stage per slot,
+// had been 6% faster than four); two 72 KB or 64 KB slots were slower.
+constexpr int B_STAGES = 3;
 constexpr int kMaxExperts = 1024;
 // Converter warps per TMEM lane quarter; one of them converts each k-stage of the
 // quarter's 32 weight rows, so they take turns over the stages.
@@ -105,10 +108,10 @@ __device__ __forceinline__ int warp_role(int w)
 // elements, even k in the low half), 32 columns per 64-k stage.
 constexpr int kACol = 2 * BN;
 static_assert(kACol + A_STAGES * (BK / 2) <= 512, "tensor memory budget");
-// Activation tiles are loaded k-block-major: one TMA box holds up to 8 k-blocks of a small
-// tile (32 rows x 8, 64 x 4, 128 x 2 k-blocks, or BN rows x 1), so small tiles keep many
+// Activation tiles are loaded k-block-major: one TMA box holds up to 12 k-blocks of a small
+// tile (32 rows x 12, 64 x 6, 128 x 3 k-blocks, or BN rows x 2), so small tiles keep many
 // k-stages in flight in the same ring slots.
-constexpr int B_BYTES = 32 * 8 * BK * 2;  // one ring slot (the largest box: 32 rows x 8 k-blocks)
+constexpr int B_BYTES = 32 * 12 * BK * 2;  // one ring slot: every box class fills it
 constexpr int NIB_BYTES = BM * BK * W_KS / 2;  // 128 rows x 128 bytes, 128-byte swizzle
 constexpr int SC_BYTES = BM * 16;               // 16 scale bytes per row (256 k NVFP4)
 constexpr int W_BYTES = NIB_BYTES + SC_BYTES;
@@ -130,7 +133,7 @@ constexpr int SMEM_BYTES =
     1024 + RING_BYTES + NUM_BARS * 8 + 16 + (kMaxExperts + 1) * 4 + kTileInfo * 4;
 static_assert(B_BYTES % 1024 == 0 && W_BYTES % 1024 == 0 && OFF_W % 1024 == 0,
               "swizzled tiles need 1024-byte alignment");
-static_assert(BN * BK * 2 <= B_BYTES && BN % 16 == 0 && BN <= 256, "activation box");
+static_assert(BN * BK * 2 * 2 <= B_BYTES && BN % 16 == 0 && BN <= 256, "activation box");
 static_assert(kThreads <= 1024, "block size");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
@@ -290,7 +293,10 @@ __device__ __forceinline__ int bmap_index(int rows)
 // Rows and k-blocks of activation box bi.
 __host__ __device__ constexpr int bmap_rows(int bi) { return bi < 3 ? 32 << bi : BN; }
 // k-blocks a slot holds: as many as fit in its 32 KB
-__host__ __device__ constexpr int bmap_kblocks(int bi) { return 8 >> bi; }
+__host__ __device__ constexpr int bmap_kblocks(int bi)
+{
+    return bi == 0 ? 12 : bi == 1 ? 6 : bi == 2 ? 3 : 2;
+}
 
 // SWIGLU: the weight maps have 16-row boxes; each weight slot is filled by eight of them
 // (block b: gate rows when b is even, up rows when odd, 16 h columns from 64 m + 16 (b / 2)),
