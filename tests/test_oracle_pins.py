@@ -862,3 +862,27 @@ def test_bound_checker_absolute_floor():
     assert oracle.within_bound(got, ref, absp, 4.0, 2.0 ** -149)[0]
     assert not oracle.within_bound(ref + np.array([2.0 ** -147, 0.0]), ref, absp, 4.0,
                                    2.0 ** -149)[0]
+
+
+def test_pow2_scale_multiply_equals_divide_every_f32():
+    """fn quant_rows forms the scale as pow2_ceil(amax * f32(1/448)); the plain statement of
+    the method divides by 448. Over every f32 amax from the 1e-4 floor to 3e38 (about 1.18e9
+    values, in chunks) the two give the same power of two, so either reading yields the
+    same scales (and, the codes being x / s, the same codes)."""
+    lo = int(np.array([1e-4], dtype=np.float32).view(np.uint32)[0])
+    hi = int(np.array([3e38], dtype=np.float32).view(np.uint32)[0])
+    inv = np.float32(1.0 / 448.0)
+    d = np.float32(448.0)
+
+    def p2c(t):
+        b = t.view(np.uint32)
+        m = b & np.uint32(0x007FFFFF)
+        e = b & np.uint32(0x7F800000)
+        return np.where(m == 0, b, e + np.uint32(0x00800000))
+
+    step = 1 << 26
+    for start in range(lo, hi + 1, step):
+        bits = np.arange(start, min(start + step, hi + 1), dtype=np.uint32)
+        a = bits.view(np.float32)
+        same = p2c(a * inv) == p2c(a / d)
+        assert same.all(), a[~same][:4]
