@@ -271,3 +271,32 @@ def test_w4a4_stalled_launch_times_out_and_the_next_call_is_correct():
     sub = offsets[:5]
     _check_all(out[:int(sub[-1])], x, row_ids[:int(sub[-1])], sub, w, sc, s2,
                "w4a4 after a stalled launch")
+
+
+def test_grouped_w4a4_expert_limit():
+    """1024 experts (the kernel's limit: its tile prefix lives in shared memory), most empty,
+    a few with rows; 1025 experts are refused on the host."""
+    rng = np.random.default_rng(9)
+    E, n, k, T = 1024, 128, 256, 64
+    sizes = np.zeros(E, dtype=np.int64)
+    hot = rng.choice(E, 40, replace=False)
+    sizes[hot] = rng.integers(1, 9, 40)
+    sizes[E - 1] = 3                                   # the last expert has rows
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    P = int(offsets[-1])
+    row_ids = rng.integers(0, T, P).astype(np.int32)
+    x = _rows(rng, T, k)
+    w = rng.integers(0, 256, (E, n, k // 2), dtype=np.uint8)
+    sc = torch.exp2(torch.empty(E, n, k // 16).uniform_(-3, 1)).to(torch.float8_e4m3fn) \
+        .view(torch.uint8).numpy()
+    s2 = np.full(E, 1 / 64, dtype=np.float32)
+    out = _run(x, row_ids, offsets, w, sc, s2)
+    assert fp4.fp4_get_device_error() == 0
+    _check_all(out, x, row_ids, offsets, w, sc, s2, "w4a4 1024 experts")
+    off = torch.as_tensor(np.concatenate([offsets, [P]]).astype(np.int32)).to(DEV)
+    wd = torch.as_tensor(np.concatenate([w, w[:1]])).to(DEV)
+    scd = torch.as_tensor(np.concatenate([sc, sc[:1]])).to(DEV)
+    with pytest.raises(fp4.Fp4Error, match="FP4_ERR_SHAPE"):
+        fp4.fp4_grouped_expert_gemm_w4a4(torch.as_tensor(x).to(DEV),
+                                         torch.as_tensor(row_ids).to(DEV), off, wd, scd,
+                                         torch.ones(E + 1, device=DEV))
