@@ -181,17 +181,23 @@ def test_grouped_w4a4_bad_row_id_gives_zero_row_and_error_bit():
 
 
 def test_grouped_w4a4_full_prefill_shape_sampled():
-    """The prefill workload's gate/up shape (256 experts, 4096 tokens top-8 Zipf(1.1),
-    [4096, 7168]) in the launch configuration the benchmark times; sampled routed rows,
-    all columns of a weight block, against the oracle."""
+    """The prefill routing (256 experts, 4096 tokens top-8 Zipf(1.1)) on a gate and up bank
+    of the layer body ([2 x 2048, 7168], k as the benchmark's gate/up projection, twice its
+    n), in the launch configuration the benchmark uses; two runs bit-identical; sampled
+    routed rows, the first and last weight block, against the oracle."""
     E, T, topk, n, k = 256, 4096, 8, 4096, 7168
     routing = synth.zipf_topk(T, E, topk, 1234, "cpu")
     gen = torch.Generator().manual_seed(99)
     x = (torch.rand(T, k, generator=gen) * 2 - 1) * 0.1
     bank = synth.make_bank(fp4.NVFP4, E, n, k, 4321, DEV, scale2_value=5.9945243e-5 * 64)
-    out = fp4.fp4_grouped_expert_gemm_w4a4(x.to(DEV), routing.row_ids.to(DEV),
-                                           routing.offsets.to(DEV), bank.w, bank.sc, bank.scale2)
+    call = lambda: fp4.fp4_grouped_expert_gemm_w4a4(x.to(DEV), routing.row_ids.to(DEV),
+                                                    routing.offsets.to(DEV), bank.w, bank.sc,
+                                                    bank.scale2)
+    out = call()
+    again = call()                                   # the same inputs: bit-identical outputs
     torch.cuda.synchronize()
+    assert torch.equal(out, again)
+    del again
     assert fp4.fp4_get_device_error() == 0
     offs = routing.offsets.numpy()
     rng = np.random.default_rng(3)
