@@ -649,6 +649,30 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1)
         pass = local / mt;
         m = local - pass * mt;
     };
+    // Steps through this CTA's items in order from t0, reading the prefix only where the
+    // expert changes (a shared-memory read behind the consumers' operand traffic costs a
+    // few hundred cycles, and the item boundary holds up every consumer warp).
+    struct Walk {
+        int e, pass, m, end;  // end: the first item past expert e
+    };
+    auto walk_start = [&](Walk &w) {
+        item(t0, w.e, w.pass, w.m);
+        w.end = prefix[w.e + 1];
+    };
+    auto walk_next = [&](Walk &w, int t) {
+        if (++w.m == mt) {
+            w.m = 0;
+            ++w.pass;
+        }
+        if (t >= w.end) {
+            do {
+                ++w.e;
+                w.end = prefix[w.e + 1];
+            } while (t >= w.end);
+            w.pass = 0;
+            w.m = 0;
+        }
+    };
 
     if (warp == CW) {
         // ---------------------------------------------------------- producer
@@ -661,10 +685,13 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1)
             int slot = 0, oslot = 0, inflight = 0;  // oslot: the oldest stage still in flight
             uint32_t phase = 0, ophase = 0, issued = 0, parity = 0;
             bool ok = true;
+            Walk wk;
+            if (t0 < t1)
+                walk_start(wk);
             for (int t = t0; t < t1 && ok; ++t) {
-                int e, pass, m;
-                item(t, e, pass, m);
-                const int y = e * n + m * BM;
+                if (t > t0)
+                    walk_next(wk, t);
+                const int y = wk.e * n + wk.m * BM;
                 for (int j = 0; j < nst; ++j) {
                     if (inflight == kInFlight) {
                         if (!mbar_wait(full(oslot), ophase, abort_flag, p.err)) {
@@ -752,9 +779,17 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1)
     int64_t c0 = 0;
     int rows = 0;
     float s2 = 1.0f;
+    bool f16 = false;
+    // the pass's values this lane's output columns 2c, 2c + 1 need, kept in registers
+    bool col_ok[2] = {false, false};
+    float col_rs[2] = {1.0f, 1.0f};
+    Walk wk;
+    if (t0 < t1)
+        walk_start(wk);
     for (int t = t0; t < t1; ++t) {
-        int e, pass, m;
-        item(t, e, pass, m);
+        if (t > t0)
+            walk_next(wk, t);
+        const int e = wk.e, pass = wk.pass, m = wk.m;
         if (e != prev_e || pass != prev_pass) {
             consumer_sync<NT>();  // every consumer is done with the previous pass's rows
             const int64_t r0 = offs[e], r1 = offs[e + 1];
@@ -767,8 +802,14 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1)
             prev_e = e;
             prev_pass = pass;
             ++npass;
+            f16 = GS == 16 && *route_f16 != 0;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int nn = 2 * c + q;
+                col_ok[q] = nn < rows && rowok[nn] != 0;
+                col_rs[q] = col_ok[q] && f16 ? rowscale[nn] : 1.0f;
+            }
         }
-        const bool f16 = GS == 16 && *route_f16 != 0;
         float d[CH][4];
 #pragma unroll
         for (int ch = 0; ch < CH; ++ch)
@@ -839,12 +880,10 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1)
         const int colA = m * BM + rA, colB = m * BM + rB;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-            const int nn = 2 * c + (jj & 1);
+            const int q = jj & 1;
             const int col = (jj < 2) ? colA : colB;
-            if (nn < rows && col < n && rowok[nn]) {
-                const float rs = f16 ? rowscale[nn] : 1.0f;
-                p.out[(c0 + nn) * (int64_t)n + col] = (r[jj] * rs) * s2;
-            }
+            if (col_ok[q] && col < n)
+                p.out[(c0 + 2 * c + q) * (int64_t)n + col] = (r[jj] * col_rs[q]) * s2;
         }
     }
 }
