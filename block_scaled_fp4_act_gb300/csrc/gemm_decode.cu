@@ -576,6 +576,12 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1)
 
     const int k = p.k, n = p.n, E = p.E, mt = dp.mt;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Launched with programmatic stream serialization: a kernel queued behind this one may
+    // be scheduled as this one's CTAs exit, and this one may start while the kernel before
+    // it drains. Nothing of global memory is read before that kernel has completed and its
+    // writes are visible (griddepcontrol.wait), so any input may come from it.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // items per expert: passes of up to PR rows x weight blocks (bad offsets: none); the
     // offsets stay in shared memory (reads of global memory behind the weight stream wait
     // for the whole memory queue)
@@ -930,7 +936,23 @@ static cudaError_t launch_dtma(const GroupedProblem &p, cudaStream_t s)
     // the exact count evenly over the CTAs it gets
     const int64_t max_items = ((p.P + PR - 1) / PR + p.E) * (int64_t)dp.mt;
     const int grid = (int)std::min<int64_t>(max_items, decode_sms());
-    kern<<<grid, (kWarps + 1) * 32, dp.L.total, s>>>(tmW, tmS, dp);
+    // programmatic stream serialization: the launch latency and CTA start-up of this kernel
+    // overlap the tail of the previous one on the stream (measured on GB300: 3 us per
+    // gate/up + down decode step); the kernel waits for that one's completion before it
+    // reads global memory
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((kWarps + 1) * 32);
+    cfg.dynamicSmemBytes = dp.L.total;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmW, tmS, dp);
+    if (e != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 
