@@ -306,34 +306,35 @@ def test_grouped_decode_expert_limit(E):
     assert fp4.fp4_get_device_error() == 0
 
 
-def test_grouped_decode_back_to_back_dependency():
+@pytest.mark.parametrize("recipe", [fp4.NVFP4, fp4.MXFP4])
+def test_grouped_decode_back_to_back_dependency(recipe):
     """Two decode-path calls queued back to back on one stream, the second reading the
     first's output as its activations (as a down projection reads h). The second kernel may
     be scheduled while the first drains, and must read nothing before the first has
     finished: the first output starts as NaN, and every output of the second call is checked
     against the oracle run on the first call's final output."""
-    gen = torch.Generator().manual_seed(909)
+    gen = torch.Generator().manual_seed(909 + recipe)
     E, T, n1, k1, n2 = 24, 16, 1536, 1024, 512
     sizes = torch.randint(0, 4, (E,), generator=gen)
     offsets = torch.zeros(E + 1, dtype=torch.int32)
     offsets[1:] = torch.cumsum(sizes, 0).to(torch.int32)
     P = int(offsets[-1])
     row_ids = torch.randint(0, T, (P,), generator=gen, dtype=torch.int32)
-    b1 = synth.make_bank(fp4.NVFP4, E, n1, k1, 901, "cpu", scale2_value=5.9945243e-5)
-    b2 = synth.make_bank(fp4.NVFP4, E, n2, n1, 902, "cpu", scale2_value=1.0 / 64.0)
-    bank1 = synth.Bank(fp4.NVFP4, b1.w.to(DEV), b1.sc.to(DEV), b1.scale2.to(DEV))
-    bank2 = synth.Bank(fp4.NVFP4, b2.w.to(DEV), b2.sc.to(DEV), b2.scale2.to(DEV))
+    b1 = synth.make_bank(recipe, E, n1, k1, 901, "cpu", scale2_value=5.9945243e-5)
+    b2 = synth.make_bank(recipe, E, n2, n1, 902, "cpu", scale2_value=1.0 / 64.0)
+    bank1 = synth.Bank(recipe, b1.w.to(DEV), b1.sc.to(DEV), b1.scale2.to(DEV))
+    bank2 = synth.Bank(recipe, b2.w.to(DEV), b2.sc.to(DEV), b2.scale2.to(DEV))
     x = (torch.randn(T, k1, generator=gen) * 2).to(DEV)
     off_d, rid_d = offsets.to(DEV), row_ids.to(DEV)
     ident = torch.arange(P, dtype=torch.int32, device=DEV)
-    assert fp4.fp4_gemm_path(P, E, n1, k1, fp4.NVFP4, False) == fp4.PATH_STREAM
+    assert fp4.fp4_gemm_path(P, E, n1, k1, recipe, False) == fp4.PATH_STREAM
     for _ in range(3):
         h = torch.full((P, n1), float("nan"), device=DEV)
         torch.cuda.synchronize()
-        fp4.fp4_grouped_expert_gemm(x, rid_d, off_d, bank1.w, bank1.sc, bank1.scale2, fp4.NVFP4,
+        fp4.fp4_grouped_expert_gemm(x, rid_d, off_d, bank1.w, bank1.sc, bank1.scale2, recipe,
                                     out=h)
         y = fp4.fp4_grouped_expert_gemm(h, ident, off_d, bank2.w, bank2.sc, bank2.scale2,
-                                        fp4.NVFP4)
+                                        recipe)
         torch.cuda.synchronize()
         assert not torch.isnan(h).any()
         proj = synth.Projection("chained", h, synth.Routing(off_d, ident), bank2)
