@@ -526,9 +526,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // releases its A slot with bar.arrive. A slot's next use is full only after the
         // converters saw the MMAs of its previous use complete, so the relay can never
         // lap the MMA warp on a named barrier.
+        // The converters run ahead of the MMAs, and an mbarrier wait costs this warp a
+        // few hundred cycles even on a completed phase (its SM sub-partition is busy with
+        // converter work), which made the relay the pace-setter at small N. So lanes 0-3
+        // test the A slots of the next four stages in one instruction, and the stages
+        // found full are released without another wait.
         Ring<A_STAGES> ra;
         Ring<B_STAGES> rb;
         int it = 0;
+        int a_ready = 0;  // stages from ra on whose converted A slot is known to be full
         bool aborted = false, stuck = false;
         for (int t = blockIdx.x; t < total && !aborted; t += gridDim.x, ++it) {
             const Tile tl = tile_at(t, prefix, p);
@@ -541,8 +547,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kb = 0; kb < nkb; ++kb) {
                 if (ok && j == 0)
                     ok = warp_mbar_wait(bfull(rb.slot), rb.phase, abort_flag, p.err, p.wait_limit);
-                if (ok)
-                    ok = warp_mbar_wait(afull(ra.slot), ra.phase, abort_flag, p.err, p.wait_limit);
+                if (ok && a_ready == 0) {
+                    // stage l ahead uses slot ra.slot + l (mod A_STAGES), one phase later
+                    // if that wraps; its previous use was released already, so a full
+                    // phase of that parity is this stage's
+                    bool full_l = false;
+                    if (lane < A_STAGES) {
+                        const int sl = ra.slot + lane;
+                        full_l = mbar_test(afull(sl % A_STAGES), ra.phase ^ (sl >= A_STAGES ? 1u : 0u));
+                    }
+                    const unsigned full_m = __ballot_sync(0xFFFFFFFFu, full_l);
+                    __syncwarp();
+                    a_ready = __ffs(~full_m) - 1;  // consecutive full stages from ra
+                    if (a_ready == 0) {
+                        ok = warp_mbar_wait(afull(ra.slot), ra.phase, abort_flag, p.err, p.wait_limit);
+                        a_ready = 1;
+                    }
+                }
                 if (!ok) {
                     // Aborting: keep the MMA warp moving to the end of this tile, then stop
                     // it at the next tile start. Release a slot only after the MMAs of its
@@ -556,6 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 named_arrive(kNamedAReady + ra.slot, kNamedThreads);
                 ra.next();
+                a_ready = a_ready > 0 ? a_ready - 1 : 0;
                 if (j == kbps - 1 || kb == nkb - 1) {
                     rb.next();
                     j = 0;

@@ -23,6 +23,20 @@ __device__ __forceinline__ bool warp_mbar_wait(uint32_t bar, uint32_t parity,
     return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
 }
 
+// Non-blocking test of an mbarrier phase: whether the phase of the given parity has
+// completed (with acquire semantics for the calling thread when it has).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool warp_mbar_drain(uint32_t bar, uint32_t parity)
 {
     bool ok = true;
