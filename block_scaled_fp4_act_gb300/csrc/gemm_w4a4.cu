@@ -431,11 +431,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kWarpRelay) {
         // ---------------------------------------------------------- relay
         // Per stage: the code slot (at a slot's first k-block), the weight stage and the
-        // scale-factor slot must be full; then the stage goes to the MMA warp.
+        // scale-factor slot must be full; then the stage goes to the MMA warp. An mbarrier
+        // wait costs this warp a few hundred cycles even on a completed phase, so lanes
+        // 0-3 test the weight and scale-factor slots of the next four stages in one
+        // instruction, and the stages found full are released without further waits.
+        static_assert(SF_STAGES <= W_STAGES && SF_STAGES <= 32, "relay look-ahead");
         Ring<SF_STAGES> rf;
         Ring<W_STAGES> rw;
         Ring<B_STAGES> rb;
         int it = 0;
+        int ready = 0;  // stages from rf / rw on whose weight and scale-factor slots are full
         bool aborted = false, stuck = false;
         for (int t = blockIdx.x; t < total && !aborted; t += gridDim.x, ++it) {
             const Tile tl = tile_at(t, prefix, p);
@@ -447,10 +452,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int j = kb & kbmask;
                 if (ok && j == 0)
                     ok = warp_mbar_wait(bfull(rb.slot), rb.phase, abort_flag, p.err, p.wait_limit);
-                if (ok)
-                    ok = warp_mbar_wait(wfull(rw.slot), rw.phase, abort_flag, p.err, p.wait_limit);
-                if (ok)
-                    ok = warp_mbar_wait(sffull(rf.slot), rf.phase, abort_flag, p.err, p.wait_limit);
+                if (ok && ready == 0) {
+                    // stage l ahead uses slots rw.slot + l and rf.slot + l (one phase later
+                    // where they wrap); their previous uses were released already, so a full
+                    // phase of that parity is this stage's
+                    bool full_l = false;
+                    if (lane < SF_STAGES) {
+                        const int fsl = rf.slot + lane, wsl = rw.slot + lane;
+                        full_l = mbar_test(sffull(fsl % SF_STAGES), rf.phase ^ (fsl >= SF_STAGES ? 1u : 0u)) &&
+                                 mbar_test(wfull(wsl % W_STAGES), rw.phase ^ (wsl >= W_STAGES ? 1u : 0u));
+                    }
+                    const unsigned full_m = __ballot_sync(0xFFFFFFFFu, full_l);
+                    __syncwarp();
+                    ready = __ffs(~full_m) - 1;  // consecutive full stages from rf / rw
+                    if (ready == 0) {
+                        ok = warp_mbar_wait(wfull(rw.slot), rw.phase, abort_flag, p.err, p.wait_limit);
+                        if (ok)
+                            ok = warp_mbar_wait(sffull(rf.slot), rf.phase, abort_flag, p.err, p.wait_limit);
+                        ready = 1;
+                    }
+                }
                 if (!ok) {
                     aborted = true;
                     if (!warp_mbar_drain(sfempty(rf.slot), rf.phase ^ 1u)) {
@@ -461,6 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_arrive(kNamedReady + rf.slot, kNamedThreads);
                 rf.next();
                 rw.next();
+                ready = ready > 0 ? ready - 1 : 0;
                 if (j == kbmask || kb == nkb - 1)
                     rb.next();
             }
