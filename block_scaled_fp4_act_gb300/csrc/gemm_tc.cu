@@ -298,10 +298,22 @@ __host__ __device__ constexpr int bmap_kblocks(int bi)
     return bi == 0 ? 12 : bi == 1 ? 6 : bi == 2 ? 3 : 2;
 }
 
-// SWIGLU: the weight maps have 16-row boxes; each weight slot is filled by eight of them
-// (block b: gate rows when b is even, up rows when odd, 16 h columns from 64 m + 16 (b / 2)),
-// so lane quarter q holds 16 gate rows in its lanes 0-15 and the matching up rows in lanes
-// 16-31, and the epilogue pairs them with one shuffle.
+// SWIGLU: a weight slot holds eight 16-row blocks (block b: gate rows when b is even, up
+// rows when odd, 16 h columns from 64 m + 16 (b / 2)), brought in by one 5-D box
+// {k, 16 rows, gate/up, 16-row block, expert} for the nibbles and one for the scales (eight
+// 2-D boxes per slot were 4% slower once the stage rate rose), so lane quarter q holds 16
+// gate rows in its lanes 0-15 and the matching up rows in lanes 16-31, and the epilogue
+// pairs them with one shuffle.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, int c3, int c4, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+                 "r"(bar)
+                 : "memory");
+}
+
 template <bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ BMaps tmB, const __grid_constant__ CUtensorMap tmW,
@@ -438,13 +450,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int k0 = j * W_KS * BK;  // first k of the slot
                         mbar_arrive_expect_tx(ful, W_BYTES);
                         if (SWIGLU) {
-#pragma unroll
-                            for (int b = 0; b < 8; ++b) {
-                                const int yb = tl.e * p.n + (b & 1) * p.inter + tl.m * 64 + (b >> 1) * 16;
-                                tma_load_2d(smem_u32(dst + b * 16 * 128), &tmW, k0 / 2, yb, ful);
-                                tma_load_2d(smem_u32(dst + NIB_BYTES + b * 16 * 16), &tmS, k0 / 16, yb,
-                                            ful);
-                            }
+                            // one 5-D box each: {k, row of a 16-row block, gate/up, block, expert}
+                            tma_load_5d(smem_u32(dst), &tmW, k0 / 2, 0, 0, tl.m * 4, tl.e, ful);
+                            tma_load_5d(smem_u32(dst + NIB_BYTES), &tmS, k0 / 16, 0, 0, tl.m * 4, tl.e,
+                                        ful);
                         } else {
                             tma_load_2d(smem_u32(dst), &tmW, k0 / 2, yw, ful);
                             tma_load_2d(smem_u32(dst + NIB_BYTES), &tmS, k0 / 16, yw, ful);
@@ -1078,11 +1087,34 @@ cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaS
         if (!make_map_kblocks(&tmB.m[i], l.act, (uint64_t)p.k, (uint64_t)p.P,
                               (uint32_t)bmap_rows(i), (uint32_t)bmap_kblocks(i)))
             return cudaErrorInvalidValue;
-    if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w, (uint64_t)p.k / 2,
-                  (uint64_t)p.E * p.n, W_KS * BK / 2, wbox, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sc, (uint64_t)p.k / 16,
-                  (uint64_t)p.E * p.n, 16, wbox, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (sw) {
+        // gate/up bank [E][2][inter][k/2] (and its scales) as 5-D {k, 16 rows, gate/up,
+        // 16-row block, expert}: one box {W slot, 16, 2, 4, 1} is a weight slot's eight
+        // 16-row boxes in slot order (block-major, gate before up)
+        auto fn = encode_fn();
+        if (!fn)
+            return cudaErrorInvalidValue;
+        const uint64_t rb = (uint64_t)p.k / 2, rs = (uint64_t)p.k / 16, in = (uint64_t)sw->inter;
+        cuuint64_t dims[5] = {rb, 16, 2, in / 16, (cuuint64_t)p.E};
+        cuuint64_t strides[4] = {rb, in * rb, 16 * rb, (uint64_t)p.n * rb};
+        cuuint32_t box[5] = {(cuuint32_t)(W_KS * BK / 2), 16, 2, 4, 1};
+        cuuint32_t es[5] = {1, 1, 1, 1, 1};
+        cuuint64_t sdims[5] = {rs, 16, 2, in / 16, (cuuint64_t)p.E};
+        cuuint64_t sstrides[4] = {rs, in * rs, 16 * rs, (uint64_t)p.n * rs};
+        cuuint32_t sbox[5] = {16, 16, 2, 4, 1};
+        if (fn(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<uint8_t *>(p.w), dims, strides,
+               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+            fn(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<uint8_t *>(p.sc), sdims, sstrides,
+               sbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    } else if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w, (uint64_t)p.k / 2,
+                         (uint64_t)p.E * p.n, W_KS * BK / 2, wbox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+               !make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.sc, (uint64_t)p.k / 16,
+                         (uint64_t)p.E * p.n, 16, wbox, CU_TENSOR_MAP_SWIZZLE_NONE)) {
         return cudaErrorInvalidValue;
+    }
     Params kp;
     kp.offsets = p.offsets;
     kp.E = p.E;
