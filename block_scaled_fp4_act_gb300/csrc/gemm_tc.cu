@@ -699,10 +699,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(accf(buf), (it >> 1) & 1, abort_flag, p.err, p.wait_limit))
                 break;
             tc_fence_after();
-            // SWIGLU: lanes 0-15 own h column col, lanes 16-31 hold the matching up rows
+            // SWIGLU: TMEM lanes 0-15 of the quarter hold gate rows and 16-31 the matching up
+            // rows; h column col is computed by lane col % 16 for even routed rows and by
+            // lane 16 + col % 16 for odd ones
             const int col = SWIGLU ? tl.m * 64 + q * 16 + (lane & 15) : tl.m * BM + q * 32 + lane;
             const int ldo = SWIGLU ? p.inter : p.n;
-            const bool colok = SWIGLU ? (lane < 16 && col < p.inter) : col < p.n;
+            const bool colok = SWIGLU ? col < p.inter : col < p.n;
             const float s2 = p.scale2 ? __ldg(p.scale2 + tl.e) : p.scale2_host;
             float *orow = p.out + tl.row0 * (int64_t)ldo + col;
             for (int c0 = 0; c0 < tl.rows; c0 += 32) {
@@ -712,16 +714,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float rs = 1.0f;
                 if (f16_route && c0 + lane < tl.rows)
                     rs = __ldg(p.rowscale + tl.row0 + c0 + lane);
+                if constexpr (SWIGLU) {
+                    // two routed rows a step: lanes 0-15 take row jj (gate here, up from lane
+                    // + 16), lanes 16-31 row jj + 1 (gate from lane - 16, up here), so each
+                    // lane evaluates SwiGLU once per two rows and a store covers both rows
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    // f16_route is uniform over the CTA, so every lane takes the shuffle
-                    const float r = f16_route ? __shfl_sync(0xFFFFFFFFu, rs, jj) : 1.0f;
-                    if constexpr (SWIGLU) {
-                        const float val = (__uint_as_float(v[jj]) * r) * s2;
-                        const float up = __shfl_xor_sync(0xFFFFFFFFu, val, 16);
-                        if (colok && c0 + jj < tl.rows)
-                            orow[(int64_t)(c0 + jj) * ldo] = swiglu_one(val, up, p.limit);
-                    } else {
+                    for (int jj = 0; jj < 32; jj += 2) {
+                        // f16_route is uniform over the CTA, so every lane takes the shuffles
+                        const float ra = f16_route ? __shfl_sync(0xFFFFFFFFu, rs, jj) : 1.0f;
+                        const float rb = f16_route ? __shfl_sync(0xFFFFFFFFu, rs, jj + 1) : 1.0f;
+                        const float va = (__uint_as_float(v[jj]) * ra) * s2;
+                        const float vb = (__uint_as_float(v[jj + 1]) * rb) * s2;
+                        const float other = __shfl_xor_sync(0xFFFFFFFFu, lane < 16 ? vb : va, 16);
+                        const float gate = lane < 16 ? va : other, up = lane < 16 ? other : vb;
+                        const int row = c0 + jj + (lane >> 4);
+                        if (colok && row < tl.rows)
+                            orow[(int64_t)row * ldo] = swiglu_one(gate, up, p.limit);
+                    }
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) {
+                        // f16_route is uniform over the CTA, so every lane takes the shuffle
+                        const float r = f16_route ? __shfl_sync(0xFFFFFFFFu, rs, jj) : 1.0f;
                         if (colok && c0 + jj < tl.rows)
                             orow[(int64_t)(c0 + jj) * ldo] = (__uint_as_float(v[jj]) * r) * s2;
                     }
