@@ -56,8 +56,11 @@ def _check_quant(x):
                                                                    oc[tuple(bad)]))
 
 
-@pytest.mark.parametrize("rows,k", [(9, 32), (16, 48), (33, 2048), (12, 7168), (3, 16)])
+@pytest.mark.parametrize("rows,k", [(9, 32), (16, 48), (33, 2048), (12, 7168), (3, 16),
+                                    (5, 512), (7, 1040), (4, 4096), (3, 8192), (2, 8720)])
 def test_act_quant_w4a4_bit_exact(rows, k):
+    """Bit-exact against the oracle on row lengths from one 16-group to past 8192, ragged
+    against the CTA's 128 threads x 4 values and exact multiples of it."""
     rng = np.random.default_rng(rows * 131 + k)
     _check_quant(_rows(rng, rows, k))
 
