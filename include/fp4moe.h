@@ -111,6 +111,10 @@ size_t fp4_grouped_workspace_size(int64_t num_tokens, int64_t total_rows, int64_
  *   workspace at least fp4_grouped_workspace_size(...) bytes (may be NULL if that is 0)
  * Experts with no rows cost nothing but a CTA exit. Offsets or row ids that fail the
  * device checks set fp4_get_device_error bits; their rows are skipped (out untouched).
+ * Stream order is kept. The weight-streaming kernel is launched with programmatic stream
+ * serialization: it may be scheduled while the kernel before it on the stream is still
+ * draining, and it reads no global memory (inputs included) until that kernel has
+ * completed, so any input may be the previous kernel's output.
  */
 int fp4_grouped_expert_gemm(const float *x, int64_t num_tokens, const int32_t *row_ids,
                             const int32_t *offsets, int num_experts, int64_t total_rows,
