@@ -696,6 +696,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
             const Tile tl = tile_at(t, prefix, p);
             const int buf = it & 1;
+            // The tile's global reads (its routed rows' scales, lane j holding row 32 c + j,
+            // and scale2) are issued before the wait for the accumulator: read chunk by chunk
+            // after it, each waited behind the kernel's own copies, and the accumulator's
+            // release for tile it + 2 came ~2,000 (N = 64) to ~6,400 (N = 192) cycles late.
+            float rsv[BN / 32];
+#pragma unroll
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                const int rr = cc * 32 + lane;
+                rsv[cc] = f16_route && rr < tl.rows ? __ldg(p.rowscale + tl.row0 + rr) : 1.0f;
+            }
+            const float s2 = p.scale2 ? __ldg(p.scale2 + tl.e) : p.scale2_host;
             if (!mbar_wait(accf(buf), (it >> 1) & 1, abort_flag, p.err, p.wait_limit))
                 break;
             tc_fence_after();
@@ -705,15 +716,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int col = SWIGLU ? tl.m * 64 + q * 16 + (lane & 15) : tl.m * BM + q * 32 + lane;
             const int ldo = SWIGLU ? p.inter : p.n;
             const bool colok = SWIGLU ? col < p.inter : col < p.n;
-            const float s2 = p.scale2 ? __ldg(p.scale2 + tl.e) : p.scale2_host;
             float *orow = p.out + tl.row0 * (int64_t)ldo + col;
-            for (int c0 = 0; c0 < tl.rows; c0 += 32) {
+#pragma unroll
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                const int c0 = cc * 32;
+                if (c0 >= tl.rows)
+                    break;
                 uint32_t v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c0), v);
                 // f16 route: column (routed row) scale 2^M_p, exact; lane j holds row c0 + j
-                float rs = 1.0f;
-                if (f16_route && c0 + lane < tl.rows)
-                    rs = __ldg(p.rowscale + tl.row0 + c0 + lane);
+                const float rs = rsv[cc];
                 if constexpr (SWIGLU) {
                     // two routed rows a step: lanes 0-15 take row jj (gate here, up from lane
                     // + 16), lanes 16-31 row jj + 1 (gate from lane - 16, up here), so each
