@@ -129,8 +129,15 @@ static_assert(kNamedAReady + A_STAGES <= 16, "named barrier ids");
 // MMA warp has read the entry's previous tile by then.
 constexpr int kTileInfo = A_STAGES;
 static_assert(2 * kTileInfo > A_STAGES, "tile info ring depth");
-constexpr int SMEM_BYTES =
-    1024 + RING_BYTES + NUM_BARS * 8 + 16 + (kMaxExperts + 1) * 4 + kTileInfo * 4;
+// Tiles looked up ahead for the relay: entry i % kTileRing holds tile i of this CTA (its
+// iteration index first, -1 until written), published by the weight producer when it
+// starts the tile's copies (at most 16 k-stages, so 4 tiles, ahead of the relay). A lookup
+// (a binary search over the expert prefix and two offset reads) cost the relay ~1,000
+// cycles at every tile start, while the MMA warp waited.
+constexpr int kTileRing = 8;
+constexpr int kTileRingInts = 8;  // seq, e, m, rows, row0 (low, high)
+constexpr int SMEM_BYTES = 1024 + RING_BYTES + NUM_BARS * 8 + 16 + (kMaxExperts + 1) * 4 +
+                           kTileInfo * 4 + kTileRing * kTileRingInts * 4;
 static_assert(B_BYTES % 1024 == 0 && W_BYTES % 1024 == 0 && OFF_W % 1024 == 0,
               "swizzled tiles need 1024-byte alignment");
 static_assert(BN * BK * 2 * 2 <= B_BYTES && BN % 16 == 0 && BN <= 256, "activation box");
@@ -329,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tile it's routed-row count (or -1: stop) at tile_info[it % kTileInfo], written by the
     // relay before its first release of the tile's first stage
     volatile int *tile_info = prefix + kMaxExperts + 1;
+    volatile int *tile_ring = tile_info + kTileInfo;
 
     // Values that feed tcgen05 operands are broadcast from lane 0: the compiler then knows
     // they are warp-uniform and issues each tcgen05 instruction once, instead of once per
@@ -382,6 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         prefix[0] = 0;
+        for (int i = 0; i < kTileRing; ++i)
+            tile_ring[i * kTileRingInts] = -1;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == kWarpMma)
@@ -427,8 +437,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (int t = blockIdx.x, pit = 0; t < total && ok; t += gridDim.x, ++pit) {
                 const Tile tl = tile_at(t, prefix, p);
+                if (!is_b) {  // publish the lookup for the relay (entry pit % kTileRing)
+                    volatile int *ent = tile_ring + (pit % kTileRing) * kTileRingInts;
+                    ent[1] = tl.e;
+                    ent[2] = tl.m;
+                    ent[3] = tl.rows;
+                    ent[4] = (int)(uint32_t)((uint64_t)tl.row0 & 0xFFFFFFFFu);
+                    ent[5] = (int)(uint32_t)((uint64_t)tl.row0 >> 32);
+                    __threadfence_block();
+                    ent[0] = pit;
+                }
                 const int yw = tl.e * p.n + tl.m * BM;
                 const int bi = bmap_index(tl.rows);
                 const int kbps = bmap_kblocks(bi);
@@ -546,7 +566,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         int a_ready = 0;  // stages from ra on whose converted A slot is known to be full
         bool aborted = false, stuck = false;
         for (int t = blockIdx.x; t < total && !aborted; t += gridDim.x, ++it) {
-            const Tile tl = tile_at(t, prefix, p);
+            Tile tl;
+            volatile int *ent = tile_ring + (it % kTileRing) * kTileRingInts;
+            if (ent[0] == it) {  // looked up ahead by the epilogue
+                __threadfence_block();
+                tl.e = ent[1];
+                tl.m = ent[2];
+                tl.rows = ent[3];
+                tl.row0 = (int64_t)(((uint64_t)(uint32_t)ent[5] << 32) | (uint32_t)ent[4]);
+            } else {
+                tl = tile_at(t, prefix, p);
+            }
             const int buf = it & 1;
             // published before the arrival that releases the tile's first stage
             tile_info[it % kTileInfo] = tl.rows;
