@@ -131,10 +131,11 @@ constexpr int kTileInfo = A_STAGES;
 static_assert(2 * kTileInfo > A_STAGES, "tile info ring depth");
 // Tiles looked up ahead for the relay: entry i % kTileRing holds tile i of this CTA (its
 // iteration index first, -1 until written), published by the weight producer when it
-// starts the tile's copies (at most 16 k-stages, so 4 tiles, ahead of the relay). A lookup
-// (a binary search over the expert prefix and two offset reads) cost the relay ~1,000
-// cycles at every tile start, while the MMA warp waited.
-constexpr int kTileRing = 8;
+// starts the tile's copies (at most 16 k-stages, so 4 tiles, ahead of the relay, which
+// checks the index before it reads an entry). A lookup (a binary search over the expert
+// prefix and two offset reads) cost the relay ~1,000 cycles at every tile start, while the
+// MMA warp waited.
+constexpr int kTileRing = 16;
 constexpr int kTileRingInts = 8;  // seq, e, m, rows, row0 (low, high)
 constexpr int SMEM_BYTES = 1024 + RING_BYTES + NUM_BARS * 8 + 16 + (kMaxExperts + 1) * 4 +
                            kTileInfo * 4 + kTileRing * kTileRingInts * 4;
