@@ -137,8 +137,13 @@ static_assert(2 * kTileInfo > A_STAGES, "tile info ring depth");
 // MMA warp waited.
 constexpr int kTileRing = 16;
 constexpr int kTileRingInts = 8;  // seq, e, m, rows, row0 (low, high)
-constexpr int SMEM_BYTES = 1024 + RING_BYTES + NUM_BARS * 8 + 16 + (kMaxExperts + 1) * 4 +
-                           kTileInfo * 4 + kTileRing * kTileRingInts * 4;
+// Epilogue staging: each epilogue warp owns two 2 KB halves, each 16 routed rows of its 32
+// output columns (16 h columns under SwiGLU), which one tensor store writes to the output
+// while the warp fills the other half.
+constexpr int kEpiHalfBytes = 2048;
+constexpr int OFF_EPI = (RING_BYTES + NUM_BARS * 8 + 16 + (kMaxExperts + 1) * 4 + kTileInfo * 4 +
+                         kTileRing * kTileRingInts * 4 + 1023) & ~1023;
+constexpr int SMEM_BYTES = 1024 + OFF_EPI + 4 * 2 * kEpiHalfBytes;
 static_assert(B_BYTES % 1024 == 0 && W_BYTES % 1024 == 0 && OFF_W % 1024 == 0,
               "swizzled tiles need 1024-byte alignment");
 static_assert(BN * BK * 2 * 2 <= B_BYTES && BN % 16 == 0 && BN <= 256, "activation box");
@@ -164,6 +169,9 @@ struct Params {
     // converter warp of CTA 0 withhold its first arrival, so this launch times out and aborts
     long long wait_limit;
     int stall;
+    // nonzero: the output tensor map is valid (row stride a multiple of 16 bytes), and the
+    // epilogue writes whole 32-row chunks through it
+    int tma_out;
     // fused SwiGLU (gate/up bank: rows [0, inter) gate, [inter, 2 inter) up): out is h
     // [P, inter]; a tile covers 64 h columns (16 gate + 16 up rows per lane quarter)
     int inter;
@@ -325,7 +333,8 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map
 template <bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ BMaps tmB, const __grid_constant__ CUtensorMap tmW,
-                   const __grid_constant__ CUtensorMap tmS, const Params p)
+                   const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmO,
+                   const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -723,6 +732,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (role == ROLE_EPI) {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;
+        float *stg = reinterpret_cast<float *>(smem + OFF_EPI + q * 2 * kEpiHalfBytes);
+        const uint32_t stg_s = smem_u32(stg);
+        int half = 0;  // halves staged so far: half & 1 is the one to fill next
         int it = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
             const Tile tl = tile_at(t, prefix, p);
@@ -744,7 +756,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // SWIGLU: TMEM lanes 0-15 of the quarter hold gate rows and 16-31 the matching up
             // rows; h column col is computed by lane col % 16 for even routed rows and by
             // lane 16 + col % 16 for odd ones
-            const int col = SWIGLU ? tl.m * 64 + q * 16 + (lane & 15) : tl.m * BM + q * 32 + lane;
+            const int col0 = SWIGLU ? tl.m * 64 + q * 16 : tl.m * BM + q * 32;
+            const int col = col0 + (SWIGLU ? (lane & 15) : lane);
             const int ldo = SWIGLU ? p.inter : p.n;
             const bool colok = SWIGLU ? col < p.inter : col < p.n;
             float *orow = p.out + tl.row0 * (int64_t)ldo + col;
@@ -757,7 +770,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c0), v);
                 // f16 route: column (routed row) scale 2^M_p, exact; lane j holds row c0 + j
                 const float rs = rsv[cc];
-                if constexpr (SWIGLU) {
+                if (p.tma_out && c0 + 32 <= tl.rows && col0 < ldo) {
+                    // A whole chunk leaves through shared memory, 16 rows a tensor store:
+                    // a shared store per value has no address arithmetic and no wait on
+                    // the global store path, which made the epilogue of a 192-row tile
+                    // release its accumulator late. Columns past the output's width are
+                    // cut off by the tensor store.
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        float *dst = stg + (half & 1) * (kEpiHalfBytes / 4);
+                        if (lane == 0)
+                            bulk_wait_read_all_but_one();  // this half's last store has read it
+                        __syncwarp();
+                        if constexpr (SWIGLU) {
+#pragma unroll
+                            for (int jj = 16 * h; jj < 16 * h + 16; jj += 2) {
+                                const float ra = f16_route ? __shfl_sync(0xFFFFFFFFu, rs, jj) : 1.0f;
+                                const float rb =
+                                    f16_route ? __shfl_sync(0xFFFFFFFFu, rs, jj + 1) : 1.0f;
+                                const float va = (__uint_as_float(v[jj]) * ra) * s2;
+                                const float vb = (__uint_as_float(v[jj + 1]) * rb) * s2;
+                                const float other =
+                                    __shfl_xor_sync(0xFFFFFFFFu, lane < 16 ? vb : va, 16);
+                                const float gate = lane < 16 ? va : other,
+                                            up = lane < 16 ? other : vb;
+                                // row jj - 16 h + lane / 16 of the half, column lane % 16
+                                dst[(jj - 16 * h) * 16 + lane] = swiglu_one(gate, up, p.limit);
+                            }
+                        } else {
+#pragma unroll
+                            for (int jj = 16 * h; jj < 16 * h + 16; ++jj) {
+                                const float r = f16_route ? __shfl_sync(0xFFFFFFFFu, rs, jj) : 1.0f;
+                                dst[(jj - 16 * h) * 32 + lane] = (__uint_as_float(v[jj]) * r) * s2;
+                            }
+                        }
+                        fence_proxy_async();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmO, stg_s + (uint32_t)((half & 1) * kEpiHalfBytes), col0,
+                                         (int)(tl.row0 + c0 + 16 * h));
+                            bulk_commit();
+                        }
+                        ++half;
+                    }
+                } else if constexpr (SWIGLU) {
                     // two routed rows a step: lanes 0-15 take row jj (gate here, up from lane
                     // + 16), lanes 16-31 row jj + 1 (gate from lane - 16, up here), so each
                     // lane evaluates SwiGLU once per two rows and a store covers both rows
@@ -789,6 +845,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0)
                 mbar_arrive(acce(buf));
         }
+        if (lane == 0)
+            bulk_wait_all();  // the staged halves stay in use until their stores complete
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -1189,6 +1248,15 @@ cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaS
     kp.wait_limit = take_stall_request(&kp.stall);
     kp.inter = sw ? (int)sw->inter : 0;
     kp.limit = sw ? sw->limit : 0.0f;
+    // output [P, ldo] f32 as a tensor map with 16-row boxes of one epilogue warp's columns;
+    // without one (a row stride that is not a multiple of 16 bytes) every value is stored
+    // from registers
+    alignas(64) CUtensorMap tmO = {};
+    const int64_t ldo = sw ? (int64_t)sw->inter : (int64_t)p.n;
+    kp.tma_out = kp.out && ldo % 4 == 0 && (reinterpret_cast<uintptr_t>(kp.out) & 15) == 0 &&
+                 p.P > 0 && p.P < ((int64_t)1 << 31) &&
+                 make_map(&tmO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kp.out, (uint64_t)ldo,
+                          (uint64_t)p.P, sw ? 16 : 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
     auto kern = sw ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
     static bool attr_set[2][64] = {};
     int dev = 0;
@@ -1203,7 +1271,7 @@ cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaS
     }
     const int64_t max_tiles = ((p.P + BN - 1) / BN + p.E) * (int64_t)kp.mt;
     const int grid = (int)(max_tiles < sms ? max_tiles : sms);
-    kern<<<grid, kThreads, SMEM_BYTES, s>>>(tmB, tmW, tmS, kp);
+    kern<<<grid, kThreads, SMEM_BYTES, s>>>(tmB, tmW, tmS, tmO, kp);
     return cudaGetLastError();
 }
 

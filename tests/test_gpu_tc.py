@@ -65,6 +65,19 @@ def test_tc_multi_block_experts(recipe):
     print("tc multi recipe %d: worst err/bound %.3g max_rel %.3g" % (recipe, worst, rel))
 
 
+@pytest.mark.parametrize("n", [130, 132, 36])
+def test_tc_output_row_stride_forms(n):
+    """Whole 32-row chunks leave the epilogue through tensor stores when an output row is a
+    multiple of 16 bytes (n = 132: the last weight block's box is cut at column 132; n = 36:
+    one partly valid warp) and through per-value stores otherwise (n = 130); ragged chunks
+    always take per-value stores."""
+    proj = _projection(fp4.NVFP4, [64, 33, 0, 200, 7], n=n, k=512, T=300, seed=3)
+    out, path = run_projection(proj)
+    assert path == fp4.PATH_TC
+    worst, rel = grouped_sampled_check(proj, out, path, np.arange(proj.routing.P), "tc n=%d" % n)
+    assert fp4.fp4_get_device_error() == 0
+
+
 @pytest.mark.parametrize("recipe", [fp4.NVFP4, fp4.MXFP4])
 def test_tc_exact_special_case(recipe, golden_dir):
     """Lossless inputs: every partial sum is exact in f32, so the tensor-core result must
