@@ -29,8 +29,9 @@
 //   warp 2      TMA producer of the weight slots (nibble box + scale box)
 //   warp 3      relay: does the MMA side's mbarrier waits and releases each A stage to
 //               warp 1 through a hardware named barrier
-//   warps 4-7   epilogue: tcgen05.ld of the accumulator, x row scale x scale2, coalesced
-//               f32 stores
+//   warps 4-7   epilogue: tcgen05.ld of the accumulator, x row scale x scale2; whole
+//               32-row chunks staged in shared memory and written by bulk tensor stores,
+//               the rest (and SwiGLU's h) by coalesced f32 stores
 //   warps 8-23  converters, four per TMEM lane quarter taking turns over the k-stages:
 //               nibbles x scales -> 16-bit A operand, tcgen05.st into TMEM
 // Two accumulators (2 x 192 TMEM columns) let the epilogue of one tile overlap the
@@ -137,9 +138,9 @@ static_assert(2 * kTileInfo > A_STAGES, "tile info ring depth");
 // MMA warp waited.
 constexpr int kTileRing = 16;
 constexpr int kTileRingInts = 8;  // seq, e, m, rows, row0 (low, high)
-// Epilogue staging: each epilogue warp owns two 2 KB halves, each 16 routed rows of its 32
-// output columns (16 h columns under SwiGLU), which one tensor store writes to the output
-// while the warp fills the other half.
+// Epilogue staging (plain output only): each epilogue warp owns two 2 KB halves, each 16
+// routed rows of its 32 output columns, which one tensor store writes to the output while
+// the warp fills the other half.
 constexpr int kEpiHalfBytes = 2048;
 constexpr int OFF_EPI = (RING_BYTES + NUM_BARS * 8 + 16 + (kMaxExperts + 1) * 4 + kTileInfo * 4 +
                          kTileRing * kTileRingInts * 4 + 1023) & ~1023;
@@ -770,39 +771,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + c0), v);
                 // f16 route: column (routed row) scale 2^M_p, exact; lane j holds row c0 + j
                 const float rs = rsv[cc];
-                if (p.tma_out && c0 + 32 <= tl.rows && col0 < ldo) {
+                if (!SWIGLU && p.tma_out && c0 + 32 <= tl.rows && col0 < ldo) {
                     // A whole chunk leaves through shared memory, 16 rows a tensor store:
                     // a shared store per value has no address arithmetic and no wait on
                     // the global store path, which made the epilogue of a 192-row tile
                     // release its accumulator late. Columns past the output's width are
-                    // cut off by the tensor store.
+                    // cut off by the tensor store. (Under SwiGLU, with 64-byte h rows per
+                    // warp, staged stores made the fused gate/up call slower instead.)
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         float *dst = stg + (half & 1) * (kEpiHalfBytes / 4);
                         if (lane == 0)
                             bulk_wait_read_all_but_one();  // this half's last store has read it
                         __syncwarp();
-                        if constexpr (SWIGLU) {
 #pragma unroll
-                            for (int jj = 16 * h; jj < 16 * h + 16; jj += 2) {
-                                const float ra = f16_route ? __shfl_sync(0xFFFFFFFFu, rs, jj) : 1.0f;
-                                const float rb =
-                                    f16_route ? __shfl_sync(0xFFFFFFFFu, rs, jj + 1) : 1.0f;
-                                const float va = (__uint_as_float(v[jj]) * ra) * s2;
-                                const float vb = (__uint_as_float(v[jj + 1]) * rb) * s2;
-                                const float other =
-                                    __shfl_xor_sync(0xFFFFFFFFu, lane < 16 ? vb : va, 16);
-                                const float gate = lane < 16 ? va : other,
-                                            up = lane < 16 ? other : vb;
-                                // row jj - 16 h + lane / 16 of the half, column lane % 16
-                                dst[(jj - 16 * h) * 16 + lane] = swiglu_one(gate, up, p.limit);
-                            }
-                        } else {
-#pragma unroll
-                            for (int jj = 16 * h; jj < 16 * h + 16; ++jj) {
-                                const float r = f16_route ? __shfl_sync(0xFFFFFFFFu, rs, jj) : 1.0f;
-                                dst[(jj - 16 * h) * 32 + lane] = (__uint_as_float(v[jj]) * r) * s2;
-                            }
+                        for (int jj = 16 * h; jj < 16 * h + 16; ++jj) {
+                            const float r = f16_route ? __shfl_sync(0xFFFFFFFFu, rs, jj) : 1.0f;
+                            dst[(jj - 16 * h) * 32 + lane] = (__uint_as_float(v[jj]) * r) * s2;
                         }
                         fence_proxy_async();
                         __syncwarp();
@@ -1248,15 +1233,15 @@ cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaS
     kp.wait_limit = take_stall_request(&kp.stall);
     kp.inter = sw ? (int)sw->inter : 0;
     kp.limit = sw ? sw->limit : 0.0f;
-    // output [P, ldo] f32 as a tensor map with 16-row boxes of one epilogue warp's columns;
-    // without one (a row stride that is not a multiple of 16 bytes) every value is stored
-    // from registers
+    // output [P, n] f32 as a tensor map with 16-row boxes of one epilogue warp's 32 columns
+    // (not under SwiGLU); without one (a row stride that is not a multiple of 16 bytes)
+    // every value is stored from registers
     alignas(64) CUtensorMap tmO = {};
-    const int64_t ldo = sw ? (int64_t)sw->inter : (int64_t)p.n;
-    kp.tma_out = kp.out && ldo % 4 == 0 && (reinterpret_cast<uintptr_t>(kp.out) & 15) == 0 &&
-                 p.P > 0 && p.P < ((int64_t)1 << 31) &&
-                 make_map(&tmO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kp.out, (uint64_t)ldo,
-                          (uint64_t)p.P, sw ? 16 : 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
+    kp.tma_out = !sw && kp.out && p.n % 4 == 0 &&
+                 (reinterpret_cast<uintptr_t>(kp.out) & 15) == 0 && p.P > 0 &&
+                 p.P < ((int64_t)1 << 31) &&
+                 make_map(&tmO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kp.out, (uint64_t)p.n,
+                          (uint64_t)p.P, 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
     auto kern = sw ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
     static bool attr_set[2][64] = {};
     int dev = 0;
