@@ -30,8 +30,8 @@
 //   warp 3      relay: does the MMA side's mbarrier waits and releases each A stage to
 //               warp 1 through a hardware named barrier
 //   warps 4-7   epilogue: tcgen05.ld of the accumulator, x row scale x scale2; whole
-//               32-row chunks staged in shared memory and written by bulk tensor stores,
-//               the rest (and SwiGLU's h) by coalesced f32 stores
+//               32-row chunks staged in shared memory and written by one bulk tensor
+//               store each, the rest (and SwiGLU's h) by coalesced f32 stores
 //   warps 8-23  converters, four per TMEM lane quarter taking turns over the k-stages:
 //               nibbles x scales -> 16-bit A operand, tcgen05.st into TMEM
 // Two accumulators (2 x 192 TMEM columns) let the epilogue of one tile overlap the
@@ -138,13 +138,14 @@ static_assert(2 * kTileInfo > A_STAGES, "tile info ring depth");
 // MMA warp waited.
 constexpr int kTileRing = 16;
 constexpr int kTileRingInts = 8;  // seq, e, m, rows, row0 (low, high)
-// Epilogue staging (plain output only): each epilogue warp owns two 2 KB halves, each 16
-// routed rows of its 32 output columns, which one tensor store writes to the output while
-// the warp fills the other half.
-constexpr int kEpiHalfBytes = 2048;
+// Epilogue staging (plain output only): each epilogue warp owns a 4 KB buffer, one 32-row
+// chunk of its 32 output columns, which one tensor store writes to the output. (Two 2 KB
+// halves of 16 rows, one filled while the other's store read it, were ~1 % slower: twice
+// the fences, waits and store issues.)
+constexpr int kEpiChunkBytes = 32 * 32 * 4;
 constexpr int OFF_EPI = (RING_BYTES + NUM_BARS * 8 + 16 + (kMaxExperts + 1) * 4 + kTileInfo * 4 +
                          kTileRing * kTileRingInts * 4 + 1023) & ~1023;
-constexpr int SMEM_BYTES = 1024 + OFF_EPI + 4 * 2 * kEpiHalfBytes;
+constexpr int SMEM_BYTES = 1024 + OFF_EPI + 4 * kEpiChunkBytes;
 static_assert(B_BYTES % 1024 == 0 && W_BYTES % 1024 == 0 && OFF_W % 1024 == 0,
               "swizzled tiles need 1024-byte alignment");
 static_assert(BN * BK * 2 * 2 <= B_BYTES && BN % 16 == 0 && BN <= 256, "activation box");
@@ -733,9 +734,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (role == ROLE_EPI) {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;
-        float *stg = reinterpret_cast<float *>(smem + OFF_EPI + q * 2 * kEpiHalfBytes);
+        float *stg = reinterpret_cast<float *>(smem + OFF_EPI + q * kEpiChunkBytes);
         const uint32_t stg_s = smem_u32(stg);
-        int half = 0;  // halves staged so far: half & 1 is the one to fill next
         int it = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
             const Tile tl = tile_at(t, prefix, p);
@@ -772,31 +772,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // f16 route: column (routed row) scale 2^M_p, exact; lane j holds row c0 + j
                 const float rs = rsv[cc];
                 if (!SWIGLU && p.tma_out && c0 + 32 <= tl.rows && col0 < ldo) {
-                    // A whole chunk leaves through shared memory, 16 rows a tensor store:
-                    // a shared store per value has no address arithmetic and no wait on
-                    // the global store path, which made the epilogue of a 192-row tile
-                    // release its accumulator late. Columns past the output's width are
-                    // cut off by the tensor store. (Under SwiGLU, with 64-byte h rows per
-                    // warp, staged stores made the fused gate/up call slower instead.)
+                    // A whole chunk leaves through shared memory and one tensor store: a
+                    // shared store per value has no address arithmetic and no wait on the
+                    // global store path, which made the epilogue of a 192-row tile release
+                    // its accumulator late. Columns past the output's width are cut off by
+                    // the tensor store. (Under SwiGLU, with 64-byte h rows per warp, staged
+                    // stores made the fused gate/up call slower instead.)
+                    if (lane == 0)
+                        bulk_wait_read_all();  // the previous chunk's store has read the buffer
+                    __syncwarp();
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        float *dst = stg + (half & 1) * (kEpiHalfBytes / 4);
-                        if (lane == 0)
-                            bulk_wait_read_all_but_one();  // this half's last store has read it
-                        __syncwarp();
-#pragma unroll
-                        for (int jj = 16 * h; jj < 16 * h + 16; ++jj) {
-                            const float r = f16_route ? __shfl_sync(0xFFFFFFFFu, rs, jj) : 1.0f;
-                            dst[(jj - 16 * h) * 32 + lane] = (__uint_as_float(v[jj]) * r) * s2;
-                        }
-                        fence_proxy_async();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&tmO, stg_s + (uint32_t)((half & 1) * kEpiHalfBytes), col0,
-                                         (int)(tl.row0 + c0 + 16 * h));
-                            bulk_commit();
-                        }
-                        ++half;
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const float r = f16_route ? __shfl_sync(0xFFFFFFFFu, rs, jj) : 1.0f;
+                        stg[jj * 32 + lane] = (__uint_as_float(v[jj]) * r) * s2;
+                    }
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmO, stg_s, col0, (int)(tl.row0 + c0));
+                        bulk_commit();
                     }
                 } else if constexpr (SWIGLU) {
                     // two routed rows a step: lanes 0-15 take row jj (gate here, up from lane
@@ -1233,7 +1227,7 @@ cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaS
     kp.wait_limit = take_stall_request(&kp.stall);
     kp.inter = sw ? (int)sw->inter : 0;
     kp.limit = sw ? sw->limit : 0.0f;
-    // output [P, n] f32 as a tensor map with 16-row boxes of one epilogue warp's 32 columns
+    // output [P, n] f32 as a tensor map with 32-row boxes of one epilogue warp's 32 columns
     // (not under SwiGLU); without one (a row stride that is not a multiple of 16 bytes)
     // every value is stored from registers
     alignas(64) CUtensorMap tmO = {};
@@ -1241,7 +1235,7 @@ cudaError_t launch_tc_gemm(const GroupedProblem &p, const void *workspace, cudaS
                  (reinterpret_cast<uintptr_t>(kp.out) & 15) == 0 && p.P > 0 &&
                  p.P < ((int64_t)1 << 31) &&
                  make_map(&tmO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kp.out, (uint64_t)p.n,
-                          (uint64_t)p.P, 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
+                          (uint64_t)p.P, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
     auto kern = sw ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
     static bool attr_set[2][64] = {};
     int dev = 0;

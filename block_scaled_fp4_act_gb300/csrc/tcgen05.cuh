@@ -67,10 +67,10 @@ __device__ __forceinline__ void bulk_commit()
 {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-// the issuing thread's bulk groups but the newest one have finished reading shared memory
-__device__ __forceinline__ void bulk_wait_read_all_but_one()
+// the issuing thread's bulk groups have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all()
 {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 // the issuing thread's bulk groups have completed (their global writes performed)
 __device__ __forceinline__ void bulk_wait_all()
